@@ -1,0 +1,228 @@
+// Device helpers shared by the kernels: PTX wrappers (mbarrier, bulk copy,
+// acquire/release, programmatic dependent launch, mma.sync), the device
+// weight layout of an expert slot, and bounded waits.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ----------------------------------------------------------------- errors --
+// Device error codes written to the context's error word.
+enum DevErr : uint32_t {
+  DEV_OK = 0,
+  DEV_TIMEOUT_BARRIER = 1,   // smem mbarrier wait gave up
+  DEV_TIMEOUT_FLAG = 2,      // global flag wait gave up
+  DEV_NOT_RESIDENT = 3,      // all-resident mode found a missing key
+  DEV_BAD_PLAN = 4,
+};
+
+// Bounded waits give up after this many nanoseconds of %globaltimer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t code) {
+  atomicCAS(err, 0u, code);
+}
+
+// ------------------------------------------------------------ smem/mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Bulk (non-tensor) TMA copy global -> shared, completing on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ------------------------------------------------- global memory ordering --
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Wait until *flag >= target (acquire); false if the wait gave up.
+__device__ __forceinline__ bool wait_flag_geq(const uint32_t* flag, uint32_t target) {
+  if (ld_acquire_u32(flag) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (ld_acquire_u32(flag) < target) {
+    __nanosleep(64);
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// L2-only loads for data written by other CTAs during this kernel.
+__device__ __forceinline__ uint2 ld_cg_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
+// --------------------------------------------- programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------ tensor cores --
+// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
+                                          const float c[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  // (a & b) | c
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// ------------------------------------------------- device weight layout ----
+// An expert slot holds the same B_x bytes as the canonical format, re-laid
+// out in "blocks" of 32 rows x 32 inputs (one quantisation group per row),
+// 448 bytes each:
+//   bytes [0, 384): three planes of 32 lane words, word (j, lane) at j*128 +
+//     4*lane.  The 96 bits (w0, w1, w2) of lane l = 4g + c hold the 32 codes
+//     of the mma.sync m16n8k16 A fragments of that lane for the block's two
+//     16-row tiles (mt) and two 16-input steps (ks): pair p = mt*8 + ks*4 + r
+//     (r = fragment register 0..3) is (row mt*16 + g + 8*(r&1),
+//     inputs k0 = ks*16 + 2c + 8*(r>>1) and k0+1).  Pairs 0..14 sit in word
+//     p/5, field p%5: the k0 code at bits [3f, 3f+3), the k0+1 code at bits
+//     [16+3f, 16+3f+3).  Pair 15 uses the spare bits: k0 code bit b is bit 15
+//     of word b, k0+1 code bit b is bit 31 of word b.
+//   bytes [384, 448): fp16 scales, row-group g8 (0..7) at 384 + 8*g8 holding
+//     the scales of rows g8, g8+8, g8+16, g8+24.
+// Section order in a slot: gate/up part, for row-block rb (f/32) and group gi
+// (d/32): the Wg block then the Wu block; then the down part, for row-block
+// rb (d/32) and group gi (f/32): the Wd block.
+constexpr int kBlockBytes = 448;
+constexpr int kBlockCodeBytes = 384;
+
+__host__ __device__ __forceinline__ int64_t gu_block_offset(int rb, int gi, int mat, int d) {
+  return ((int64_t)(rb * (d / 32) + gi) * 2 + mat) * kBlockBytes;
+}
+__host__ __device__ __forceinline__ int64_t down_block_offset(int rb, int gi, int d, int f) {
+  return (int64_t)(f / 32) * (d / 32) * 2 * kBlockBytes + (int64_t)(rb * (f / 32) + gi) * kBlockBytes;
+}
+
+// fp16 constants of the code -> value conversion (see dequant_block)
+constexpr uint32_t kMagic = 0x64006400u;     // 1024.0 | 1024.0
+constexpr uint32_t kOne2 = 0x3C003C00u;      // 1.0
+constexpr uint32_t kNeg1028 = 0xE404E404u;   // -1028.0
+constexpr uint32_t kEighth2 = 0x30003000u;   // 0.125
+constexpr uint32_t kNeg132 = 0xD820D820u;    // -132.0
+constexpr uint32_t kSixtyFourth2 = 0x24002400u;  // 1/64
+constexpr uint32_t kNeg20 = 0xCD00CD00u;     // -20.0
+
+// Expand one lane's 96 code bits into 16 fp16x2 A-fragment registers holding
+// q = u - 4 exactly.  OR-ing a 3-bit field into the mantissa of 1024.0 gives
+// 1024 + u * 2^(3f') for field offset 3f' within the mantissa; one fused
+// multiply-add with exact constants maps that to u - 4.
+__device__ __forceinline__ void dequant_block(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t a[16]) {
+  const uint32_t ws[3] = {w0, w1, w2};
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const uint32_t w = ws[j];
+    const uint32_t t = w >> 9;
+    a[j * 5 + 0] = hfma2_u32(lop3_and_or(w, 0x00070007u, kMagic), kOne2, kNeg1028);
+    a[j * 5 + 1] = hfma2_u32(lop3_and_or(w, 0x00380038u, kMagic), kEighth2, kNeg132);
+    a[j * 5 + 2] = hfma2_u32(lop3_and_or(w, 0x01C001C0u, kMagic), kSixtyFourth2, kNeg20);
+    a[j * 5 + 3] = hfma2_u32(lop3_and_or(t, 0x00070007u, kMagic), kOne2, kNeg1028);
+    a[j * 5 + 4] = hfma2_u32(lop3_and_or(t, 0x00380038u, kMagic), kEighth2, kNeg132);
+  }
+  uint32_t v = lop3_and_or(w0 >> 15, 0x00010001u, kMagic);
+  v = lop3_and_or(w1 >> 14, 0x00020002u, v);
+  v = lop3_and_or(w2 >> 13, 0x00040004u, v);
+  a[15] = hfma2_u32(v, kOne2, kNeg1028);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+}  // namespace moe

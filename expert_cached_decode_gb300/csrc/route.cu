@@ -1,0 +1,408 @@
+// Router + top-k + cache plan for one decode layer-call (T <= 16 tokens).
+//
+// Router (workload definition; the pages only fix 10-of-512 routing plus a
+// shared expert, page "一张 RTX 4090 跑千亿模型", §如何做到：三层存储):
+//   l[t,e] = x_t . Wr[e] + b[e] in fp32 from bf16 inputs; the k largest
+//   logits are chosen (ties to the lower id); w_i = softmax over the whole
+//   row restricted to the chosen set and renormalised, which equals a softmax
+//   over the k chosen logits alone.
+//
+// Cache (LRU by (layer, expert), ties to the lower slot id; misses fetched
+// from pinned host RAM, page "单卡5090跑125B 大模型", §2.1 and §7.2):
+//   U = distinct experts of the call (ascending).  Resident keys are hits
+//   and are stamped first; the misses, in ascending expert id, take the
+//   least recently used slots in (stamp, slot id) order.  The LRU order is
+//   kept as an array q (least recent first); one call moves its touched slots
+//   (hits and victims), in slot-id order, to the most recent end.
+//
+// One launch: ceil(E/8) CTAs of 8 warps, one warp per expert row.  The last
+// CTA to finish its logits (arrival counter) selects, forms U and the plan.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// exclusive prefix sum over the 256 threads of the CTA; returns the total
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < kRouteWarps ? s_warp[lane] : 0;
+    int wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < kRouteWarps) s_warp[lane] = wi - wv;
+    if (lane == kRouteWarps - 1) s_warp[kRouteWarps] = wi;
+  }
+  __syncthreads();
+  int r = s_warp[warp] + inc - v;
+  *total = s_warp[kRouteWarps];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
+  pdl_launch_dependents();
+
+  __shared__ uint32_t s_mask[kMaxE / 32];
+  __shared__ int s_word_base[kMaxE / 32];
+  __shared__ int s_sel_id[kMaxDecodeT][kMaxTopK];
+  __shared__ float s_sel_w[kMaxDecodeT][kMaxTopK];
+  __shared__ int s_act[kMaxPicks];
+  __shared__ int s_slot[kMaxPicks];
+  __shared__ int s_hit[kMaxPicks];
+  __shared__ int s_miss_act[kMaxPicks];
+  __shared__ int s_victim[kMaxPicks];
+  __shared__ uint32_t s_bits[kMaxSlots / 32];
+  __shared__ int s_scan[kRouteWarps + 1];
+  __shared__ int s_last, s_n_act, s_n_miss;
+  __shared__ long long s_clock;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, d = a.d, E = a.E, K = a.k;
+
+  // ---- router logits: one warp per expert row, all T tokens -------------
+  const int e = blockIdx.x * kRouteWarps + warp;
+  if (e < E) {
+    float acc[kMaxDecodeT];
+#pragma unroll
+    for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.f;
+    const uint16_t* wrow = a.wr + (size_t)e * d;
+    for (int j = lane * 8; j < d; j += 256) {
+      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + j));
+      float wf[8];
+      wf[0] = bf16_bits_to_float(wv.x & 0xffffu); wf[1] = bf16_bits_to_float(wv.x >> 16);
+      wf[2] = bf16_bits_to_float(wv.y & 0xffffu); wf[3] = bf16_bits_to_float(wv.y >> 16);
+      wf[4] = bf16_bits_to_float(wv.z & 0xffffu); wf[5] = bf16_bits_to_float(wv.z >> 16);
+      wf[6] = bf16_bits_to_float(wv.w & 0xffffu); wf[7] = bf16_bits_to_float(wv.w >> 16);
+#pragma unroll
+      for (int t = 0; t < kMaxDecodeT; ++t) {
+        if (t < T) {
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d + j));
+          float s = acc[t];
+          s = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wf[0], s);
+          s = fmaf(bf16_bits_to_float(xv.x >> 16), wf[1], s);
+          s = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wf[2], s);
+          s = fmaf(bf16_bits_to_float(xv.y >> 16), wf[3], s);
+          s = fmaf(bf16_bits_to_float(xv.z & 0xffffu), wf[4], s);
+          s = fmaf(bf16_bits_to_float(xv.z >> 16), wf[5], s);
+          s = fmaf(bf16_bits_to_float(xv.w & 0xffffu), wf[6], s);
+          s = fmaf(bf16_bits_to_float(xv.w >> 16), wf[7], s);
+          acc[t] = s;
+        }
+      }
+    }
+    const float b = a.bias[e];
+#pragma unroll
+    for (int t = 0; t < kMaxDecodeT; ++t) {
+      if (t < T) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
+      }
+    }
+  }
+
+  // ---- last CTA to arrive does the selection -----------------------------
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(a.cnt, 1u);
+    s_last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  for (int i = threadIdx.x; i < kMaxE / 32; i += kRouteThreads) s_mask[i] = 0;
+  if (threadIdx.x == 0) {
+    *a.cnt = 0;   // ready for the next launch (stream-ordered)
+    s_clock = (a.mode == ROUTE_ONLY) ? 0 : (long long)*a.clock;
+  }
+  __syncthreads();
+
+  // top-k per token, one warp per token
+  const int per_lane = (E + 31) / 32;
+  for (int t = warp; t < T; t += kRouteWarps) {
+    float v[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int id = lane + 32 * i;
+      v[i] = (i < per_lane && id < E) ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float my_v = -INFINITY;
+    int my_id = 0x7fffffff;
+    for (int r = 0; r < K; ++r) {
+      float bv = -INFINITY;
+      int bid = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i) {
+        const int id = lane + 32 * i;
+        if (i < per_lane && id < E && !((taken >> i) & 1u) && beats(v[i], id, bv, bid)) {
+          bv = v[i];
+          bid = id;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+        if (beats(ov, oid, bv, bid)) {
+          bv = ov;
+          bid = oid;
+        }
+      }
+      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+      if (lane == r) {
+        my_v = bv;
+        my_id = bid;
+      }
+    }
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ex = lane < K ? expf(my_v - top) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    int rank = 0;
+    for (int j = 0; j < K; ++j) {
+      const int oid = __shfl_sync(0xffffffffu, my_id, j);
+      rank += (oid < my_id) ? 1 : 0;
+    }
+    if (lane < K) {
+      s_sel_id[t][rank] = my_id;
+      s_sel_w[t][rank] = ex / sum;
+      atomicOr(&s_mask[my_id >> 5], 1u << (my_id & 31));
+    }
+  }
+  __syncthreads();
+
+  // distinct experts U, ascending
+  const int n_words = (E + 31) / 32;
+  if (warp == 0) {
+    const uint32_t m = lane < n_words ? s_mask[lane] : 0u;
+    const int c = __popc(m);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    const int base = inc - c;
+    if (lane < n_words) s_word_base[lane] = base;
+    if (lane == 31) s_n_act = inc;
+    uint32_t mm = m;
+    int pos = base;
+    while (mm) {
+      const int bit = __ffs(mm) - 1;
+      mm &= mm - 1;
+      s_act[pos++] = lane * 32 + bit;
+    }
+  }
+  __syncthreads();
+  const int n_act = s_n_act;
+  Plan* P = a.plan;
+
+  if (a.mode == ROUTE_ONLY) {
+    for (int i = threadIdx.x; i < T * K; i += kRouteThreads) {
+      a.out_idx[i] = s_sel_id[i / K][i % K];
+      a.out_w[i] = s_sel_w[i / K][i % K];
+    }
+    return;
+  }
+
+  // plan: routing part
+  for (int i = threadIdx.x; i < T * K; i += kRouteThreads) {
+    const int id = s_sel_id[i / K][i % K];
+    P->idx[i] = id;
+    P->w[i] = s_sel_w[i / K][i % K];
+    P->pick_act[i] = s_word_base[id >> 5] + __popc(s_mask[id >> 5] & ((1u << (id & 31)) - 1u));
+    if (a.out_idx) {
+      a.out_idx[i] = id;
+      a.out_w[i] = s_sel_w[i / K][i % K];
+    }
+  }
+  for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
+    const int slot = a.table[(size_t)a.layer * E + s_act[i]];
+    s_slot[i] = slot;
+    s_hit[i] = slot >= 0;
+    P->act_expert[i] = s_act[i];
+  }
+  __syncthreads();
+
+  if (a.mode == ROUTE_RESIDENT) {
+    for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
+      int slot = s_slot[i];
+      if (slot < 0) {
+        set_error(a.err, DEV_NOT_RESIDENT);
+        slot = 0;
+      }
+      a.stamp[slot] = s_clock;
+      P->act_slot[i] = slot;
+      P->act_hit[i] = 1;
+    }
+    if (threadIdx.x == 0) {
+      P->n_act = n_act;
+      P->n_miss = 0;
+      P->T = T;
+      P->clock = s_clock;
+      P->token_hits = (int64_t)T * K;
+      P->token_misses = 0;
+      a.stats[ST_CALLS] += 1;
+      a.stats[ST_TOK_HIT] += (int64_t)T * K;
+      a.stats[ST_DIST_HIT] += n_act;
+      *a.clock = s_clock + 1;
+    }
+    return;
+  }
+
+  // ---- ROUTE_PLAN: LRU victims and the next LRU order (no state commit) ---
+  const int C = a.C;
+  const int c_words = (C + 31) / 32;
+  for (int i = threadIdx.x; i < c_words; i += kRouteThreads) s_bits[i] = 0;
+  if (threadIdx.x == 0) {
+    int m = 0;
+    for (int i = 0; i < n_act; ++i)
+      if (!s_hit[i]) s_miss_act[m++] = i;   // ascending expert id
+    s_n_miss = m;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_act; i += kRouteThreads)
+    if (s_hit[i]) atomicOr(&s_bits[s_slot[i] >> 5], 1u << (s_slot[i] & 31));
+  __syncthreads();
+  const int m = s_n_miss;
+
+  // walk q (least recent first) skipping this call's hits: the first m
+  // entries are the victims, the rest keep their order at the front of q_out
+  const int chunk = (C + kRouteThreads - 1) / kRouteThreads;
+  const int lo = min(C, (int)threadIdx.x * chunk), hi = min(C, lo + chunk);
+  int cnt = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int s = a.q_in[i];
+    cnt += !((s_bits[s >> 5] >> (s & 31)) & 1u);
+  }
+  int total;
+  int r = block_exclusive_scan(cnt, s_scan, &total);
+  for (int i = lo; i < hi; ++i) {
+    const int s = a.q_in[i];
+    if (!((s_bits[s >> 5] >> (s & 31)) & 1u)) {
+      if (r < m) s_victim[r] = s;
+      else a.q_out[r - m] = s;
+      ++r;
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < m; j += kRouteThreads)
+    atomicOr(&s_bits[s_victim[j] >> 5], 1u << (s_victim[j] & 31));
+  __syncthreads();
+  // touched slots (hits and victims) in ascending slot id to the recent end
+  const int wchunk = (c_words + kRouteThreads - 1) / kRouteThreads;
+  const int wlo = min(c_words, (int)threadIdx.x * wchunk), whi = min(c_words, wlo + wchunk);
+  int tc = 0;
+  for (int i = wlo; i < whi; ++i) tc += __popc(s_bits[i]);
+  int tr = block_exclusive_scan(tc, s_scan, &total);
+  for (int i = wlo; i < whi; ++i) {
+    uint32_t bits = s_bits[i];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      a.q_out[C - n_act + tr] = i * 32 + b;
+      ++tr;
+    }
+  }
+  for (int j = threadIdx.x; j < m; j += kRouteThreads) {
+    const int ai = s_miss_act[j];
+    const int v = s_victim[j];
+    s_slot[ai] = v;
+    P->miss_expert[j] = s_act[ai];
+    P->miss_slot[j] = v;
+    P->evicted_key[j] = a.owner[v];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
+    P->act_slot[i] = s_slot[i];
+    P->act_hit[i] = s_hit[i];
+  }
+  if (threadIdx.x == 0) {
+    int64_t th = 0;
+    for (int i = 0; i < T * K; ++i) {
+      const int id = s_sel_id[i / K][i % K];
+      const int ai = s_word_base[id >> 5] + __popc(s_mask[id >> 5] & ((1u << (id & 31)) - 1u));
+      th += s_hit[ai];
+    }
+    P->n_act = n_act;
+    P->n_miss = m;
+    P->T = T;
+    P->clock = s_clock;
+    P->token_hits = th;
+    P->token_misses = (int64_t)T * K - th;
+  }
+}
+
+// Applies a ROUTE_PLAN plan once its miss copies are enqueued.
+__global__ void __launch_bounds__(256) commit_kernel(CommitArgs a) {
+  const Plan* P = a.plan;
+  const int n_act = P->n_act, m = P->n_miss;
+  const int64_t clk = P->clock;
+  __shared__ int s_evict;
+  if (threadIdx.x == 0) s_evict = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_act; i += blockDim.x)
+    if (P->act_hit[i]) a.stamp[P->act_slot[i]] = clk;
+  for (int j = threadIdx.x; j < m; j += blockDim.x) {
+    const int old = P->evicted_key[j];
+    if (old >= 0) {
+      a.table[old] = -1;
+      atomicAdd(&s_evict, 1);
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < m; j += blockDim.x) {
+    const int v = P->miss_slot[j];
+    const int key = a.layer * a.E + P->miss_expert[j];
+    a.owner[v] = key;
+    a.table[key] = v;
+    a.stamp[v] = clk;
+  }
+  if (threadIdx.x == 0) {
+    a.stats[ST_CALLS] += 1;
+    a.stats[ST_TOK_HIT] += P->token_hits;
+    a.stats[ST_TOK_MISS] += P->token_misses;
+    a.stats[ST_DIST_HIT] += n_act - m;
+    a.stats[ST_DIST_MISS] += m;
+    a.stats[ST_EVICT] += s_evict;
+    a.stats[ST_MISS_BYTES] += (int64_t)m * a.expert_bytes;
+    *a.clock = clk + 1;
+  }
+}
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+  const int grid = (a.E + kRouteWarps - 1) / kRouteWarps;
+  route_kernel<<<grid, kRouteThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s) {
+  commit_kernel<<<1, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

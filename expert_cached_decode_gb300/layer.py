@@ -1,0 +1,127 @@
+"""Python binding of the C ABI with the same entry-point names.
+
+PyTorch supplies device memory and streams only; every step of the path runs
+in the CUDA library.  Tensors are passed by ``data_ptr()`` and streams by
+their ``cuda_stream`` handle.
+"""
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _abi
+from ._abi import MoeLayerDesc, MoeStats, MoeTrace, check
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, torch.Tensor):
+        if not a.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return ctypes.c_void_p(a.data_ptr())
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("array must be C-contiguous")
+        return ctypes.c_void_p(a.ctypes.data)
+    raise TypeError(f"unsupported buffer type {type(a)}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class MoELayer:
+    """One context of the library: a stack of n_layers MoE layers of one shape.
+
+    router_w: [L, E, d] bf16 (torch bf16 tensor or uint16 array, host or device)
+    router_b: [L, E] fp32 or None
+    shared_q: [L, B_x] uint8 canonical packed shared experts
+    host_pool: [P, B_x] uint8 canonical packed experts in host memory; keep it
+               alive as long as the layer (pinned torch tensors avoid a
+               registration)
+    """
+
+    def __init__(self, d, f, n_experts, top_k, n_layers, router_w, router_b, shared_q, host_pool,
+                 host_pool_entries=0, shared_weight=1.0, group=32):
+        self._lib = _abi.load()
+        self._keep = (router_w, router_b, shared_q, host_pool)
+        desc = MoeLayerDesc(d=d, f=f, n_experts=n_experts, top_k=top_k, n_layers=n_layers, group=group,
+                            router_w=_ptr(router_w), router_b=_ptr(router_b), shared_q=_ptr(shared_q),
+                            host_pool=_ptr(host_pool), host_pool_entries=host_pool_entries,
+                            shared_weight=shared_weight)
+        ctx = ctypes.c_void_p()
+        check(self._lib.moe_layer_create(ctypes.byref(desc), ctypes.byref(ctx)), "moe_layer_create")
+        self.ctx = ctx
+        self.d, self.f, self.E, self.k, self.L = d, f, n_experts, top_k, n_layers
+        self.capacity = 0
+
+    # --- entry points ---------------------------------------------------------
+    def moe_cache_configure(self, capacity, preload_keys=None):
+        keys = None
+        n = 0
+        if preload_keys is not None:
+            keys = np.ascontiguousarray(np.asarray(preload_keys, dtype=np.int32))
+            n = keys.size
+        check(self._lib.moe_cache_configure(self.ctx, int(capacity), _ptr(keys), n), "moe_cache_configure")
+        self.capacity = int(capacity)
+
+    def moe_route_topk(self, layer, x, idx, w, stream=None):
+        T = x.shape[0]
+        check(self._lib.moe_route_topk(self.ctx, layer, _ptr(x), T, _ptr(idx), _ptr(w), _stream(stream)),
+              "moe_route_topk")
+
+    def moe_forward(self, layer, x, y, stream=None, trace=False):
+        """y[T, d] (fp32, device) <- layer-call on x[T, d] (bf16, device).
+        With trace=True returns a dict of host arrays (synchronises)."""
+        T = x.shape[0]
+        if not trace:
+            check(self._lib.moe_forward(self.ctx, layer, _ptr(x), T, _ptr(y), _stream(stream), None),
+                  "moe_forward")
+            return None
+        n = T * self.k
+        bufs = {"idx": np.zeros(n, np.int32), "w": np.zeros(n, np.float32), "slot": np.zeros(n, np.int32),
+                "miss_expert": np.zeros(n, np.int32), "miss_slot": np.zeros(n, np.int32),
+                "evicted_key": np.zeros(n, np.int32)}
+        tr = MoeTrace(**{k: _ptr(v) for k, v in bufs.items()})
+        check(self._lib.moe_forward(self.ctx, layer, _ptr(x), T, _ptr(y), _stream(stream), ctypes.byref(tr)),
+              "moe_forward")
+        m = tr.n_miss
+        return {"idx": bufs["idx"].reshape(T, self.k), "w": bufs["w"].reshape(T, self.k),
+                "slot": bufs["slot"].reshape(T, self.k), "miss_expert": bufs["miss_expert"][:m].copy(),
+                "miss_slot": bufs["miss_slot"][:m].copy(), "evicted_key": bufs["evicted_key"][:m].copy(),
+                "n_distinct": int(tr.n_distinct), "token_hits": int(tr.token_hits),
+                "token_misses": int(tr.token_misses)}
+
+    def moe_sync(self):
+        check(self._lib.moe_sync(self.ctx), "moe_sync")
+
+    def moe_cache_stats(self, per_layer=False):
+        tot = MoeStats()
+        pl = (MoeStats * self.L)() if per_layer else None
+        check(self._lib.moe_cache_stats(self.ctx, ctypes.byref(tot), pl), "moe_cache_stats")
+        if per_layer:
+            return tot.as_dict(), [s.as_dict() for s in pl]
+        return tot.as_dict()
+
+    def moe_cache_export(self):
+        owner = np.zeros(self.capacity, np.int32)
+        stamp = np.zeros(self.capacity, np.int64)
+        check(self._lib.moe_cache_export(self.ctx, _ptr(owner), _ptr(stamp)), "moe_cache_export")
+        return owner, stamp
+
+    def moe_layer_destroy(self):
+        if self.ctx is not None and self.ctx.value:
+            self._lib.moe_layer_destroy(self.ctx)
+        self.ctx = None
+
+    close = moe_layer_destroy
+
+    def __del__(self):
+        try:
+            self.moe_layer_destroy()
+        except Exception:
+            pass

@@ -1,0 +1,168 @@
+/*
+ * moe_gb300.h -- C ABI of the routed-expert FFN step on one GB300 (sm_103a).
+ *
+ * The step (one MoE layer of an offloaded-MoE serving engine, as described in
+ * the blog posts "一张 RTX 4090 跑千亿模型，Strata 实测 155 tok/s",
+ * §如何做到：三层存储, and "单卡5090跑125B 大模型：Strata 把服务器级 MoE 拉进普通 PC",
+ * §2.1-§2.3):
+ *   1. router: logits l = x.Wr^T + b, softmax over all E experts, the k largest
+ *      logits chosen (ties to the lower id), weights renormalised over the k;
+ *   2. expert cache: each distinct (layer, expert) of the call is looked up in
+ *      a fixed-capacity VRAM slot pool; misses are copied from pinned host
+ *      memory (LRU by (layer, expert), ties to the lower slot id);
+ *   3. SwiGLU experts over 3-bit group-quantised weights,
+ *      E(x) = Wd.(silu(Wg.x) * (Wu.x)), for every distinct expert once for all
+ *      tokens routed to it (a verify batch shares one fetch, §2.3);
+ *   4. combine y[t] = sum_i w[t,i] E_idx[t,i](x_t) + shared_weight * E_shared(x_t).
+ * The pages give the structure (512 routed experts, top-10, one shared
+ * expert, 48 layers, hits/lookups per token pick); the formulas and the
+ * weight format are the workload definition's.
+ *
+ * Conventions for every entry point:
+ *   - Every call returns a moe_status; nothing crosses the ABI as an
+ *     exception.  moe_last_error() gives a thread-local message for the last
+ *     failing call on the calling thread.
+ *   - "device" pointers are CUDA device (or managed) memory of the current
+ *     device; "host" pointers are CPU memory.
+ *   - Streams are cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Calls on one context must be serialised by the caller.
+ *   - The library never frees caller memory.
+ *
+ * Canonical packed expert (host pool, shared experts), bytes in this order:
+ *   Wg codes [f][d/32][12 B], Wu codes [f][d/32][12 B], Wd codes [d][f/32][12 B],
+ *   Wg scales [f][d/32] fp16, Wu scales [f][d/32] fp16, Wd scales [d][f/32] fp16.
+ *   In a 12-byte group, weight i (0..31 along the input dimension) is the 3-bit
+ *   field u at bits [3i, 3i+3) of the 96-bit little-endian integer; the weight
+ *   is (u - 4) * scale.  Size B_x = 3*d*f*3/8 + 3*d*f/32*2 bytes
+ *   (2,064,384 B at d=2048, f=768).  The library keeps its own device layout
+ *   in the slot pool; a miss copies B_x bytes and re-lays them out on the GPU.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_ctx moe_ctx; /* opaque, library-owned */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* bad pointer, size, shape or layer index */
+  MOE_ERR_OOM = -2,           /* device or host allocation failed */
+  MOE_ERR_CUDA = -3,          /* a CUDA call failed (message has the CUDA error) */
+  MOE_ERR_HOST_PIN = -4,      /* the host pool could not be pinned/registered */
+  MOE_ERR_TIMEOUT = -5,       /* a bounded device-side wait gave up; context reset */
+  MOE_ERR_STATE = -6,         /* call out of order (e.g. forward before configure) */
+  MOE_ERR_UNIMPLEMENTED = -7  /* shape or mode this build does not support */
+} moe_status;
+
+/* Shapes and weights of one MoE stack (n_layers layers of one shape).
+ * Supported shapes: group == 32, d % 256 == 0, f % 64 == 0, f <= 1024,
+ * 2 <= top_k <= 16, top_k < n_experts <= 1024. */
+typedef struct {
+  int32_t d;               /* hidden size */
+  int32_t f;               /* expert intermediate size */
+  int32_t n_experts;       /* routed experts per layer (E) */
+  int32_t top_k;           /* routed experts per token (k) */
+  int32_t n_layers;        /* L */
+  int32_t group;           /* quantisation group, must be 32 */
+  const void* router_w;    /* [L][E][d] bf16, host or device; copied at create */
+  const float* router_b;   /* [L][E] fp32, host or device, or NULL (zero bias) */
+  const void* shared_q;    /* [L] canonical packed shared experts, host or device; copied */
+  const void* host_pool;   /* [P] canonical packed experts, HOST memory owned by the
+                              caller; must stay valid until moe_layer_destroy.  If it
+                              is not page-locked the library registers it
+                              (cudaHostRegister) and unregisters it at destroy. */
+  int64_t host_pool_entries; /* P; identity (l, e) reads entry (l*E + e) mod P;
+                                0 means P = L*E (one entry per identity) */
+  float shared_weight;     /* weight of the shared expert in the combine (1.0) */
+} moe_layer_desc;
+
+/* Cumulative counters since the last moe_cache_configure.  A token pick is a
+ * hit iff its (layer, expert) was resident when the layer-call began ("hits /
+ * lookups" per pick, page "单卡5090跑125B 大模型", §7.2); shared experts are not
+ * counted, so token_hits + token_misses = k * tokens per layer-call. */
+typedef struct {
+  int64_t layer_calls;
+  int64_t token_hits;
+  int64_t token_misses;
+  int64_t distinct_hits;   /* distinct (layer, expert) per layer-call */
+  int64_t distinct_misses;
+  int64_t evictions;       /* misses whose victim slot held a key */
+  int64_t miss_bytes;      /* bytes copied host -> device for misses */
+} moe_stats;
+
+/* Optional per-call record (host buffers owned by the caller, capacity T*k
+ * entries each unless noted).  Passing a trace makes moe_forward synchronise
+ * with the stream before returning. */
+typedef struct {
+  int32_t* idx;            /* [T][k] routed expert ids, ascending per token */
+  float* w;                /* [T][k] renormalised routing weights */
+  int32_t* slot;           /* [T][k] cache slot used by each pick */
+  int32_t* miss_expert;    /* [<=T*k] missed expert ids, ascending */
+  int32_t* miss_slot;      /* [<=T*k] victim slot of each miss */
+  int32_t* evicted_key;    /* [<=T*k] key (l*E+e) the victim held, -1 if empty */
+  int32_t n_miss;          /* out: number of misses */
+  int32_t n_distinct;      /* out: distinct routed experts of the call */
+  int64_t token_hits;      /* out */
+  int64_t token_misses;    /* out */
+} moe_trace;
+
+/* Create a context: copies router weights, bias and shared experts to the
+ * device (re-laid out), pins or registers the host pool.  *out receives the
+ * context.  Errors: INVALID_ARG (shapes, NULL pointers), OOM, HOST_PIN, CUDA. */
+moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out);
+
+/* Size the expert cache to capacity_slots (each B_x bytes of device memory)
+ * and preload the keys preload_keys[0..n_preload) (key = l*E + e, strictly
+ * ascending) into slots 0, 1, ... from the host pool.  Resets the LRU state,
+ * the logical clock and the counters.  When every key of the stack is
+ * preloaded no miss can occur and moe_forward never waits on the host.
+ * Synchronous.  Errors: INVALID_ARG (capacity < k*16 distinct picks of one
+ * call, n_preload > capacity, unsorted keys), OOM, CUDA. */
+moe_status moe_cache_configure(moe_ctx* ctx, int64_t capacity_slots,
+                               const int32_t* preload_keys, int64_t n_preload);
+
+/* Router only: idx[T][k] (ascending expert id) and w[T][k] for tokens
+ * x[T][d] (bf16, device) at layer `layer`.  idx and w are device buffers.
+ * Asynchronous on `stream`; does not touch the cache.  1 <= T <= 16. */
+moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T,
+                          int32_t* idx, float* w, void* stream);
+
+/* One layer-call: route, look up / fill the cache, run the experts and write
+ * y[T][d] (fp32, device).  x[T][d] bf16 (device).  1 <= T <= 16 uses the
+ * decode path; larger T (up to 16,384) the prefill path.  Asynchronous on
+ * `stream` when every key is resident (see moe_cache_configure); otherwise the
+ * host waits for the routing kernel, issues the miss copies on a side stream
+ * and joins it with an event before the experts run.  On error the cache
+ * state is unchanged.  `trace` may be NULL. */
+moe_status moe_forward(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T,
+                       float* y, void* stream, moe_trace* trace);
+
+/* Wait for all work of the context and report a deferred device error
+ * (MOE_ERR_TIMEOUT if a bounded device wait gave up). */
+moe_status moe_sync(moe_ctx* ctx);
+
+/* Counters (synchronises).  per_layer may be NULL or point to n_layers
+ * entries that receive the per-layer split. */
+moe_status moe_cache_stats(moe_ctx* ctx, moe_stats* total, moe_stats* per_layer);
+
+/* Copy the LRU state to host buffers: owner[C] (key or -1) and stamp[C]
+ * (logical clock of the last use, -1 never used).  Synchronises. */
+moe_status moe_cache_export(moe_ctx* ctx, int32_t* owner, int64_t* stamp);
+
+/* Free every library-owned resource.  NULL is accepted. */
+void moe_layer_destroy(moe_ctx* ctx);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

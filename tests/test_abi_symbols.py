@@ -1,0 +1,61 @@
+"""The C-ABI library loads and exports every entry point include/*.h declares
+(no compute calls: this runs without a GPU)."""
+
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(moe_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from expert_cached_decode_gb300 import LIB_PATH, build_library
+    if not os.path.exists(LIB_PATH):
+        build_library()
+    return LIB_PATH
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    names = _declared()
+    assert names
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert names <= exported
+
+
+def test_binding_names_match_header():
+    from expert_cached_decode_gb300 import ENTRY_POINTS
+    assert set(ENTRY_POINTS) == _declared()
+
+
+def test_null_arguments_are_rejected_without_a_gpu(lib_path):
+    from expert_cached_decode_gb300 import _abi
+    L = _abi.load()
+    assert L.moe_layer_create(None, None) == -1
+    assert b"NULL" in L.moe_last_error()
+    assert L.moe_forward(None, 0, None, 1, None, None, None) == -1
+    L.moe_layer_destroy(None)
