@@ -25,7 +25,7 @@ MARGIN_DELTA = 1e-3  # minimum fp64 gap between the k-th and (k+1)-th router log
 
 # Zipf bias scale, calibrated once for the T=5 verify stack (95% +- 1% token
 # hit rate in the measured pass) and reused for the T=16 stack.
-BIAS_LAMBDA = 0.6
+BIAS_LAMBDA = 0.6062
 
 
 @dataclass(frozen=True)
