@@ -147,6 +147,71 @@ def build_decode_layer(calls, seed_cfg=2):
     return s, layer, xs
 
 
+PREFILL_FLOPS_PER_TOKEN = 11 * 3 * 2 * 2048 * 768          # (k+1) experts x 3 matrices x 2 d f
+ROUTER_FLOPS_PER_TOKEN = 2 * 2048 * 512
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured (bf16 burst; fp16 dense rate is the same)"
+    return 1900.0, "fallback"
+
+
+def run_prefill(steps, warmup, sweep=(4096, 6144, 8192, 12288, 16384)):
+    """12,288-token prefill chunk at one layer (all 512 experts resident) and
+    the chunk-size sweep: tokens/s and tensor-core FLOP rate of the whole call."""
+    import torch
+    from moe_inputs import synth
+    from expert_cached_decode_gb300.layer import MoELayer
+    s = synth(5)
+    wl = s.wl
+    wr, _, b = s.router(0)
+    shared = np.stack([s.shared_packed(0)])
+    pool = torch.empty((wl.keys, s.B), dtype=torch.uint8, pin_memory=True)
+    pv = pool.numpy()
+    for e in range(wl.keys):
+        s.expert_packed(e, out=pv[e])
+    layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, 1, wr.reshape(1, wl.n_experts, wl.d),
+                     b.reshape(1, -1), shared, pool)
+    layer.moe_cache_configure(wl.capacity, np.arange(wl.keys))
+    peak, src = tensor_peak()
+    out = {"workload": "prefill-chunk: one layer, T tokens bf16 N(0,1), top-10/512 + shared, all experts resident",
+           "flops_per_token": PREFILL_FLOPS_PER_TOKEN, "router_flops_per_token": ROUTER_FLOPS_PER_TOKEN,
+           "peak_tflops": peak, "peak_source": src, "sweep": []}
+    stream = torch.cuda.Stream()
+    for T in sweep:
+        xb = s.tokens_many(0, [T], T=T)[0]
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                layer.moe_forward(0, x, y)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                layer.moe_forward(0, x, y)
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        tflops = PREFILL_FLOPS_PER_TOKEN * T / (ms / 1e3) / 1e12
+        out["sweep"].append({"T": T, "ms": ms, "tokens_per_s": T / (ms / 1e3), "tflops": tflops,
+                             "frac": tflops / peak})
+    layer.moe_sync()
+    layer.close()
+    main = [r for r in out["sweep"] if r["T"] == 12288]
+    if main:
+        out["tokens_per_s"] = main[0]["tokens_per_s"]
+        out["roofline"] = {"bound": "tensor", "achieved": main[0]["tflops"], "peak": peak, "unit": "TFLOP/s",
+                           "frac": main[0]["frac"],
+                           "note": "whole prefill call (router GEMM, top-k, sort, gather, gate/up and down "
+                                   "grouped GEMMs) against the expert FLOPs T*103,809,024"}
+    return out
+
+
 def cpu_oracle_sample(n_calls, threads=1):
     """Time the fp64 oracle on the first n_calls of the decode stream in a
     child process with BLAS limited to `threads`."""
@@ -320,6 +385,11 @@ def run_gpu(args):
             "clocks": clk.summary(local),
             "cache": {"token_hits": stats["token_hits"], "token_misses": stats["token_misses"]},
         }
+        if args.prefill:
+            try:
+                line["prefill"] = run_prefill(args.prefill_steps, 3)
+            except Exception as ex:   # reported, not hidden
+                line["prefill"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline:
             n = args.cpu_calls
             r = cpu_oracle_sample(n)
@@ -341,6 +411,8 @@ def main():
     ap.add_argument("--cpu-calls", type=int, default=12)
     ap.add_argument("--ref-calls", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true", help="also time the 12,288-token prefill chunk and sweep")
+    ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--calls", type=int, default=CALLS,
                     help="calls per step (the workload is 10,000; smaller only for profiling)")
     args = ap.parse_args()

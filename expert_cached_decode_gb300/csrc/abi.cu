@@ -11,6 +11,7 @@
 //                        the side stream's event -> commit kernel (LRU state,
 //                        counters) -> expert kernel.  Nothing of the cache
 //                        state changes unless every copy was enqueued.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -86,6 +87,21 @@ struct moe_ctx {
   uint32_t* done = nullptr;
   uint32_t* err = nullptr;
   int max_exp = 0;
+  // prefill scratch (allocated on first use, sized for kMaxPrefillT tokens)
+  float* p_logits = nullptr;
+  int32_t* p_idx = nullptr;
+  float* p_w = nullptr;
+  int32_t* p_counts = nullptr;
+  uint16_t* p_xg = nullptr;      // [T*(k+1)][d] fp16, expert-sorted activations
+  uint16_t* p_hg = nullptr;      // [T*(k+1)][f] fp16
+  int32_t* p_perm = nullptr;
+  float* p_wsort = nullptr;
+  int32_t* p_cursor = nullptr;
+  int32_t* p_group_slot = nullptr;
+  PrefillTile* p_tiles_gu = nullptr;
+  PrefillTile* p_tiles_dn = nullptr;
+  int32_t* p_ntiles = nullptr;
+  int64_t p_max_tiles = 0;
   // miss path
   uint8_t* staging = nullptr;
   int staging_n = 0;
@@ -94,6 +110,43 @@ struct moe_ctx {
 };
 
 extern "C" const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+constexpr int kMaxPrefillT = 16384;
+
+// ---- TMA tensor maps (driver entry point fetched through the runtime) -----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major [rows][cols] 16-bit tensor, box = 64 columns x box_rows rows,
+// 128-byte swizzle.
+static moe_status make_tmap_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                               bool bf16) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MOE_OK;
+}
 
 static bool is_device_ptr(const void* p) {
   cudaPointerAttributes at;
@@ -272,6 +325,19 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->counters);
   cudaFree(c->err);
   cudaFree(c->staging);
+  cudaFree(c->p_logits);
+  cudaFree(c->p_idx);
+  cudaFree(c->p_w);
+  cudaFree(c->p_counts);
+  cudaFree(c->p_xg);
+  cudaFree(c->p_hg);
+  cudaFree(c->p_perm);
+  cudaFree(c->p_wsort);
+  cudaFree(c->p_cursor);
+  cudaFree(c->p_group_slot);
+  cudaFree(c->p_tiles_gu);
+  cudaFree(c->p_tiles_dn);
+  cudaFree(c->p_ntiles);
   if (c->side) cudaStreamDestroy(c->side);
   if (c->ev_route) cudaEventDestroy(c->ev_route);
   if (c->ev_copy) cudaEventDestroy(c->ev_copy);
@@ -401,11 +467,70 @@ static RouteArgs route_args(moe_ctx* c, int layer, const void* x, int T, int mod
   return ra;
 }
 
+static moe_status ensure_prefill_scratch(moe_ctx* c) {
+  if (c->p_logits) return MOE_OK;
+  CUDA_TRY(cudaMalloc(&c->p_logits, (size_t)kMaxPrefillT * c->E * sizeof(float)));
+  CUDA_TRY(cudaMalloc(&c->p_idx, (size_t)kMaxPrefillT * c->k * sizeof(int32_t)));
+  CUDA_TRY(cudaMalloc(&c->p_w, (size_t)kMaxPrefillT * c->k * sizeof(float)));
+  CUDA_TRY(cudaMalloc(&c->p_counts, (size_t)(c->E + 1) * sizeof(int32_t)));
+  return MOE_OK;
+}
+
+static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
+  if (c->p_xg) return MOE_OK;
+  const int64_t rows = (int64_t)kMaxPrefillT * (c->k + 1);
+  c->p_max_tiles = (int64_t)(c->E + 1 + (rows + kPrefillBN - 1) / kPrefillBN);
+  CUDA_TRY(cudaMalloc(&c->p_xg, (size_t)rows * c->d * sizeof(uint16_t)));
+  CUDA_TRY(cudaMalloc(&c->p_hg, (size_t)rows * c->f * sizeof(uint16_t)));
+  CUDA_TRY(cudaMalloc(&c->p_perm, (size_t)rows * sizeof(int32_t)));
+  CUDA_TRY(cudaMalloc(&c->p_wsort, (size_t)rows * sizeof(float)));
+  CUDA_TRY(cudaMalloc(&c->p_cursor, (size_t)c->E * sizeof(int32_t)));
+  CUDA_TRY(cudaMalloc(&c->p_group_slot, (size_t)(c->E + 1) * sizeof(int32_t)));
+  CUDA_TRY(cudaMalloc(&c->p_tiles_gu, (size_t)c->p_max_tiles * (c->f / 128) * sizeof(PrefillTile)));
+  CUDA_TRY(cudaMalloc(&c->p_tiles_dn, (size_t)c->p_max_tiles * (c->d / 128) * sizeof(PrefillTile)));
+  CUDA_TRY(cudaMalloc(&c->p_ntiles, 2 * sizeof(int32_t)));
+  return MOE_OK;
+}
+
+// Router logits (tcgen05) + top-k for T tokens; idx/w device outputs.
+static moe_status prefill_route(moe_ctx* c, int layer, const void* x, int T, int32_t* idx, float* w,
+                                int32_t* counts, cudaStream_t s) {
+  moe_status st = ensure_prefill_scratch(c);
+  if (st != MOE_OK) return st;
+  CUtensorMap ta, tb;
+  st = make_tmap_2d(&ta, c->router_w + (size_t)layer * c->E * c->d, c->E, c->d, 128, true);
+  if (st != MOE_OK) return st;
+  st = make_tmap_2d(&tb, x, T, c->d, 256, true);
+  if (st != MOE_OK) return st;
+  RouterGemmArgs ga{};
+  ga.bias = c->router_b + (size_t)layer * c->E;
+  ga.logits = c->p_logits;
+  ga.T = T;
+  ga.E = c->E;
+  ga.d = c->d;
+  ga.err = c->err;
+  CUDA_TRY(launch_router_gemm(ta, tb, ga, s, c->num_sms));
+  PrefillTopkArgs ka{};
+  ka.logits = c->p_logits;
+  ka.idx = idx;
+  ka.w = w;
+  ka.counts = counts;
+  ka.T = T;
+  ka.E = c->E;
+  ka.k = c->k;
+  CUDA_TRY(launch_prefill_topk(ka, s));
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_route_topk(moe_ctx* c, int32_t layer, const void* x, int32_t T, int32_t* idx,
                                      float* w, void* stream) {
-  moe_status st = check_common(c, layer, x, T, kMaxDecodeT);
+  moe_status st = check_common(c, layer, x, T, kMaxPrefillT);
   if (st != MOE_OK) return st;
   if (!idx || !w) return fail(MOE_ERR_INVALID_ARG, "NULL output");
+  if (T > kMaxDecodeT) {
+    if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    return prefill_route(c, layer, x, T, idx, w, nullptr, static_cast<cudaStream_t>(stream));
+  }
   RouteArgs ra = route_args(c, layer, x, T, ROUTE_ONLY);
   ra.out_idx = idx;
   ra.out_w = w;
@@ -460,17 +585,103 @@ static moe_status fill_trace(moe_ctx* c, cudaStream_t s, int T, moe_trace* tr) {
   return MOE_OK;
 }
 
+// Prefill layer-call (T > 16, every key resident): routing on the tensor
+// cores, counting sort by expert, gather, gate/up and down grouped GEMMs.
+static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, float* y, cudaStream_t s,
+                                  moe_trace* trace) {
+  if (!c->all_resident)
+    return fail(MOE_ERR_UNIMPLEMENTED, "prefill (T > %d) needs every expert resident in this build", kMaxDecodeT);
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
+    return fail(MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  moe_status st = ensure_prefill_scratch(c);
+  if (st == MOE_OK) st = ensure_prefill_ffn_scratch(c);
+  if (st != MOE_OK) return st;
+  const int rows = T * (c->k + 1);
+  CUDA_TRY(cudaMemsetAsync(c->p_counts, 0, (size_t)(c->E + 1) * sizeof(int32_t), s));
+  st = prefill_route(c, layer, x, T, c->p_idx, c->p_w, c->p_counts, s);
+  if (st != MOE_OK) return st;
+  PrefillPlanArgs pa{};
+  pa.counts = c->p_counts;
+  pa.cursor = c->p_cursor;
+  pa.group_slot = c->p_group_slot;
+  pa.tiles_gu = c->p_tiles_gu;
+  pa.tiles_dn = c->p_tiles_dn;
+  pa.n_tiles = c->p_ntiles;
+  pa.table = c->table;
+  pa.stamp = c->stamp;
+  pa.clock = c->clock;
+  pa.stats = c->stats + (size_t)layer * ST_N;
+  pa.T = T;
+  pa.E = c->E;
+  pa.k = c->k;
+  pa.d = c->d;
+  pa.f = c->f;
+  pa.layer = layer;
+  pa.err = c->err;
+  CUDA_TRY(launch_prefill_plan(pa, s));
+  PrefillScatterArgs sa{};
+  sa.idx = c->p_idx;
+  sa.w = c->p_w;
+  sa.cursor = c->p_cursor;
+  sa.perm = c->p_perm;
+  sa.wsort = c->p_wsort;
+  sa.T = T;
+  sa.k = c->k;
+  sa.shared_weight = c->shared_weight;
+  CUDA_TRY(launch_prefill_scatter(sa, s));
+  CUDA_TRY(launch_prefill_gather(static_cast<const uint16_t*>(x), c->p_perm, c->p_xg, rows, c->d, s));
+  CUDA_TRY(cudaMemsetAsync(y, 0, (size_t)T * c->d * sizeof(float), s));
+  CUtensorMap tx, th;
+  st = make_tmap_2d(&tx, c->p_xg, rows, c->d, kPrefillBN, false);
+  if (st == MOE_OK) st = make_tmap_2d(&th, c->p_hg, rows, c->f, kPrefillBN, false);
+  if (st != MOE_OK) return st;
+  PrefillGemmArgs ga{};
+  ga.slots = c->slots;
+  ga.shared_expert = c->shared + (size_t)layer * c->B;
+  ga.expert_bytes = c->B;
+  ga.group_slot = c->p_group_slot;
+  ga.tiles_gu = c->p_tiles_gu;
+  ga.tiles_dn = c->p_tiles_dn;
+  ga.n_tiles = c->p_ntiles;
+  ga.hg = c->p_hg;
+  ga.perm = c->p_perm;
+  ga.wsort = c->p_wsort;
+  ga.y = y;
+  ga.E = c->E;
+  ga.d = c->d;
+  ga.f = c->f;
+  ga.err = c->err;
+  CUDA_TRY(launch_prefill_gate_up(tx, ga, s, c->num_sms));
+  CUDA_TRY(launch_prefill_down(th, ga, s, c->num_sms));
+  if (trace) {
+    const int n = T * c->k;
+    std::vector<int32_t> gslot(c->E + 1);
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (trace->idx) CUDA_TRY(cudaMemcpy(trace->idx, c->p_idx, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    if (trace->w) CUDA_TRY(cudaMemcpy(trace->w, c->p_w, n * sizeof(float), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemcpy(gslot.data(), c->p_group_slot, (c->E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    std::vector<int32_t> idx(n);
+    CUDA_TRY(cudaMemcpy(idx.data(), c->p_idx, n * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    int distinct = 0;
+    for (int e = 0; e < c->E; ++e) distinct += gslot[e] >= 0;
+    if (trace->slot)
+      for (int i = 0; i < n; ++i) trace->slot[i] = gslot[idx[i]];
+    trace->n_miss = 0;
+    trace->n_distinct = distinct;
+    trace->token_hits = n;
+    trace->token_misses = 0;
+  }
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int32_t T, float* y, void* stream,
                                   moe_trace* trace) {
-  moe_status st = check_common(c, layer, x, T, kMaxDecodeT);
-  if (st != MOE_OK) {
-    if (c && T > kMaxDecodeT && T <= 16384)
-      return fail(MOE_ERR_UNIMPLEMENTED, "prefill path (T > %d) not available in this build", kMaxDecodeT);
-    return st;
-  }
+  moe_status st = check_common(c, layer, x, T, kMaxPrefillT);
+  if (st != MOE_OK) return st;
   if (!c->configured) return fail(MOE_ERR_STATE, "moe_cache_configure must come first");
   if (!y) return fail(MOE_ERR_INVALID_ARG, "NULL output");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T > kMaxDecodeT) return prefill_forward(c, layer, x, T, y, s, trace);
   FfnArgs fa = ffn_args(c, layer, x, T, y);
   if (c->all_resident) {
     RouteArgs ra = route_args(c, layer, x, T, ROUTE_RESIDENT);

@@ -103,9 +103,87 @@ struct FfnArgs {
   int grid;
 };
 
+struct RouterGemmArgs {
+  const float* bias;   // [E]
+  float* logits;       // [T][E]
+  int T, E, d;
+  uint32_t* err;
+};
+
+struct PrefillTopkArgs {
+  const float* logits; // [T][E]
+  int32_t* idx;        // [T][k]
+  float* w;            // [T][k]
+  int32_t* counts;     // [E] picks per expert (atomic), or NULL
+  int T, E, k;
+};
+
+constexpr int kPrefillBN = 256;   // tokens per prefill GEMM tile (max)
+
+struct PrefillTile {
+  int group;   // routed expert id, or E for the shared expert
+  int row0;    // first row in the expert-sorted token order
+  int nlen;    // rows in this tile (<= kPrefillBN)
+  int m;       // 128-row block of the weight matrix
+};
+
+struct PrefillPlanArgs {
+  const int32_t* counts;   // [E] picks per expert
+  int32_t* cursor;         // [E] scatter cursors (out)
+  int32_t* group_slot;     // [E+1] slot of each routed expert with tokens (out)
+  PrefillTile* tiles_gu;
+  PrefillTile* tiles_dn;
+  int32_t* n_tiles;        // [2] (out)
+  const int32_t* table;
+  int64_t* stamp;
+  int64_t* clock;
+  int64_t* stats;
+  int T, E, k, d, f, layer;
+  uint32_t* err;
+};
+
+struct PrefillScatterArgs {
+  const int32_t* idx;
+  const float* w;
+  int32_t* cursor;
+  int32_t* perm;           // [T*k + T] token of each sorted row
+  float* wsort;            // [T*k + T] combine weight of each sorted row
+  int T, k;
+  float shared_weight;
+};
+
+struct PrefillGemmArgs {
+  const uint8_t* slots;
+  const uint8_t* shared_expert;
+  int64_t expert_bytes;
+  const int32_t* group_slot;
+  const PrefillTile* tiles_gu;
+  const PrefillTile* tiles_dn;
+  const int32_t* n_tiles;
+  uint16_t* hg;            // [rows][f] fp16 (gate/up output, down input)
+  const int32_t* perm;
+  const float* wsort;
+  float* y;                // [T][d]
+  int E, d, f;
+  uint32_t* err;
+};
+
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
+}  // namespace moe
+
+#include <cuda.h>
+namespace moe {
+cudaError_t launch_router_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const RouterGemmArgs& a,
+                               cudaStream_t s, int num_sms);
+cudaError_t launch_prefill_topk(const PrefillTopkArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_plan(const PrefillPlanArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_scatter(const PrefillScatterArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16_t* xg, int rows, int d,
+                                  cudaStream_t s);
+cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid);
+cudaError_t launch_prefill_down(const CUtensorMap& tmH, const PrefillGemmArgs& a, cudaStream_t s, int grid);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl, int num_sms);
 
 }  // namespace moe

@@ -1,0 +1,492 @@
+// Prefill expert FFN (T up to 16,384 tokens): grouped GEMMs on tcgen05.
+//
+// The chunk's token picks are counting-sorted by expert (the shared expert
+// takes every token, as the last group), the activations gathered to fp16 in
+// that order, and two grouped GEMMs run every expert once for all its tokens
+// (a 12,288-token chunk is the pages' single-GPU prefill size, page
+// "一张 RTX 4090 跑千亿模型", §加个草稿层):
+//   gate/up:  [g|u]^T[f x n_e] = [Wg|Wu][f x d] . X_e^T   -> h = silu(g)*u (fp16)
+//   down:     o^T[d x n_e] = Wd[d x f] . H_e^T            -> y[t] += w[t,e] * o[t]
+// Weights sit on the MMA M side (128 rows per tile), tokens on N (<= 256 per
+// tile, rounded up to 16).  Producer warps expand the 3-bit blocks of the
+// slot to fp16 RN(q * scale) straight into the 128-byte-swizzled K-major
+// operand tile; the token tile comes by TMA; one thread issues tcgen05.mma
+// into tensor memory; four epilogue warps read the accumulators back.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ plan ---
+// One CTA: expert offsets, scatter cursors, tile lists, slot lookup, stamps.
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillPlanArgs a) {
+  __shared__ int s_off[kMaxE + 2];
+  __shared__ int s_nt[kMaxE + 2];
+  __shared__ int s_warp[32];
+  __shared__ int s_total[2];
+  const int E = a.E, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_groups = E + 1;   // routed experts, then the shared expert
+  // exclusive scan of counts and of n-tiles (n_groups <= 1025 -> two rounds)
+  for (int pass = 0; pass < 2; ++pass) {
+    int carry = 0;
+    for (int base = 0; base < n_groups; base += 1024) {
+      const int g = base + tid;
+      int n = 0;
+      if (g < n_groups) n = (g < E) ? a.counts[g] : a.T;
+      int v = pass == 0 ? n : (n + kPrefillBN - 1) / kPrefillBN;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+      }
+      if (lane == 31) s_warp[warp] = inc;
+      __syncthreads();
+      if (warp == 0) {
+        const int wv = s_warp[lane];
+        int wi = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, wi, o);
+          if (lane >= o) wi += t;
+        }
+        s_warp[lane] = wi - wv;
+        if (lane == 31) s_total[pass] = wi;
+      }
+      __syncthreads();
+      if (g < n_groups) {
+        const int ex = carry + s_warp[warp] + inc - v;
+        if (pass == 0) s_off[g] = ex; else s_nt[g] = ex;
+      }
+      carry += s_total[pass];
+      __syncthreads();
+    }
+    if (tid == 0) {
+      if (pass == 0) s_off[n_groups] = carry; else s_nt[n_groups] = carry;
+    }
+    __syncthreads();
+  }
+  const int n_ntiles = s_nt[n_groups];
+  const int MG = a.f / 128, MD = a.d / 128;
+  for (int g = tid; g < n_groups; g += 1024) {
+    const int off = s_off[g];
+    const int n = s_off[g + 1] - off;
+    if (g < E) a.cursor[g] = off;
+    int slot = -1;
+    if (g < E && n > 0) {
+      slot = a.table[(size_t)a.layer * E + g];
+      if (slot < 0) set_error(a.err, DEV_NOT_RESIDENT);
+      else a.stamp[slot] = *a.clock;
+    }
+    a.group_slot[g] = slot;
+    for (int j = 0; j * kPrefillBN < n; ++j) {
+      const int nt = s_nt[g] + j;
+      PrefillTile tl;
+      tl.group = g;
+      tl.row0 = off + j * kPrefillBN;
+      tl.nlen = min(kPrefillBN, n - j * kPrefillBN);
+      for (int m = 0; m < MG; ++m) {
+        tl.m = m;
+        a.tiles_gu[nt * MG + m] = tl;
+      }
+      for (int m = 0; m < MD; ++m) {
+        tl.m = m;
+        a.tiles_dn[nt * MD + m] = tl;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.n_tiles[0] = n_ntiles * MG;
+    a.n_tiles[1] = n_ntiles * MD;
+    int n_act = 0;
+    for (int g = 0; g < E; ++g) n_act += (s_off[g + 1] > s_off[g]);
+    a.stats[ST_CALLS] += 1;
+    a.stats[ST_TOK_HIT] += (int64_t)a.T * a.k;
+    a.stats[ST_DIST_HIT] += n_act;
+    *a.clock += 1;
+  }
+}
+
+__global__ void prefill_scatter_kernel(PrefillScatterArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int picks = a.T * a.k;
+  if (i < picks) {
+    const int e = a.idx[i];
+    const int pos = atomicAdd(&a.cursor[e], 1);
+    a.perm[pos] = i / a.k;
+    a.wsort[pos] = a.w[i];
+  } else if (i < picks + a.T) {
+    const int t = i - picks;
+    a.perm[picks + t] = t;
+    a.wsort[picks + t] = a.shared_weight;
+  }
+}
+
+// Xg[r] = fp16(x[perm[r]]), one CTA of 256 threads per row (d % 2048 handled by a loop)
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, const int32_t* perm, uint16_t* xg,
+                                                             int d) {
+  const int r = blockIdx.x;
+  const int t = perm[r];
+  const uint16_t* src = x + (size_t)t * d;
+  uint16_t* dst = xg + (size_t)r * d;
+  for (int j = threadIdx.x * 8; j < d; j += 256 * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + j));
+    uint4 o;
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(bf16_bits_to_float(in[q] & 0xffffu), bf16_bits_to_float(in[q] >> 16));
+      out[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    o.x = out[0];
+    o.y = out[1];
+    o.z = out[2];
+    o.w = out[3];
+    *reinterpret_cast<uint4*>(dst + j) = o;
+  }
+}
+
+// ---------------------------------------------------------- grouped GEMMs ---
+namespace pg {
+constexpr int BM = 128, BN = kPrefillBN, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB per weight matrix tile
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int NPROD = 4;               // dequant warps, one 32-row block each
+constexpr int PSTAGES = 3;             // packed-weight staging depth per producer
+constexpr int THREADS = 10 * 32;       // 0 TMA, 1 MMA, 2-5 producers, 6-9 epilogue
+}  // namespace pg
+
+// Expand one 32x32 block (448 B at `bp`, shared memory) into rows
+// [row_base, row_base+32) and k columns [k_base, k_base+32) of a swizzled
+// K-major fp16 tile, as RN(q * scale).
+__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint8_t* tile, int row_base,
+                                                      int k_base) {
+  const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
+  const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
+  const uint2 sc = *reinterpret_cast<const uint2*>(bp + kBlockCodeBytes + (lane >> 2) * 8);
+  const uint32_t s2[4] = {(sc.x & 0xffffu) * 0x10001u, (sc.x >> 16) * 0x10001u, (sc.y & 0xffffu) * 0x10001u,
+                          (sc.y >> 16) * 0x10001u};
+  uint32_t A[16];
+  dequant_block(w0, w1, w2, A);
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const int mt = p >> 3, ks = (p >> 2) & 1, r = p & 3;
+    const int row = row_base + mt * 16 + g + 8 * (r & 1);
+    const int k0 = k_base + ks * 16 + 2 * c + 8 * (r >> 1);
+    uint32_t v;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(A[p]), "r"(s2[2 * mt + (r & 1)]));
+    *reinterpret_cast<uint32_t*>(tile + sw128_offset(row, k0 >> 3) + (k0 & 7) * 2) = v;
+  }
+}
+
+// DOWN = false: gate/up tiles (A = Wg and Wu blocks, two accumulators,
+// SwiGLU epilogue writing Hg).  DOWN = true: down tiles (A = Wd blocks, one
+// double-buffered accumulator, weighted atomic combine into y).
+template <bool DOWN>
+__global__ void __launch_bounds__(pg::THREADS, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, PrefillGemmArgs a) {
+  using namespace pg;
+  constexpr int NMAT = DOWN ? 1 : 2;
+  constexpr int STAGES = DOWN ? 4 : 3;
+  constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
+  constexpr int PCHUNK = NMAT * 2 * kBlockBytes;    // packed bytes per producer per k block
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  constexpr int EPI_BYTES = DOWN ? 32 * BM * 4 : 32 * BM * 2;     // fp32 / fp16 staging
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;
+  uint8_t* pstage = epi + EPI_BYTES;                               // NPROD * PSTAGES * PCHUNK
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pstage + NPROD * PSTAGES * PCHUNK);
+  uint64_t* full_a = bars;
+  uint64_t* full_b = full_a + STAGES;
+  uint64_t* empty = full_b + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* pbar = tempty + 2;                                     // NPROD * PSTAGES
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pbar + NPROD * PSTAGES);
+  __shared__ float s_w[32];
+  __shared__ int s_tok[32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = a.n_tiles[DOWN ? 1 : 0];
+  const int K = DOWN ? a.f : a.d;
+  const int n_kb = K / BK;
+  const PrefillTile* tiles = DOWN ? a.tiles_dn : a.tiles_gu;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_a[i], NPROD);
+      mbar_init(&full_b[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    for (int i = 0; i < NPROD * PSTAGES; ++i) mbar_init(&pbar[i], 1);
+    mbar_init_fence();
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto weights = [&](int group) -> const uint8_t* {
+    return group < a.E ? a.slots + (int64_t)a.group_slot[group] * a.expert_bytes : a.shared_expert;
+  };
+  // packed source of producer p for (tile, kb): contiguous PCHUNK bytes
+  auto psrc = [&](const PrefillTile& tl, int p, int kb) -> const uint8_t* {
+    const int rb = tl.m * 4 + p;
+    if (DOWN) return weights(tl.group) + down_block_offset(rb, 2 * kb, a.d, a.f);
+    return weights(tl.group) + gu_block_offset(rb, 2 * kb, 0, a.d);
+  };
+
+  if (warp == 0) {
+    // ---- token tiles by TMA -------------------------------------------------
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+        const PrefillTile tl = tiles[ti];
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t use = it / STAGES;
+          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            goto done;
+          }
+          uint8_t* st = stages + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_b[s], B_BYTES);
+          tma_load_2d(st + NMAT * A_BYTES, &tmB, kb * BK, tl.row0, &full_b[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue ----------------------------------------------------------
+    if (lane == 0) {
+      uint32_t it = 0, lt = 0;
+      for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
+        const PrefillTile tl = tiles[ti];
+        const int nmma = (tl.nlen + 15) & ~15;
+        const uint32_t idesc = idesc_f16(BM, nmma, 0);
+        const int ab = DOWN ? (lt & 1) : 0;
+        const uint32_t use_b = DOWN ? (lt >> 1) : lt;
+        if (use_b > 0 && !mbar_wait(&tempty[ab], (use_b - 1) & 1)) {
+          set_error(a.err, DEV_TIMEOUT_BARRIER);
+          goto done;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t par = (it / STAGES) & 1;
+          if (!mbar_wait(&full_a[s], par) || !mbar_wait(&full_b[s], par)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            goto done;
+          }
+          tc_fence_after();
+          uint8_t* st = stages + s * STAGE_BYTES;
+          const uint64_t db = smem_desc_sw128(st + NMAT * A_BYTES);
+#pragma unroll
+          for (int mat = 0; mat < NMAT; ++mat) {
+            const uint64_t da = smem_desc_sw128(st + mat * A_BYTES);
+            const uint32_t d_tmem = tmem + (DOWN ? ab * BN : mat * BN);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+          }
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&tfull[ab]);
+      }
+    }
+  } else if (warp < 2 + NPROD) {
+    // ---- weight producers: 3-bit blocks -> fp16 swizzled tiles -------------
+    const int p = warp - 2;
+    uint8_t* my_stage = pstage + p * PSTAGES * PCHUNK;
+    uint64_t* my_bar = pbar + p * PSTAGES;
+    // enumerate (tile, kb) items of this CTA
+    int ti_issue = blockIdx.x, kb_issue = 0;
+    uint32_t n_issued = 0;
+    auto issue_next = [&]() {
+      if (ti_issue >= n_tiles) return;
+      const PrefillTile tl = tiles[ti_issue];
+      const int ps = n_issued % PSTAGES;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&my_bar[ps], PCHUNK);
+        bulk_g2s(my_stage + ps * PCHUNK, psrc(tl, p, kb_issue), PCHUNK, &my_bar[ps]);
+      }
+      ++n_issued;
+      if (++kb_issue == n_kb) {
+        kb_issue = 0;
+        ti_issue += gridDim.x;
+      }
+    };
+    for (int i = 0; i < PSTAGES - 1; ++i) issue_next();
+    uint32_t it = 0;
+    for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+      for (int kb = 0; kb < n_kb; ++kb, ++it) {
+        __syncwarp();
+        issue_next();   // refills the slot consumed two items ago
+        const int ps = it % PSTAGES;
+        if (!mbar_wait(&my_bar[ps], (it / PSTAGES) & 1)) {
+          set_error(a.err, DEV_TIMEOUT_BARRIER);
+          goto done;
+        }
+        const int s = it % STAGES;
+        const uint32_t use = it / STAGES;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+          set_error(a.err, DEV_TIMEOUT_BARRIER);
+          goto done;
+        }
+        uint8_t* st = stages + s * STAGE_BYTES;
+        const uint8_t* src = my_stage + ps * PCHUNK;
+        if (DOWN) {
+          dequant_block_to_tile(src, lane, st, p * 32, 0);
+          dequant_block_to_tile(src + kBlockBytes, lane, st, p * 32, 32);
+        } else {
+          // blocks in order: (g0, Wg), (g0, Wu), (g1, Wg), (g1, Wu)
+          dequant_block_to_tile(src, lane, st, p * 32, 0);
+          dequant_block_to_tile(src + kBlockBytes, lane, st + A_BYTES, p * 32, 0);
+          dequant_block_to_tile(src + 2 * kBlockBytes, lane, st, p * 32, 32);
+          dequant_block_to_tile(src + 3 * kBlockBytes, lane, st + A_BYTES, p * 32, 32);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_a[s]);
+      }
+    }
+  } else {
+    // ---- epilogue: warps 6-9 cover the four 32-lane quarters of TMEM -------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;          // M row of the tile
+    const int et = threadIdx.x - (2 + NPROD) * 32; // 0..127
+    uint32_t lt = 0;
+    for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
+      const PrefillTile tl = tiles[ti];
+      const int ab = DOWN ? (lt & 1) : 0;
+      const uint32_t use_b = DOWN ? (lt >> 1) : lt;
+      if (!mbar_wait(&tfull[ab], use_b & 1)) {
+        set_error(a.err, DEV_TIMEOUT_BARRIER);
+        goto done;
+      }
+      tc_fence_after();
+      const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+      for (int c = 0; c * 32 < tl.nlen; ++c) {
+        const int nrow = min(32, tl.nlen - c * 32);
+        if (!DOWN) {
+          uint32_t rg[32], ru[32];
+          tmem_ld32(tmem + lane_addr + c * 32, rg);
+          tmem_ld32(tmem + lane_addr + BN + c * 32, ru);
+          tmem_ld_wait();
+          __half* eh = reinterpret_cast<__half*>(epi);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
+            eh[j * BM + row] = __float2half_rn(g / (1.f + expf(-g)) * u);
+          }
+          named_bar(1, 128);
+          // 32 token rows x 128 f values (256 B) -> Hg
+          for (int q = et; q < 32 * 16; q += 128) {
+            const int j = q >> 4, ch = q & 15;
+            if (j < nrow) {
+              const uint4 v = *reinterpret_cast<const uint4*>(epi + j * 256 + ch * 16);
+              *reinterpret_cast<uint4*>(a.hg + (size_t)(tl.row0 + c * 32 + j) * a.f + tl.m * BM + ch * 8) = v;
+            }
+          }
+          named_bar(1, 128);
+        } else {
+          if (et < 32) {
+            const int j = et;
+            s_w[j] = j < nrow ? a.wsort[tl.row0 + c * 32 + j] : 0.f;
+            s_tok[j] = j < nrow ? a.perm[tl.row0 + c * 32 + j] : 0;
+          }
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_addr + ab * BN + c * 32, r);
+          tmem_ld_wait();
+          named_bar(1, 128);
+          float* ef = reinterpret_cast<float*>(epi);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ef[j * BM + row] = __uint_as_float(r[j]) * s_w[j];
+          named_bar(1, 128);
+          for (int q = et; q < 32 * 32; q += 128) {
+            const int j = q >> 5, r4 = q & 31;
+            if (j < nrow) {
+              const float4 v = *reinterpret_cast<const float4*>(ef + j * BM + r4 * 4);
+              red_add_v4(a.y + (size_t)s_tok[j] * a.d + tl.m * BM + r4 * 4, v.x, v.y, v.z, v.w);
+            }
+          }
+          named_bar(1, 128);
+        }
+      }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(&tempty[ab]);
+    }
+  }
+done:
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool DOWN>
+static size_t gemm_smem() {
+  constexpr int NMAT = DOWN ? 1 : 2;
+  constexpr int STAGES = DOWN ? 4 : 3;
+  constexpr int STAGE_BYTES = NMAT * pg::A_BYTES + pg::B_BYTES;
+  constexpr int PCHUNK = NMAT * 2 * kBlockBytes;
+  constexpr int EPI_BYTES = DOWN ? 32 * pg::BM * 4 : 32 * pg::BM * 2;
+  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + pg::NPROD * pg::PSTAGES * PCHUNK +
+         (3 * STAGES + 4 + pg::NPROD * pg::PSTAGES) * 8 + 16;
+}
+
+template <bool DOWN>
+static cudaError_t launch_gemm(const CUtensorMap& tmB, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
+  static bool configured = false;
+  const size_t smem = gemm_smem<DOWN>();
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  prefill_gemm_kernel<DOWN><<<grid, pg::THREADS, smem, s>>>(tmB, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_plan(const PrefillPlanArgs& a, cudaStream_t s) {
+  prefill_plan_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_scatter(const PrefillScatterArgs& a, cudaStream_t s) {
+  const int n = a.T * a.k + a.T;
+  prefill_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16_t* xg, int rows, int d,
+                                  cudaStream_t s) {
+  prefill_gather_kernel<<<rows, 256, 0, s>>>(x, perm, xg, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
+  return launch_gemm<false>(tmX, a, s, grid);
+}
+
+cudaError_t launch_prefill_down(const CUtensorMap& tmH, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
+  return launch_gemm<true>(tmH, a, s, grid);
+}
+
+}  // namespace moe

@@ -128,8 +128,9 @@ moe_status moe_cache_configure(moe_ctx* ctx, int64_t capacity_slots,
                                const int32_t* preload_keys, int64_t n_preload);
 
 /* Router only: idx[T][k] (ascending expert id) and w[T][k] for tokens
- * x[T][d] (bf16, device) at layer `layer`.  idx and w are device buffers.
- * Asynchronous on `stream`; does not touch the cache.  1 <= T <= 16. */
+ * x[T][d] (bf16, device, 16-byte aligned) at layer `layer`.  idx and w are
+ * device buffers.  Asynchronous on `stream`; does not touch the cache.
+ * 1 <= T <= 16,384 (T > 16 computes the logits on the tensor cores). */
 moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T,
                           int32_t* idx, float* w, void* stream);
 
