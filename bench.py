@@ -52,6 +52,21 @@ def _dist():
     return ws, rank, local
 
 
+def reduce_max(value, dist, device):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world_size, max_ms):
+    """Units of all ranks over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world_size / (max_ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -326,12 +341,8 @@ def run_gpu(args):
         dist.barrier()
     ms = e0.elapsed_time(e1)
     layer.moe_sync()
-    ms_t = torch.tensor([ms], device="cuda")
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms = float(ms_t.item())
-    tokens = CALLS * args.steps * ws
-    value = tokens / (ms / 1e3)
+    ms = reduce_max(ms, dist, "cuda")
+    value = whole_job_rate(CALLS * args.steps, ws, ms)
     per_call_s = (ms / 1e3) / (CALLS * args.steps)
 
     # end to end: H2D of the step's inputs, the calls, D2H of the outputs
@@ -351,12 +362,9 @@ def run_gpu(args):
         y_host.copy_(y_dev, non_blocking=True)
     e3.record(cur)
     torch.cuda.synchronize()
-    ms_e2e = e2.elapsed_time(e3)
-    t = torch.tensor([ms_e2e], device="cuda")
+    ms_e2e = reduce_max(e2.elapsed_time(e3), dist, "cuda")
     if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-    ms_e2e = float(t.item())
     stats = layer.moe_cache_stats()
 
     if rank == 0:
@@ -380,7 +388,7 @@ def run_gpu(args):
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                          "kernel": "route_kernel + decode_ffn_kernel per call (duration of the whole call)",
                          "alg_bytes_per_launch": ALG_BYTES_PER_CALL, "router_bytes": ROUTER_BYTES},
-            "e2e": {"value": CALLS * args.steps * ws / (ms_e2e / 1e3), "unit": "tokens/s",
+            "e2e": {"value": whole_job_rate(CALLS * args.steps, ws, ms_e2e), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(y_host.numel() * 4)},
             "clocks": clk.summary(local),
             "cache": {"token_hits": stats["token_hits"], "token_misses": stats["token_misses"]},
