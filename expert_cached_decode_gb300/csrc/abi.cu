@@ -39,6 +39,18 @@ static moe_status fail(moe_status st, const char* fmt, ...) {
   return st;
 }
 
+namespace moe {
+moe_status set_last_error(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+}  // namespace moe
+
 #define CUDA_TRY(call)                                                                          \
   do {                                                                                          \
     cudaError_t e_ = (call);                                                                    \

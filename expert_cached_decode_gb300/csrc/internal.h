@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe_gb300.h"
+
 namespace moe {
 
 constexpr int kMaxDecodeT = 16;   // tokens per call on the decode path
@@ -167,6 +169,9 @@ struct PrefillGemmArgs {
   int E, d, f;
   uint32_t* err;
 };
+
+// Records the thread-local message returned by moe_last_error().
+moe_status set_last_error(moe_status st, const char* fmt, ...);
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);

@@ -17,6 +17,9 @@
 //
 // One launch: ceil(E/8) CTAs of 8 warps, one warp per expert row.  The last
 // CTA to finish its logits (arrival counter) selects, forms U and the plan.
+#include <mutex>
+
+#include "moe_gb300.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -405,4 +408,95 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free router: moe_route_topk_noalloc.
+//
+// Its scratch (the logits of up to 16 tokens x 1024 experts and the CTA
+// arrival counter) is a fixed array in the library image, so the call needs
+// no cudaMalloc.  Every GPU that loads the library holds these 64 KiB (+8 KiB)
+// until the process exits.  A zero-bias row serves callers without a bias.
+static __device__ __align__(256) float g_noalloc_logits[kMaxDecodeT * kMaxE];
+static __device__ __align__(256) uint32_t g_noalloc_counter[64];
+static __device__ __align__(256) float g_noalloc_zero_bias[kMaxE];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+
+struct NoallocScratch {
+  float* logits = nullptr;
+  uint32_t* counter = nullptr;
+  float* zero_bias = nullptr;
+};
+std::mutex g_noalloc_mu;
+NoallocScratch g_noalloc[kNoallocMaxDevices];
+
+// Device addresses of the static scratch on the current device, looked up once
+// per device (with that device current) and cached.
+cudaError_t noalloc_scratch(NoallocScratch* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocScratch& s = g_noalloc[dev];
+  if (!s.logits) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_logits)) != cudaSuccess) return e;
+    void* q = nullptr;
+    if ((e = cudaGetSymbolAddress(&q, g_noalloc_counter)) != cudaSuccess) return e;
+    void* z = nullptr;
+    if ((e = cudaGetSymbolAddress(&z, g_noalloc_zero_bias)) != cudaSuccess) return e;
+    s.logits = static_cast<float*>(p);
+    s.counter = static_cast<uint32_t*>(q);
+    s.zero_bias = static_cast<float*>(z);
+  }
+  *out = s;
+  return cudaSuccess;
+}
+}  // namespace
+
 }  // namespace moe
+
+extern "C" moe_status moe_route_topk_noalloc(const void* x_bf16, const void* router_w_bf16, const float* router_b,
+                                             int32_t T, int32_t d, int32_t n_experts, int32_t top_k, int32_t* idx,
+                                             float* w, void* stream) {
+  using namespace moe;
+  if (!x_bf16 || !router_w_bf16 || !idx || !w)
+    return set_last_error(MOE_ERR_INVALID_ARG, "moe_route_topk_noalloc: NULL pointer");
+  if (T < 1 || T > kMaxDecodeT)
+    return set_last_error(MOE_ERR_INVALID_ARG, "moe_route_topk_noalloc: T=%d exceeds the static scratch (1..%d)",
+                          T, kMaxDecodeT);
+  if (n_experts > kMaxE || top_k < 2 || top_k > kMaxTopK || n_experts <= top_k)
+    return set_last_error(MOE_ERR_INVALID_ARG,
+                          "moe_route_topk_noalloc: need 2 <= top_k <= %d and top_k < n_experts <= %d", kMaxTopK,
+                          kMaxE);
+  if (d <= 0 || d % 256 != 0)
+    return set_last_error(MOE_ERR_INVALID_ARG, "moe_route_topk_noalloc: d must be a positive multiple of 256");
+  if (reinterpret_cast<uintptr_t>(x_bf16) % 16 || reinterpret_cast<uintptr_t>(router_w_bf16) % 16)
+    return set_last_error(MOE_ERR_INVALID_ARG, "moe_route_topk_noalloc: x and router_w must be 16-byte aligned");
+  NoallocScratch sc;
+  cudaError_t e = noalloc_scratch(&sc);
+  if (e != cudaSuccess)
+    return set_last_error(MOE_ERR_CUDA, "moe_route_topk_noalloc: static scratch lookup failed: %s",
+                          cudaGetErrorString(e));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the arrival counter must start at zero
+  e = cudaMemsetAsync(sc.counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return set_last_error(MOE_ERR_CUDA, "moe_route_topk_noalloc: %s", cudaGetErrorString(e));
+  RouteArgs a{};
+  a.x = static_cast<const uint16_t*>(x_bf16);
+  a.wr = static_cast<const uint16_t*>(router_w_bf16);
+  a.bias = router_b ? router_b : sc.zero_bias;
+  a.T = T;
+  a.d = d;
+  a.E = n_experts;
+  a.k = top_k;
+  a.mode = ROUTE_ONLY;
+  a.logits = sc.logits;
+  a.cnt = sc.counter;
+  a.out_idx = idx;
+  a.out_w = w;
+  e = launch_route(a, s);
+  if (e != cudaSuccess) return set_last_error(MOE_ERR_CUDA, "moe_route_topk_noalloc: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}

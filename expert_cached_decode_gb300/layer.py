@@ -125,3 +125,14 @@ class MoELayer:
             self.moe_layer_destroy()
         except Exception:
             pass
+
+
+def moe_route_topk_noalloc(x, router_w, router_b, top_k, idx, w, stream=None):
+    """Binding of the allocation-free router entry point: x[T, d] bf16,
+    router_w[E, d] bf16, router_b[E] fp32 or None (all device tensors);
+    writes idx[T, k] int32 and w[T, k] fp32 (device)."""
+    L = _abi.load()
+    T, d = x.shape
+    E = router_w.shape[0]
+    check(L.moe_route_topk_noalloc(_ptr(x), _ptr(router_w), _ptr(router_b), T, d, E, top_k, _ptr(idx), _ptr(w),
+                                   _stream(stream)), "moe_route_topk_noalloc")

@@ -159,6 +159,28 @@ moe_status moe_cache_export(moe_ctx* ctx, int32_t* owner, int64_t* stamp);
 /* Free every library-owned resource.  NULL is accepted. */
 void moe_layer_destroy(moe_ctx* ctx);
 
+/* Router only, allocating nothing: the same result as moe_route_topk
+ * (idx[T][k] ascending expert ids, w[T][k] renormalised weights, device
+ * buffers) for tokens x[T][d] (bf16, device) and one layer's router weights
+ * router_w[E][d] (bf16, device) and bias router_b[E] (fp32, device, or NULL
+ * for zero), without a context.  No counterpart on the pages: it exists for
+ * callers that cannot call cudaMalloc, e.g. code whose device memory is all
+ * reserved up front by its own allocator, or code on a latency-critical path
+ * that must not risk the device-wide synchronisation an allocation can cause.
+ * Its scratch is a fixed array inside the library (logits of at most 16
+ * tokens x 1024 experts plus a counter, about 72 KiB, held by every GPU that
+ * loads the library until the process exits).  Limits: 1 <= T <= 16,
+ * 2 <= k <= 16, k < E <= 1024, d a positive multiple of 256, x and router_w
+ * 16-byte aligned; larger sizes are rejected with MOE_ERR_INVALID_ARG and a
+ * message.  The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  Every call shares the one scratch array: calls that
+ * overlap on the GPU (e.g. on two streams) race and must be serialised by the
+ * caller.  Asynchronous on `stream`. */
+moe_status moe_route_topk_noalloc(const void* x_bf16, const void* router_w_bf16, const float* router_b,
+                                  int32_t T, int32_t d, int32_t n_experts, int32_t top_k,
+                                  int32_t* idx, float* w, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* moe_last_error(void);
 
