@@ -30,10 +30,13 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose=False, extra_flags=()):
+def build(verbose=False, extra_flags=(), out_dir=None):
+    """Compile every .cu of csrc/ and link the library; returns its path.
+    out_dir (default _lib/) lets an instrumented variant live elsewhere."""
     nvcc = nvcc_path()
-    os.makedirs(OUT_DIR, exist_ok=True)
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    out_dir = out_dir or OUT_DIR
+    os.makedirs(out_dir, exist_ok=True)
+    obj_dir = os.path.join(out_dir, "obj")
     os.makedirs(obj_dir, exist_ok=True)
     common = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", os.path.join(ROOT, "include"), "-I", CSRC, *extra_flags]
@@ -51,7 +54,7 @@ def build(verbose=False, extra_flags=()):
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    lib = os.path.join(OUT_DIR, LIB_NAME)
+    lib = os.path.join(out_dir, LIB_NAME)
     tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

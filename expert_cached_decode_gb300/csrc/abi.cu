@@ -89,7 +89,7 @@ struct moe_ctx {
   Plan* plan = nullptr;
   Plan* plan_host = nullptr;  // pinned
   float* gu_partial = nullptr;
-  uint16_t* hfrag = nullptr;
+  uint16_t* hbuf = nullptr;      // [max_exp][16][f] fp16
   float* obuf = nullptr;
   uint32_t* counters = nullptr;  // gu_cnt | h_ready | d_cnt | done
   size_t counters_n = 0;
@@ -105,7 +105,8 @@ struct moe_ctx {
   float* p_w = nullptr;
   int32_t* p_counts = nullptr;
   uint16_t* p_xg = nullptr;      // [T*(k+1)][d] fp16, expert-sorted activations
-  uint16_t* p_hg = nullptr;      // [T*(k+1)][f] fp16
+  uint16_t* p_hg = nullptr;      // [T*(k+1)][f] fp16 (hi part of h)
+  uint16_t* p_hg_lo = nullptr;   // [T*(k+1)][f] fp16 (lo part of h)
   int32_t* p_perm = nullptr;
   float* p_wsort = nullptr;
   int32_t* p_cursor = nullptr;
@@ -287,7 +288,7 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(cudaMemset(c->plan, 0, sizeof(Plan)));
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
   CREATE_TRY(cudaMalloc(&c->gu_partial, (size_t)c->max_exp * RG * KC * 2 * 512 * sizeof(float)));
-  CREATE_TRY(cudaMalloc(&c->hfrag, (size_t)c->max_exp * 2 * RG * 2 * 32 * 4 * sizeof(uint16_t)));
+  CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
   CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
   c->counters_n = (size_t)c->max_exp * RG + c->max_exp + RD + 1;
   CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
@@ -332,7 +333,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->plan);
   if (c->plan_host) cudaFreeHost(c->plan_host);
   cudaFree(c->gu_partial);
-  cudaFree(c->hfrag);
+  cudaFree(c->hbuf);
   cudaFree(c->obuf);
   cudaFree(c->counters);
   cudaFree(c->err);
@@ -343,6 +344,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->p_counts);
   cudaFree(c->p_xg);
   cudaFree(c->p_hg);
+  cudaFree(c->p_hg_lo);
   cudaFree(c->p_perm);
   cudaFree(c->p_wsort);
   cudaFree(c->p_cursor);
@@ -494,6 +496,7 @@ static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
   c->p_max_tiles = (int64_t)(c->E + 1 + (rows + kPrefillBN - 1) / kPrefillBN);
   CUDA_TRY(cudaMalloc(&c->p_xg, (size_t)rows * c->d * sizeof(uint16_t)));
   CUDA_TRY(cudaMalloc(&c->p_hg, (size_t)rows * c->f * sizeof(uint16_t)));
+  CUDA_TRY(cudaMalloc(&c->p_hg_lo, (size_t)rows * c->f * sizeof(uint16_t)));
   CUDA_TRY(cudaMalloc(&c->p_perm, (size_t)rows * sizeof(int32_t)));
   CUDA_TRY(cudaMalloc(&c->p_wsort, (size_t)rows * sizeof(float)));
   CUDA_TRY(cudaMalloc(&c->p_cursor, (size_t)c->E * sizeof(int32_t)));
@@ -539,10 +542,8 @@ extern "C" moe_status moe_route_topk(moe_ctx* c, int32_t layer, const void* x, i
   moe_status st = check_common(c, layer, x, T, kMaxPrefillT);
   if (st != MOE_OK) return st;
   if (!idx || !w) return fail(MOE_ERR_INVALID_ARG, "NULL output");
-  if (T > kMaxDecodeT) {
-    if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
-    return prefill_route(c, layer, x, T, idx, w, nullptr, static_cast<cudaStream_t>(stream));
-  }
+  if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  if (T > kMaxDecodeT) return prefill_route(c, layer, x, T, idx, w, nullptr, static_cast<cudaStream_t>(stream));
   RouteArgs ra = route_args(c, layer, x, T, ROUTE_ONLY);
   ra.out_idx = idx;
   ra.out_w = w;
@@ -564,7 +565,7 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.shared_weight = c->shared_weight;
   fa.plan = c->plan;
   fa.gu_partial = c->gu_partial;
-  fa.hfrag = c->hfrag;
+  fa.hbuf = c->hbuf;
   fa.obuf = c->obuf;
   fa.gu_cnt = c->gu_cnt;
   fa.h_ready = c->h_ready;
@@ -643,9 +644,10 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   CUDA_TRY(launch_prefill_scatter(sa, s));
   CUDA_TRY(launch_prefill_gather(static_cast<const uint16_t*>(x), c->p_perm, c->p_xg, rows, c->d, s));
   CUDA_TRY(cudaMemsetAsync(y, 0, (size_t)T * c->d * sizeof(float), s));
-  CUtensorMap tx, th;
+  CUtensorMap tx, th, thl;
   st = make_tmap_2d(&tx, c->p_xg, rows, c->d, kPrefillBN, false);
   if (st == MOE_OK) st = make_tmap_2d(&th, c->p_hg, rows, c->f, kPrefillBN, false);
+  if (st == MOE_OK) st = make_tmap_2d(&thl, c->p_hg_lo, rows, c->f, kPrefillBN, false);
   if (st != MOE_OK) return st;
   PrefillGemmArgs ga{};
   ga.slots = c->slots;
@@ -656,6 +658,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   ga.tiles_dn = c->p_tiles_dn;
   ga.n_tiles = c->p_ntiles;
   ga.hg = c->p_hg;
+  ga.hg_lo = c->p_hg_lo;
   ga.perm = c->p_perm;
   ga.wsort = c->p_wsort;
   ga.y = y;
@@ -664,7 +667,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   ga.f = c->f;
   ga.err = c->err;
   CUDA_TRY(launch_prefill_gate_up(tx, ga, s, c->num_sms));
-  CUDA_TRY(launch_prefill_down(th, ga, s, c->num_sms));
+  CUDA_TRY(launch_prefill_down(th, thl, ga, s, c->num_sms));
   if (trace) {
     const int n = T * c->k;
     std::vector<int32_t> gslot(c->E + 1);
@@ -694,6 +697,7 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   if (!y) return fail(MOE_ERR_INVALID_ARG, "NULL output");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T > kMaxDecodeT) return prefill_forward(c, layer, x, T, y, s, trace);
+  if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   FfnArgs fa = ffn_args(c, layer, x, T, y);
   if (c->all_resident) {
     RouteArgs ra = route_args(c, layer, x, T, ROUTE_RESIDENT);

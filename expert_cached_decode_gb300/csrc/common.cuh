@@ -29,6 +29,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Optional phase timeline (build with -DMOE_TIMELINE): %globaltimer stamps
+// written to a per-file device array [rows][16] that a debug entry point
+// (moe_debug_timeline_*, present only in such builds) copies out.
+#ifdef MOE_TIMELINE
+#define MOE_TL(arr, row, slot) ((arr)[(row)][(slot)] = globaltimer())
+#else
+#define MOE_TL(arr, row, slot) ((void)0)
+#endif
+
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t code) {
   atomicCAS(err, 0u, code);
 }

@@ -95,7 +95,7 @@ struct FfnArgs {
   float shared_weight;
   const Plan* plan;
   float* gu_partial;
-  uint16_t* hfrag;
+  uint16_t* hbuf;               // [max_exp][T][f] fp16 h of each expert
   float* obuf;
   uint32_t* gu_cnt;
   uint32_t* h_ready;
@@ -162,7 +162,8 @@ struct PrefillGemmArgs {
   const PrefillTile* tiles_gu;
   const PrefillTile* tiles_dn;
   const int32_t* n_tiles;
-  uint16_t* hg;            // [rows][f] fp16 (gate/up output, down input)
+  uint16_t* hg;            // [rows][f] fp16 hi part of h (gate/up output, down input)
+  uint16_t* hg_lo;         // [rows][f] fp16 lo part of h
   const int32_t* perm;
   const float* wsort;
   float* y;                // [T][d]
@@ -188,7 +189,8 @@ cudaError_t launch_prefill_scatter(const PrefillScatterArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16_t* xg, int rows, int d,
                                   cudaStream_t s);
 cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid);
-cudaError_t launch_prefill_down(const CUtensorMap& tmH, const PrefillGemmArgs& a, cudaStream_t s, int grid);
+cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
+                                cudaStream_t s, int grid);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl, int num_sms);
 
 }  // namespace moe

@@ -7,6 +7,9 @@
 // "一张 RTX 4090 跑千亿模型", §加个草稿层):
 //   gate/up:  [g|u]^T[f x n_e] = [Wg|Wu][f x d] . X_e^T   -> h = silu(g)*u (fp16)
 //   down:     o^T[d x n_e] = Wd[d x f] . H_e^T            -> y[t] += w[t,e] * o[t]
+// h is carried as an fp16 pair (hi = RN(h), lo = RN(h - hi)) and the down
+// GEMM accumulates Wd.hi + Wd.lo, so h keeps ~22 bits; the fp16 weight
+// RN(q * scale) is the only rounding of an operand.
 // Weights sit on the MMA M side (128 rows per tile), tokens on N (<= 256 per
 // tile, rounded up to 16).  Producer warps expand the 3-bit blocks of the
 // slot to fp16 RN(q * scale) straight into the 128-byte-swizzled K-major
@@ -188,11 +191,13 @@ __device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lan
 // double-buffered accumulator, weighted atomic combine into y).
 template <bool DOWN>
 __global__ void __launch_bounds__(pg::THREADS, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, PrefillGemmArgs a) {
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                        PrefillGemmArgs a) {
   using namespace pg;
-  constexpr int NMAT = DOWN ? 1 : 2;
-  constexpr int STAGES = DOWN ? 4 : 3;
-  constexpr int STAGE_BYTES = NMAT * A_BYTES + B_BYTES;
+  constexpr int NMAT = DOWN ? 1 : 2;           // weight tiles per stage
+  constexpr int NB = DOWN ? 2 : 1;             // token tiles per stage (down: h hi and lo)
+  constexpr int STAGES = DOWN ? 2 : 3;
+  constexpr int STAGE_BYTES = NMAT * A_BYTES + NB * B_BYTES;
   constexpr int PCHUNK = NMAT * 2 * kBlockBytes;    // packed bytes per producer per k block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -230,6 +235,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     for (int i = 0; i < NPROD * PSTAGES; ++i) mbar_init(&pbar[i], 1);
     mbar_init_fence();
     prefetch_tmap(&tmB);
+    if (DOWN) prefetch_tmap(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -264,8 +270,9 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             goto done;
           }
           uint8_t* st = stages + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_b[s], B_BYTES);
+          mbar_arrive_expect_tx(&full_b[s], NB * B_BYTES);
           tma_load_2d(st + NMAT * A_BYTES, &tmB, kb * BK, tl.row0, &full_b[s]);
+          if (DOWN) tma_load_2d(st + NMAT * A_BYTES + B_BYTES, &tmB2, kb * BK, tl.row0, &full_b[s]);
         }
       }
     }
@@ -299,8 +306,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             const uint64_t da = smem_desc_sw128(st + mat * A_BYTES);
             const uint32_t d_tmem = tmem + (DOWN ? ab * BN : mat * BN);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
+            for (int kk = 0; kk < BK / 16; ++kk) {
               umma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+              if (DOWN) {
+                const uint64_t db_lo = smem_desc_sw128(st + NMAT * A_BYTES + B_BYTES);
+                umma_f16(d_tmem, da + 2 * kk, db_lo + 2 * kk, idesc, 1u);
+              }
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -387,21 +399,31 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
           tmem_ld32(tmem + lane_addr + BN + c * 32, ru);
           tmem_ld_wait();
           __half* eh = reinterpret_cast<__half*>(epi);
+          float hv[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
-            eh[j * BM + row] = __float2half_rn(g / (1.f + expf(-g)) * u);
+            hv[j] = g / (1.f + expf(-g)) * u;
           }
-          named_bar(1, 128);
-          // 32 token rows x 128 f values (256 B) -> Hg
-          for (int q = et; q < 32 * 16; q += 128) {
-            const int j = q >> 4, ch = q & 15;
-            if (j < nrow) {
-              const uint4 v = *reinterpret_cast<const uint4*>(epi + j * 256 + ch * 16);
-              *reinterpret_cast<uint4*>(a.hg + (size_t)(tl.row0 + c * 32 + j) * a.f + tl.m * BM + ch * 8) = v;
+          // pass 0 writes hi = RN(h) to Hg, pass 1 writes lo = RN(h - hi) to Hg_lo
+          for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const __half hi = __float2half_rn(hv[j]);
+              eh[j * BM + row] = pass == 0 ? hi : __float2half_rn(hv[j] - __half2float(hi));
             }
+            named_bar(1, 128);
+            uint16_t* dst = pass == 0 ? a.hg : a.hg_lo;
+            // 32 token rows x 128 f values (256 B)
+            for (int q = et; q < 32 * 16; q += 128) {
+              const int j = q >> 4, ch = q & 15;
+              if (j < nrow) {
+                const uint4 v = *reinterpret_cast<const uint4*>(epi + j * 256 + ch * 16);
+                *reinterpret_cast<uint4*>(dst + (size_t)(tl.row0 + c * 32 + j) * a.f + tl.m * BM + ch * 8) = v;
+              }
+            }
+            named_bar(1, 128);
           }
-          named_bar(1, 128);
         } else {
           if (et < 32) {
             const int j = et;
@@ -442,8 +464,9 @@ done:
 template <bool DOWN>
 static size_t gemm_smem() {
   constexpr int NMAT = DOWN ? 1 : 2;
-  constexpr int STAGES = DOWN ? 4 : 3;
-  constexpr int STAGE_BYTES = NMAT * pg::A_BYTES + pg::B_BYTES;
+  constexpr int NB = DOWN ? 2 : 1;
+  constexpr int STAGES = DOWN ? 2 : 3;
+  constexpr int STAGE_BYTES = NMAT * pg::A_BYTES + NB * pg::B_BYTES;
   constexpr int PCHUNK = NMAT * 2 * kBlockBytes;
   constexpr int EPI_BYTES = DOWN ? 32 * pg::BM * 4 : 32 * pg::BM * 2;
   return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + pg::NPROD * pg::PSTAGES * PCHUNK +
@@ -451,7 +474,8 @@ static size_t gemm_smem() {
 }
 
 template <bool DOWN>
-static cudaError_t launch_gemm(const CUtensorMap& tmB, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
+static cudaError_t launch_gemm(const CUtensorMap& tmB, const CUtensorMap& tmB2, const PrefillGemmArgs& a,
+                               cudaStream_t s, int grid) {
   static bool configured = false;
   const size_t smem = gemm_smem<DOWN>();
   if (!configured) {
@@ -460,7 +484,7 @@ static cudaError_t launch_gemm(const CUtensorMap& tmB, const PrefillGemmArgs& a,
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  prefill_gemm_kernel<DOWN><<<grid, pg::THREADS, smem, s>>>(tmB, a);
+  prefill_gemm_kernel<DOWN><<<grid, pg::THREADS, smem, s>>>(tmB, tmB2, a);
   return cudaGetLastError();
 }
 
@@ -482,11 +506,12 @@ cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16
 }
 
 cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
-  return launch_gemm<false>(tmX, a, s, grid);
+  return launch_gemm<false>(tmX, tmX, a, s, grid);
 }
 
-cudaError_t launch_prefill_down(const CUtensorMap& tmH, const PrefillGemmArgs& a, cudaStream_t s, int grid) {
-  return launch_gemm<true>(tmH, a, s, grid);
+cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
+                                cudaStream_t s, int grid) {
+  return launch_gemm<true>(tmH, tmHlo, a, s, grid);
 }
 
 }  // namespace moe

@@ -25,6 +25,10 @@
 
 namespace moe {
 
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_route_timeline[256][16];
+#endif
+
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
@@ -62,6 +66,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 }
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
+  if (threadIdx.x == 0) MOE_TL(g_route_timeline, blockIdx.x, 0);
   pdl_launch_dependents();
 
   __shared__ uint32_t s_mask[kMaxE / 32];
@@ -88,26 +93,37 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
 #pragma unroll
     for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.f;
     const uint16_t* wrow = a.wr + (size_t)e * d;
-    for (int j = lane * 8; j < d; j += 256) {
-      const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wrow + j));
-      float wf[8];
-      wf[0] = bf16_bits_to_float(wv.x & 0xffffu); wf[1] = bf16_bits_to_float(wv.x >> 16);
-      wf[2] = bf16_bits_to_float(wv.y & 0xffffu); wf[3] = bf16_bits_to_float(wv.y >> 16);
-      wf[4] = bf16_bits_to_float(wv.z & 0xffffu); wf[5] = bf16_bits_to_float(wv.z >> 16);
-      wf[6] = bf16_bits_to_float(wv.w & 0xffffu); wf[7] = bf16_bits_to_float(wv.w >> 16);
+    // all loads of a 2048-wide block issued before the arithmetic (lane chunk
+    // j = lane*8 + 256*u, accumulated in u order)
+    for (int jb = 0; jb < d; jb += 2048) {
+      uint4 wv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = jb + lane * 8 + 256 * u;
+        wv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(wrow + j)) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int t = 0; t < kMaxDecodeT; ++t) {
         if (t < T) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d + j));
+          uint4 xv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = jb + lane * 8 + 256 * u;
+            xv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d + j)) : make_uint4(0u, 0u, 0u, 0u);
+          }
           float s = acc[t];
-          s = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wf[0], s);
-          s = fmaf(bf16_bits_to_float(xv.x >> 16), wf[1], s);
-          s = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wf[2], s);
-          s = fmaf(bf16_bits_to_float(xv.y >> 16), wf[3], s);
-          s = fmaf(bf16_bits_to_float(xv.z & 0xffffu), wf[4], s);
-          s = fmaf(bf16_bits_to_float(xv.z >> 16), wf[5], s);
-          s = fmaf(bf16_bits_to_float(xv.w & 0xffffu), wf[6], s);
-          s = fmaf(bf16_bits_to_float(xv.w >> 16), wf[7], s);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w4 = wv[u], x4 = xv[u];
+            s = fmaf(bf16_bits_to_float(x4.x & 0xffffu), bf16_bits_to_float(w4.x & 0xffffu), s);
+            s = fmaf(bf16_bits_to_float(x4.x >> 16), bf16_bits_to_float(w4.x >> 16), s);
+            s = fmaf(bf16_bits_to_float(x4.y & 0xffffu), bf16_bits_to_float(w4.y & 0xffffu), s);
+            s = fmaf(bf16_bits_to_float(x4.y >> 16), bf16_bits_to_float(w4.y >> 16), s);
+            s = fmaf(bf16_bits_to_float(x4.z & 0xffffu), bf16_bits_to_float(w4.z & 0xffffu), s);
+            s = fmaf(bf16_bits_to_float(x4.z >> 16), bf16_bits_to_float(w4.z >> 16), s);
+            s = fmaf(bf16_bits_to_float(x4.w & 0xffffu), bf16_bits_to_float(w4.w & 0xffffu), s);
+            s = fmaf(bf16_bits_to_float(x4.w >> 16), bf16_bits_to_float(w4.w >> 16), s);
+          }
           acc[t] = s;
         }
       }
@@ -126,6 +142,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
 
   // ---- last CTA to arrive does the selection -----------------------------
   __syncthreads();
+  if (threadIdx.x == 0) MOE_TL(g_route_timeline, blockIdx.x, 1);
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(a.cnt, 1u);
@@ -134,6 +151,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 0);
 
   for (int i = threadIdx.x; i < kMaxE / 32; i += kRouteThreads) s_mask[i] = 0;
   if (threadIdx.x == 0) {
@@ -198,6 +216,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   }
   __syncthreads();
 
+  if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 1);
   // distinct experts U, ascending
   const int n_words = (E + 31) / 32;
   if (warp == 0) {
@@ -251,6 +270,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   }
   __syncthreads();
 
+  if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 2);
   if (a.mode == ROUTE_RESIDENT) {
     for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
       int slot = s_slot[i];
@@ -273,6 +293,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
       a.stats[ST_TOK_HIT] += (int64_t)T * K;
       a.stats[ST_DIST_HIT] += n_act;
       *a.clock = s_clock + 1;
+      MOE_TL(g_route_timeline, 200, 3);
     }
     return;
   }
@@ -396,6 +417,12 @@ __global__ void __launch_bounds__(256) commit_kernel(CommitArgs a) {
     *a.clock = clk + 1;
   }
 }
+
+#ifdef MOE_TIMELINE
+extern "C" int moe_debug_timeline_route(unsigned long long* out) {
+  return (int)cudaMemcpyFromSymbol(out, g_route_timeline, sizeof(g_route_timeline));
+}
+#endif
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const int grid = (a.E + kRouteWarps - 1) / kRouteWarps;
