@@ -227,6 +227,146 @@ def run_prefill(steps, warmup, sweep=(4096, 6144, 8192, 12288, 16384)):
     return out
 
 
+# ------------------------------------------------------------ 48-layer stack --
+def _draw_layer_tokens(args):
+    cfg_id, lam, layer, calls = args
+    sys.path.insert(0, ROOT)
+    from moe_inputs import Synth, WORKLOADS
+    s = Synth(WORKLOADS[cfg_id], bias_lambda=lam)
+    return layer, s.tokens_many(layer, list(range(calls)))
+
+
+def draw_stack_tokens(cfg_id, calls, n_layers, workers=16):
+    """Seeded activations [L, calls, T, d] (bf16 bits) of a stack workload,
+    one spawn-pool job per layer."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    from moe_inputs import BIAS_LAMBDA
+    out = [None] * n_layers
+    with cf.ProcessPoolExecutor(max_workers=min(workers, n_layers), mp_context=mp.get_context("spawn")) as ex:
+        for layer, xs in ex.map(_draw_layer_tokens, [(cfg_id, BIAS_LAMBDA, l, calls) for l in range(n_layers)]):
+            out[layer] = xs
+    return np.stack(out)
+
+
+def _fill_pool_range(args):
+    shm_name, B, cfg_id, lam, lo, hi = args
+    sys.path.insert(0, ROOT)
+    from multiprocessing import shared_memory
+    from moe_inputs import Synth, WORKLOADS
+    shm = shared_memory.SharedMemory(name=shm_name)
+    try:
+        view = np.ndarray((hi - lo, B), dtype=np.uint8, buffer=shm.buf, offset=lo * B)
+        s = Synth(WORKLOADS[cfg_id], bias_lambda=lam)
+        for p in range(lo, hi):
+            s.expert_packed(p, out=view[p - lo])
+        del view
+    finally:
+        shm.close()
+    return hi - lo
+
+
+def make_host_pool(cfg_id, entries, workers=16):
+    """Canonical packed experts of host-pool entries [0, entries) in a shared
+    memory block filled by a spawn pool (the library registers it)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    from moe_inputs import WORKLOADS, BIAS_LAMBDA, expert_nbytes
+    wl = WORKLOADS[cfg_id]
+    B = expert_nbytes(wl.d, wl.f)
+    shm = shared_memory.SharedMemory(create=True, size=entries * B)
+    step = max(1, (entries + workers * 4 - 1) // (workers * 4))
+    jobs = [(shm.name, B, cfg_id, BIAS_LAMBDA, lo, min(entries, lo + step)) for lo in range(0, entries, step)]
+    with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        assert sum(ex.map(_fill_pool_range, jobs)) == entries
+    return shm, np.ndarray((entries, B), dtype=np.uint8, buffer=shm.buf)
+
+
+def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
+    """Host -> device bandwidth of back-to-back expert-sized copies from pinned memory."""
+    import torch
+    n = total // chunk
+    src = torch.empty((n, chunk), dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty((n, chunk), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    out = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        with torch.cuda.stream(st):
+            for i in range(n):
+                dst[i].copy_(src[i], non_blocking=True)
+        e1.record(st)
+        st.synchronize()
+        out.append(n * chunk / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    return float(np.median(out))
+
+
+def run_stack(cfg_id, pool_entries=0, calls=0):
+    """48-layer stack with the 8,445-slot cache that starts empty (miss path):
+    the warm-up passes over the call stream, then the measured pass."""
+    import time
+    import torch
+    from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA, expert_nbytes
+    from expert_cached_decode_gb300.layer import MoELayer
+    wl = WORKLOADS[cfg_id]
+    calls = calls or wl.calls
+    P = pool_entries or wl.keys
+    t0 = time.time()
+    xs = draw_stack_tokens(cfg_id, calls, wl.n_layers)
+    shm, pool = make_host_pool(cfg_id, P)
+    s = Synth(wl, bias_lambda=BIAS_LAMBDA)
+    wr = np.stack([s.router(l)[0] for l in range(wl.n_layers)])
+    b = np.stack([s.router(l)[2] for l in range(wl.n_layers)])
+    shared = np.stack([s.shared_packed(l) for l in range(wl.n_layers)])
+    layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
+                     host_pool_entries=0 if P == wl.keys else P)
+    layer.moe_cache_configure(wl.capacity)
+    setup_s = time.time() - t0
+    xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty((wl.tokens, wl.d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(wl.warm_passes):
+            for c in range(calls):
+                for l in range(wl.n_layers):
+                    layer.moe_forward(l, xdev[l, c], y)
+    stream.synchronize()
+    before = layer.moe_cache_stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for c in range(calls):
+            for l in range(wl.n_layers):
+                layer.moe_forward(l, xdev[l, c], y)
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    after = layer.moe_cache_stats()
+    dlt = {k: after[k] - before[k] for k in after}
+    layer.close()
+    del pool
+    shm.close()
+    shm.unlink()
+    h2d = measure_h2d_gbs()
+    hbm, _ = peaks()
+    B = expert_nbytes(wl.d, wl.f)
+    distinct_bytes = (dlt["distinct_hits"] + dlt["distinct_misses"] + dlt["layer_calls"]) * B  # + shared
+    t_bound = max(distinct_bytes / (hbm * 1e9), dlt["miss_bytes"] / (h2d * 1e9))
+    tokens = calls * wl.tokens
+    return {"workload": f"{wl.name}: 48 layers, T={wl.tokens} per call, Zipf s={wl.zipf_s} (lambda "
+                        f"{BIAS_LAMBDA}), {wl.capacity} slots starting empty, {wl.warm_passes} warm-up passes "
+                        f"then the measured pass of {calls} calls",
+            "host_pool_entries": P, "tokens_per_s": tokens / (ms / 1e3), "ms_measured_pass": ms,
+            "token_hit_rate": dlt["token_hits"] / max(1, dlt["token_hits"] + dlt["token_misses"]),
+            "distinct_expert_bytes": distinct_bytes, "miss_bytes": dlt["miss_bytes"],
+            "h2d_gbs_measured": h2d, "hbm_gbs": hbm,
+            "roofline": {"bound_ms": 1e3 * t_bound, "frac": 1e3 * t_bound / ms,
+                         "note": "max(distinct-expert bytes / HBM, miss bytes / measured H2D)"},
+            "setup_s": setup_s}
+
+
 def cpu_oracle_sample(n_calls, threads=1):
     """Time the fp64 oracle on the first n_calls of the decode stream in a
     child process with BLAS limited to `threads`."""
@@ -398,6 +538,11 @@ def run_gpu(args):
                 line["prefill"] = run_prefill(args.prefill_steps, 3)
             except Exception as ex:   # reported, not hidden
                 line["prefill"] = {"error": str(ex)[:300]}
+        if args.stack:
+            try:
+                line["stack"] = [run_stack(c, args.stack_pool) for c in (3, 4)]
+            except Exception as ex:   # reported, not hidden
+                line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline:
             n = args.cpu_calls
             r = cpu_oracle_sample(n)
@@ -421,6 +566,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true", help="also time the 12,288-token prefill chunk and sweep")
     ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--stack", action="store_true",
+                    help="also run the 48-layer stacks (T=5 Zipf 1.1, T=16 Zipf 0.8) with the 8,445-slot cache")
+    ap.add_argument("--stack-pool", type=int, default=0,
+                    help="host-pool entries for --stack (default: one per (layer, expert), 50.7 GB)")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
+                    help="time only the prefill path at T tokens (profiling runs)")
     ap.add_argument("--calls", type=int, default=CALLS,
                     help="calls per step (the workload is 10,000; smaller only for profiling)")
     args = ap.parse_args()
@@ -428,6 +579,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        import torch
+        torch.cuda.set_device(_dist()[2])
+        print(json.dumps({"prefill": run_prefill(args.steps, args.warmup, sweep=(args.prefill_only,))}), flush=True)
     else:
         run_gpu(args)
 

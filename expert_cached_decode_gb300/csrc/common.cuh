@@ -142,6 +142,11 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   return v;
 }
 
+// named barrier among `count` threads (multiple of 32)
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // --------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -233,5 +238,68 @@ __device__ __forceinline__ void dequant_block(uint32_t w0, uint32_t w1, uint32_t
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// ------------------------------------------------------------- warp top-k ---
+// Order-preserving 32-bit key of a float (larger float -> larger key; -inf
+// maps above 0, so 0 marks "no entry").
+__device__ __forceinline__ uint32_t float_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One warp selects the K largest of its E values (lane holds entries
+// id = lane + 32*i, i < VPL; ties go to the lower id).  Each lane first sorts
+// its own (key, ~id) pairs descending with a bitonic network; then each of
+// the K rounds takes the warp maximum of the lane heads with two redux.sync
+// reductions (largest key, then smallest id among equal keys) and the owner
+// pops its head.  Lane r < K receives the r-th largest value and its id.
+template <int VPL>
+__device__ __forceinline__ void warp_topk(const float (&v)[VPL], int E, int K, int lane, float& out_v, int& out_id) {
+  uint64_t s[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int id = lane + 32 * i;
+    s[i] = id < E ? ((uint64_t)float_key(v[i]) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
+  }
+  // bitonic sort, descending
+#pragma unroll
+  for (int k = 2; k <= VPL; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool desc = (i & k) == 0;
+          const uint64_t a = s[i], b = s[l];
+          const bool swap = desc ? (a < b) : (a > b);
+          s[i] = swap ? b : a;
+          s[l] = swap ? a : b;
+        }
+      }
+    }
+  }
+  out_v = -INFINITY;
+  out_id = 0x7fffffff;
+  for (int r = 0; r < K; ++r) {
+    const uint32_t hk = (uint32_t)(s[0] >> 32);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t hid = ~(uint32_t)s[0];
+    const uint32_t win = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xffffffffu);
+    if (lane == r) {
+      out_v = key_float(m);
+      out_id = (int)win;
+    }
+    if (hk == m && hid == win) {
+#pragma unroll
+      for (int i = 0; i + 1 < VPL; ++i) s[i] = s[i + 1];
+      s[VPL - 1] = 0ull;
+    }
+  }
+}
+
 
 }  // namespace moe

@@ -160,42 +160,24 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(PrefillTopkArgs a) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= a.T) return;
   const int t = warp, E = a.E, K = a.k;
-  const int per_lane = (E + 31) / 32;
-  float v[kMaxE / 32];
+  float my_v;
+  int my_id;
+  if (E <= 512) {
+    float v[16];
 #pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int id = lane + 32 * i;
-    v[i] = (i < per_lane && id < E) ? a.logits[(size_t)t * E + id] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float my_v = -INFINITY;
-  int my_id = 0x7fffffff;
-  for (int r = 0; r < K; ++r) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const int id = lane + 32 * i;
-      const bool better = v[i] > bv || (v[i] == bv && id < bid);
-      if (i < per_lane && id < E && !((taken >> i) & 1u) && better) {
-        bv = v[i];
-        bid = id;
-      }
+      v[i] = id < E ? a.logits[(size_t)t * E + id] : -INFINITY;
     }
+    warp_topk<16>(v, E, K, lane, my_v, my_id);
+  } else {
+    float v[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
+    for (int i = 0; i < 32; ++i) {
+      const int id = lane + 32 * i;
+      v[i] = id < E ? a.logits[(size_t)t * E + id] : -INFINITY;
     }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    if (lane == r) {
-      my_v = bv;
-      my_id = bid;
-    }
+    warp_topk<32>(v, E, K, lane, my_v, my_id);
   }
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = lane < K ? expf(my_v - top) : 0.f;

@@ -161,42 +161,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   __syncthreads();
 
   // top-k per token, one warp per token
-  const int per_lane = (E + 31) / 32;
   for (int t = warp; t < T; t += kRouteWarps) {
-    float v[kMaxE / 32];
+    float my_v;
+    int my_id;
+    if (E <= 512) {
+      float v[16];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int id = lane + 32 * i;
-      v[i] = (i < per_lane && id < E) ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
-    }
-    uint32_t taken = 0;
-    float my_v = -INFINITY;
-    int my_id = 0x7fffffff;
-    for (int r = 0; r < K; ++r) {
-      float bv = -INFINITY;
-      int bid = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const int id = lane + 32 * i;
-        if (i < per_lane && id < E && !((taken >> i) & 1u) && beats(v[i], id, bv, bid)) {
-          bv = v[i];
-          bid = id;
-        }
+        v[i] = id < E ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
       }
+      warp_topk<16>(v, E, K, lane, my_v, my_id);
+    } else {
+      float v[32];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-        if (beats(ov, oid, bv, bid)) {
-          bv = ov;
-          bid = oid;
-        }
+      for (int i = 0; i < 32; ++i) {
+        const int id = lane + 32 * i;
+        v[i] = id < E ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
       }
-      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-      if (lane == r) {
-        my_v = bv;
-        my_id = bid;
-      }
+      warp_topk<32>(v, E, K, lane, my_v, my_id);
     }
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = lane < K ? expf(my_v - top) : 0.f;
