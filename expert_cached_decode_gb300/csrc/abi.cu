@@ -1,9 +1,11 @@
 // C ABI of the routed-expert FFN step (declared in include/moe_gb300.h).
 //
 // Host-side orchestration of one layer-call:
-//   all keys resident  : route kernel (ROUTE_RESIDENT, stamps the hits) and
-//                        the expert kernel, launched back to back with
-//                        programmatic dependent launch; no host wait.
+//   all keys resident  : one launch of the decode kernel with fused routing
+//                        (router, selection, stamps of the hits, expert
+//                        work); programmatic dependent launch lets it be
+//                        scheduled while the previous call drains.  No host
+//                        wait.
 //   otherwise          : route kernel (ROUTE_PLAN) -> the host reads the
 //                        miss list -> one cudaMemcpyAsync per miss (host pool
 //                        -> staging) on a side stream and a re-layout kernel
@@ -88,15 +90,16 @@ struct moe_ctx {
   uint32_t* route_cnt = nullptr;
   Plan* plan = nullptr;
   Plan* plan_host = nullptr;  // pinned
-  float* gu_partial = nullptr;
   uint16_t* hbuf = nullptr;      // [max_exp][16][f] fp16
   float* obuf = nullptr;
-  uint32_t* counters = nullptr;  // gu_cnt | h_ready | d_cnt | done
+  uint32_t* counters = nullptr;  // h_ready | d_cnt | done | gbar
   size_t counters_n = 0;
-  uint32_t* gu_cnt = nullptr;
   uint32_t* h_ready = nullptr;
   uint32_t* d_cnt = nullptr;
   uint32_t* done = nullptr;
+  uint32_t* gbar = nullptr;
+  int2* part = nullptr;          // [num_sms + 1][nx] decode work bounds
+  int nx = 0;
   uint32_t* err = nullptr;
   int max_exp = 0;
   // prefill scratch (allocated on first use, sized for kMaxPrefillT tokens)
@@ -280,23 +283,29 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   }
   // scratch
   c->max_exp = (kMaxDecodeT * c->k < c->E ? kMaxDecodeT * c->k : c->E) + 1;
-  const int RG = c->f / 32, KC = c->d / 256, RD = c->d / 32;
+  const int RD = c->d / 32;
   CREATE_TRY(cudaMalloc(&c->logits, (size_t)kMaxDecodeT * c->E * sizeof(float)));
   CREATE_TRY(cudaMalloc(&c->route_cnt, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
   CREATE_TRY(cudaMalloc(&c->plan, sizeof(Plan)));
   CREATE_TRY(cudaMemset(c->plan, 0, sizeof(Plan)));
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
-  CREATE_TRY(cudaMalloc(&c->gu_partial, (size_t)c->max_exp * RG * KC * 2 * 512 * sizeof(float)));
   CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
   CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
-  c->counters_n = (size_t)c->max_exp * RG + c->max_exp + RD + 1;
+  c->counters_n = (size_t)c->max_exp + RD + 2;
   CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
-  c->gu_cnt = c->counters;
-  c->h_ready = c->gu_cnt + (size_t)c->max_exp * RG;
+  c->h_ready = c->counters;
   c->d_cnt = c->h_ready + c->max_exp;
   c->done = c->d_cnt + RD;
+  c->gbar = c->done + 1;
+  {
+    c->nx = c->max_exp + 1;
+    std::vector<int2> part((size_t)(c->num_sms + 1) * c->nx);
+    decode_partition(c->num_sms, c->nx, c->d, c->f, part.data());
+    CREATE_TRY(cudaMalloc(&c->part, part.size() * sizeof(int2)));
+    CREATE_TRY(cudaMemcpy(c->part, part.data(), part.size() * sizeof(int2), cudaMemcpyHostToDevice));
+  }
   CREATE_TRY(cudaMalloc(&c->err, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->err, 0, sizeof(uint32_t)));
   CREATE_TRY(cudaMalloc(&c->clock, sizeof(int64_t)));
@@ -332,7 +341,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->route_cnt);
   cudaFree(c->plan);
   if (c->plan_host) cudaFreeHost(c->plan_host);
-  cudaFree(c->gu_partial);
+  cudaFree(c->part);
   cudaFree(c->hbuf);
   cudaFree(c->obuf);
   cudaFree(c->counters);
@@ -564,15 +573,26 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.k = c->k;
   fa.shared_weight = c->shared_weight;
   fa.plan = c->plan;
-  fa.gu_partial = c->gu_partial;
   fa.hbuf = c->hbuf;
   fa.obuf = c->obuf;
-  fa.gu_cnt = c->gu_cnt;
   fa.h_ready = c->h_ready;
   fa.d_cnt = c->d_cnt;
   fa.done = c->done;
+  fa.gbar = c->gbar;
   fa.err = c->err;
+  fa.part = c->part;
+  fa.nx = c->nx;
   fa.grid = c->num_sms;
+  // fused routing (used when every key is resident)
+  fa.wr = c->router_w + (size_t)layer * c->E * c->d;
+  fa.bias = c->router_b + (size_t)layer * c->E;
+  fa.logits = c->logits;
+  fa.E = c->E;
+  fa.layer = layer;
+  fa.table = c->table;
+  fa.stamp = c->stamp;
+  fa.stats = c->stats + (size_t)layer * ST_N;
+  fa.clock = c->clock;
   return fa;
 }
 
@@ -700,9 +720,8 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   FfnArgs fa = ffn_args(c, layer, x, T, y);
   if (c->all_resident) {
-    RouteArgs ra = route_args(c, layer, x, T, ROUTE_RESIDENT);
-    CUDA_TRY(launch_route(ra, s));
-    CUDA_TRY(launch_decode_ffn(fa, s, true, c->num_sms));
+    fa.fused = 1;
+    CUDA_TRY(launch_decode_ffn(fa, s, true));
     if (trace) return fill_trace(c, s, T, trace);
     return MOE_OK;
   }
@@ -747,7 +766,7 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   ca.expert_bytes = c->B;
   CUDA_TRY(launch_commit(ca, s));
   c->qcur ^= 1;
-  CUDA_TRY(launch_decode_ffn(fa, s, false, c->num_sms));
+  CUDA_TRY(launch_decode_ffn(fa, s, false));
   if (trace) {
     moe_status t = fill_trace(c, s, T, trace);
     if (t != MOE_OK) return t;

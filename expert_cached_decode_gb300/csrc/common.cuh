@@ -142,6 +142,12 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   return v;
 }
 
+// orders this thread's earlier generic-proxy shared-memory accesses (and
+// those it synchronised with) before its later async-proxy (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // named barrier among `count` threads (multiple of 32)
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

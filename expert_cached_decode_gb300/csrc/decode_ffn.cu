@@ -1,8 +1,16 @@
-// Decode / verify expert FFN (T <= 16 tokens): every distinct routed expert
-// and the shared expert run once for all tokens routed to them (a verify
-// batch shares one fetch of each expert, page "单卡5090跑125B 大模型", §2.3),
+// Decode / verify step (T <= 16 tokens): every distinct routed expert and
+// the shared expert run once for all tokens routed to them (a verify batch
+// shares one fetch of each expert, page "单卡5090跑125B 大模型", §2.3),
 //   g = Wg.x, u = Wu.x, h = silu(g) * u, o = Wd.h,
 //   y[t] = shared_weight * o_shared[t] + sum_i w[t,i] * o_idx[t,i][t].
+//
+// Fused routing (every key resident): the same launch first computes the
+// router logits (CTA c takes rows c, c + G, ...), passes a grid-wide arrival
+// counter, and then every CTA selects the experts of the call from the full
+// logits itself (the same selection as the routing kernel), so no second
+// kernel and no plan round trip separate routing from the expert work.  CTA 0
+// publishes the plan, stamps the hit slots and bumps the layer counters.
+// Otherwise the kernel follows the routing kernel and reads its plan.
 //
 // Work is cut into tiles of contiguous bytes of the device block layout:
 //   gate/up tile (expert a, 32-row block rb of f): the Wg and Wu blocks of
@@ -13,17 +21,19 @@
 //     (R = 2 at f = 768); it multiplies by h_a, writes o_a for its rows, and
 //     the last expert to finish a row block combines y for those rows in a
 //     fixed order (shared expert, then routed experts in ascending id).
-// One persistent CTA per SM takes a byte-balanced share: a contiguous range
-// of gate/up tiles, then a contiguous range of down tiles.  A producer thread
-// streams every tile through a ring of 16-block stages with bulk TMA copies
-// (mbarrier completion); an h-loader thread bulk-copies each expert's h into
-// shared memory once per CTA when it is ready.  All 8 consumer warps work on
-// every stage (2 blocks each): they expand the 3-bit codes to fp16 in
-// registers and multiply on the tensor cores (mma.sync m16n8k16, fp32
-// accumulate, per-group scale in fp32); a tile's per-warp partial sums are
-// reduced through shared memory in a fixed order.  All waits are bounded.
+// One persistent CTA per SM takes a byte-balanced share (a host-computed
+// table per expert count): a contiguous range of gate/up tiles, then a
+// contiguous range of down tiles.  A producer thread streams every tile
+// through a ring of 16-block stages with bulk TMA copies (mbarrier
+// completion); an h-loader thread bulk-copies each expert's h into shared
+// memory once per CTA when it is ready.  All 8 consumer warps work on every
+// stage (2 blocks each): they expand the 3-bit codes to fp16 in registers and
+// multiply on the tensor cores (mma.sync m16n8k16, fp32 accumulate, per-group
+// scale in fp32); a tile's per-warp partial sums are reduced through shared
+// memory in a fixed order.  All waits are bounded.
 #include "common.cuh"
 #include "internal.h"
+#include "select.cuh"
 
 namespace moe {
 
@@ -139,7 +149,12 @@ __device__ __forceinline__ void h_frags(const uint8_t* hb, int hrow, int T, int 
   }
 }
 
-template <int NT>
+// bytes of the routing-phase scratch kept in the (not yet used) stage ring
+__host__ __device__ __forceinline__ size_t route_scratch_bytes(int E, int nx) {
+  return ((sizeof(SelSmem) + 15) & ~size_t(15)) + (size_t)E * 4 + (size_t)2 * nx * 8;
+}
+
+template <int NT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   constexpr int NS = FfnCfg<NT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -161,12 +176,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   uint64_t* empty = full + NS;
   uint64_t* hfull = empty + NS;
   uint64_t* hempty = hfull + kHSlots;
+  // routing-phase scratch, overlaid on the stage ring (free until the first copy)
+  SelSmem* sel = reinterpret_cast<SelSmem*>(ring);
+  int* s_tab = reinterpret_cast<int*>(ring + ((sizeof(SelSmem) + 15) & ~size_t(15)));
+  int2* s_part = reinterpret_cast<int2*>(s_tab + (FUSED ? a.E : 0));
+  __shared__ int s_act_slot[kMaxPicks];   // slot of each distinct routed expert
+  __shared__ int s_pick_act[kMaxPicks];   // [T][k] index of each pick in the distinct list
+  __shared__ float s_w[kMaxPicks];        // [T][k] routing weights
   __shared__ int s_g0, s_g1, s_d0, s_d1, s_nexp, s_last;
+  __shared__ long long s_clock;
   __shared__ volatile int s_hexp[kHSlots];
   __shared__ int s_comb[kMaxRT];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 0);
+  const int G = gridDim.x, cta = blockIdx.x, nx = a.nx;
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 0);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
@@ -178,6 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       s_hexp[i] = -1;
     }
     mbar_init_fence();
+  }
+  // x, the slot table and the clock may be written by earlier work in the
+  // stream: the fused kernel waits for it before reading anything
+  if (FUSED) {
+    pdl_launch_dependents();
+    pdl_wait();
+  }
+  // work bounds of this CTA and the next for every expert count
+  for (int i = tid; i < 2 * nx; i += kThreads) s_part[i] = a.part[(size_t)cta * nx + i];
+  if (FUSED) {
+    for (int i = tid; i < a.E; i += kThreads) s_tab[i] = a.table[(size_t)a.layer * a.E + i];
+    if (tid == 0) s_clock = cta == 0 ? (long long)*a.clock : 0;
   }
   // x fragments (B operand of the gate/up products), fp16, zero past T.
   // Entry (nt, kstep, lane) holds tokens nt*8 + lane/4, inputs
@@ -196,53 +232,98 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         xf[(((size_t)nt * nks + kstep) * 32 + (n & 7) * 4 + q) * 2 + reg] = pack_half2_from_bf16(in[q]);
     }
   }
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 1);
-  pdl_wait();   // the routing plan is complete and visible
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 2);
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 1);
 
+  if (FUSED) {
+    // ---- router rows e = cta + G*j, one warp per row ----------------------
+    const int E = a.E;
+    for (int j = warp;; j += kThreads / 32) {
+      const int e = cta + G * j;
+      if (e >= E) break;
+      router_row(a.wr + (size_t)e * d, a.x, a.bias[e], T, d, E, e, lane, a.logits);
+    }
+    __syncthreads();
+    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
+    // ---- every CTA's logits are written -----------------------------------
+    if (tid == 0) {
+      red_release_add(a.gbar, 1u);
+      if (!wait_flag_geq(a.gbar, (uint32_t)G)) set_error(a.err, DEV_TIMEOUT_FLAG);
+      MOE_TL(g_ffn_timeline, cta, 7);
+    }
+    __syncthreads();
+    select_call(a.logits, T, E, K, sel);
+    const int n_act = sel->n_act;
+    for (int i = tid; i < T * K; i += kThreads) {
+      const int id = sel->sel_id[i / K][i % K];
+      s_pick_act[i] = sel_act_index(sel, id);
+      s_w[i] = sel->sel_w[i / K][i % K];
+    }
+    for (int i = tid; i < n_act; i += kThreads) {
+      int slot = s_tab[sel->act[i]];
+      if (slot < 0) {
+        set_error(a.err, DEV_NOT_RESIDENT);
+        slot = 0;
+      }
+      s_act_slot[i] = slot;
+    }
+    if (tid == 0) s_nexp = n_act + 1;
+    __syncthreads();
+    if (cta == 0) {
+      // the plan of the call (read back for traces), LRU stamps, counters
+      Plan* P = a.plan;
+      const long long clk = s_clock;
+      for (int i = tid; i < T * K; i += kThreads) {
+        P->idx[i] = sel->sel_id[i / K][i % K];
+        P->w[i] = s_w[i];
+        P->pick_act[i] = s_pick_act[i];
+      }
+      for (int i = tid; i < n_act; i += kThreads) {
+        P->act_expert[i] = sel->act[i];
+        P->act_slot[i] = s_act_slot[i];
+        P->act_hit[i] = 1;
+        a.stamp[s_act_slot[i]] = clk;
+      }
+      if (tid == 0) {
+        P->n_act = n_act;
+        P->n_miss = 0;
+        P->T = T;
+        P->clock = clk;
+        P->token_hits = (int64_t)T * K;
+        P->token_misses = 0;
+        a.stats[ST_CALLS] += 1;
+        a.stats[ST_TOK_HIT] += (int64_t)T * K;
+        a.stats[ST_DIST_HIT] += n_act;
+        *a.clock = clk + 1;
+      }
+    }
+  } else {
+    pdl_wait();   // the routing plan is complete and visible
+    const Plan* P = a.plan;
+    for (int i = tid; i < kMaxPicks; i += kThreads) s_act_slot[i] = P->act_slot[i];
+    for (int i = tid; i < T * K; i += kThreads) {
+      s_pick_act[i] = P->pick_act[i];
+      s_w[i] = P->w[i];
+    }
+    if (tid == 0) s_nexp = P->n_act + 1;
+  }
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 2);
+  __syncthreads();
   // ---- this CTA's share: gate/up tiles [g0, g1), down tiles [d0, d1) ------
-  if (warp == 0) {
-    const int n_exp = a.plan->n_act + 1;
-    const long long G = gridDim.x, c = blockIdx.x;
-    const long long NG = (long long)n_exp * RG, ND = (long long)n_exp * (RD / RT);
-    const long long BG = 2LL * (d / 32), BD = (long long)RT * DG;   // blocks per tile
-    const long long W = NG * BG + ND * BD;
-    // down tiles owed to CTAs before cc: the rounded share of the bytes not
-    // covered by their gate/up tiles, made monotone by a prefix maximum
-    auto raw = [&](long long cc) -> long long {
-      const long long gu_before = (cc * NG / G) * BG;
-      long long v = (cc * W / G - gu_before + BD / 2) / BD;
-      return v < 0 ? 0 : (v > ND ? ND : v);
-    };
-    long long m0 = 0, m1 = 0;
-    for (long long cc = lane; cc <= c + 1; cc += 32) {
-      const long long v = raw(cc);
-      if (cc <= c) m0 = v > m0 ? v : m0;
-      m1 = v > m1 ? v : m1;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const long long t0 = __shfl_xor_sync(0xffffffffu, m0, o);
-      const long long t1 = __shfl_xor_sync(0xffffffffu, m1, o);
-      m0 = t0 > m0 ? t0 : m0;
-      m1 = t1 > m1 ? t1 : m1;
-    }
-    if (lane == 0) {
-      s_g0 = (int)(c * NG / G);
-      s_g1 = (int)((c + 1) * NG / G);
-      s_d0 = (int)m0;
-      s_d1 = c + 1 == G ? (int)ND : (int)m1;
-      s_nexp = n_exp;
-    }
+  if (tid == 0) {
+    const int n = s_nexp;
+    const int2 lo = s_part[n], hi = s_part[nx + n];
+    s_g0 = lo.x;
+    s_d0 = lo.y;
+    s_g1 = hi.x;
+    s_d1 = hi.y;
   }
   __syncthreads();
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 3);
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 3);
   const int g0 = s_g0, g1 = s_g1, d0 = s_d0, d1 = s_d1, n_exp = s_nexp;
   const int n_gt = g1 - g0, n_dt = d1 - d0;
   const int DPE = RD / RT;               // down tiles per expert
-  const Plan* P = a.plan;
   auto expert_base = [&](int ai) -> const uint8_t* {
-    return ai == 0 ? a.shared_expert : a.slots + (int64_t)P->act_slot[ai - 1] * a.expert_bytes;
+    return ai == 0 ? a.shared_expert : a.slots + (int64_t)s_act_slot[ai - 1] * a.expert_bytes;
   };
   const int a_first = n_dt > 0 ? d0 / DPE : 0;
   const int a_last = n_dt > 0 ? (d1 - 1) / DPE : -1;
@@ -250,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   if (warp == kCW) {
     // ---------------- producer: stages of every tile, in order -------------
     if (lane == 0) {
+      // the ring held generic-proxy scratch; order it before the bulk copies
+      fence_proxy_async_smem();
       uint32_t it = 0;
       bool ok = true;
       for (int ti = 0; ti < n_gt + n_dt && ok; ++ti) {
@@ -275,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           bulk_g2s(ring + (size_t)s * kStageBytes, tbase + (size_t)st * kStageBytes, kStageBytes, &full[s]);
         }
-        if (ti == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 4);
+        if (ti == 0) MOE_TL(g_ffn_timeline, cta, 4);
       }
-      MOE_TL(g_ffn_timeline, blockIdx.x, 5);
+      MOE_TL(g_ffn_timeline, cta, 5);
     }
   } else if (warp == kCW + 1) {
     // ---------------- h loader: one bulk copy of h_a per expert ------------
@@ -293,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           set_error(a.err, DEV_TIMEOUT_FLAG);
           break;
         }
-        if (i == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 8);
+        if (i == 0) MOE_TL(g_ffn_timeline, cta, 8);
         // h was written through the generic proxy by other CTAs; order it
         // before the bulk copy (async proxy) reads it
         asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -374,10 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           }
         }
         named_bar(1, kCW * 32);
-        if (ctid == 0) {
-          __threadfence();
-          red_release_add(&a.h_ready[ai], 1u);
-        }
+        if (ctid == 0) red_release_add(&a.h_ready[ai], 1u);
       } else {
         // ===== down tile: RT row blocks of Wd for expert ai =====
         const int td = d0 + ti - n_gt, ai = td / DPE, rp = td % DPE;
@@ -456,24 +536,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           }
         }
         named_bar(1, kCW * 32);
-        if (ctid < RT) {
-          __threadfence();
-          s_comb[ctid] = atomicAdd(&a.d_cnt[rp * RT + ctid], 1u) == (uint32_t)(n_exp - 1) ? 1 : 0;
-        }
+        if (ctid < RT)
+          s_comb[ctid] = atom_acq_rel_add(&a.d_cnt[rp * RT + ctid], 1u) == (uint32_t)(n_exp - 1) ? 1 : 0;
         named_bar(1, kCW * 32);
-        // combine the row blocks whose last expert this was (fixed order)
-        for (int r = 0; r < RT; ++r) {
+        // combine the row blocks whose last expert this was (fixed order); the
+        // loads of one (row block, token) are all issued before the sum
+        for (int q = warp; q < RT * T; q += kCW) {
+          const int r = q / T, t = q - r * T;
           if (!s_comb[r]) continue;
-          __threadfence();
           const int row = (rp * RT + r) * 32 + lane;
-          for (int t = warp; t < T; t += kCW) {
-            float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + row);
-            for (int k2 = 0; k2 < K; ++k2) {
-              const int ap = 1 + P->pick_act[t * K + k2];
-              yv = fmaf(P->w[t * K + k2], ld_cg_f32(a.obuf + ((size_t)ap * T + t) * d + row), yv);
-            }
-            a.y[(size_t)t * d + row] = yv;
-          }
+          float ov[kMaxTopK];
+#pragma unroll
+          for (int k2 = 0; k2 < kMaxTopK; ++k2)
+            ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + row) : 0.f;
+          float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + row);
+#pragma unroll
+          for (int k2 = 0; k2 < kMaxTopK; ++k2)
+            if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
+          a.y[(size_t)t * d + row] = yv;
         }
         named_bar(1, kCW * 32);   // s_comb is reused by the next tile
       }
@@ -482,18 +562,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
 
   // ---- the last CTA to finish clears the per-call counters ---------------
   __syncthreads();
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 11);
-  if (tid == 0) {
-    __threadfence();
-    s_last = (atomicAdd(a.done, 1u) == gridDim.x - 1);
-  }
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 11);
+  if (tid == 0) s_last = (atom_acq_rel_add(a.done, 1u) == (uint32_t)G - 1);
   __syncthreads();
   if (s_last) {
-    __threadfence();
     for (int i = tid; i < n_exp; i += kThreads) a.h_ready[i] = 0;
     for (int i = tid; i < RD; i += kThreads) a.d_cnt[i] = 0;
-    if (tid == 0) *a.done = 0;
-    if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 12);
+    if (tid == 0) {
+      *a.done = 0;
+      *a.gbar = 0;
+    }
+    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 12);
   }
 }
 
@@ -503,13 +582,15 @@ extern "C" int moe_debug_timeline_ffn(unsigned long long* out) {
 }
 #endif
 
-template <int NT>
+template <int NT, bool FUSED>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   const size_t smem = ffn_smem_bytes<NT>(a.d, a.f);
+  if (route_scratch_bytes(FUSED ? a.E : 0, a.nx) > (size_t)FfnCfg<NT>::kStages * kStageBytes)
+    return cudaErrorInvalidValue;
   // raise the dynamic shared-memory limit once per size (not during stream capture)
   static size_t configured = 0;
   if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
@@ -524,13 +605,35 @@ static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int gri
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel<NT>, a);
+  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel<NT, FUSED>, a);
 }
 
-cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl, int num_sms) {
-  const int grid = a.grid > 0 ? a.grid : num_sms;
-  if (a.T <= 8) return launch_nt<1>(a, s, pdl, grid);
-  return launch_nt<2>(a, s, pdl, grid);
+cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl) {
+  if (a.grid <= 0) return cudaErrorInvalidValue;
+  if (a.T <= 8) return a.fused ? launch_nt<1, true>(a, s, pdl, a.grid) : launch_nt<1, false>(a, s, pdl, a.grid);
+  return a.fused ? launch_nt<2, true>(a, s, pdl, a.grid) : launch_nt<2, false>(a, s, pdl, a.grid);
+}
+
+// CTA c of G takes gate/up tiles [g_c, g_c+1) of the n*f/32 (n = experts of
+// the call, shared one included): g_c = floor(c*NG/G).  Its down tiles
+// [d_c, d_c+1) make up the rest of an equal share of the call's blocks:
+// d_c = the rounded count of down tiles that the bytes of CTAs 0..c-1 leave
+// after their gate/up tiles, made monotone by a running maximum; d_G = all.
+void decode_partition(int G, int nx, int d, int f, int2* out) {
+  const int RT = down_rows_per_tile(f);
+  const long long RG = f / 32, DPE = (d / 32) / RT;
+  const long long BG = 2LL * (d / 32), BD = (long long)RT * (f / 32);   // blocks per tile
+  for (int n = 0; n < nx; ++n) {
+    const long long NG = n * RG, ND = n * DPE, W = NG * BG + ND * BD;
+    long long m = 0;
+    for (int c = 0; c <= G; ++c) {
+      const long long g = (long long)c * NG / G;
+      long long v = ((long long)c * W / G - g * BG + BD / 2) / BD;
+      v = v < 0 ? 0 : (v > ND ? ND : v);
+      m = v > m ? v : m;
+      out[(size_t)c * nx + n] = make_int2((int)g, c == G ? (int)ND : (int)m);
+    }
+  }
 }
 
 }  // namespace moe

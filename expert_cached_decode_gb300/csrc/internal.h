@@ -35,7 +35,7 @@ struct Plan {
   int32_t evicted_key[kMaxPicks];
 };
 
-enum RouteMode : int { ROUTE_ONLY = 0, ROUTE_RESIDENT = 1, ROUTE_PLAN = 2 };
+enum RouteMode : int { ROUTE_ONLY = 0, ROUTE_PLAN = 1 };
 
 // per-layer statistics block (int64 each)
 enum StatIdx : int {
@@ -93,16 +93,27 @@ struct FfnArgs {
   float* y;                     // [T][d]
   int T, d, f, k;
   float shared_weight;
-  const Plan* plan;
-  float* gu_partial;
+  Plan* plan;                   // read (after the routing kernel) or written (fused routing)
   uint16_t* hbuf;               // [max_exp][T][f] fp16 h of each expert
-  float* obuf;
-  uint32_t* gu_cnt;
-  uint32_t* h_ready;
-  uint32_t* d_cnt;
-  uint32_t* done;
+  float* obuf;                  // [max_exp][T][d] fp32 output of each expert
+  uint32_t* h_ready;            // [max_exp] gate/up tiles finished per expert
+  uint32_t* d_cnt;              // [d/32] experts finished per down row block
+  uint32_t* done;               // CTAs finished
+  uint32_t* gbar;               // CTAs past the router phase (fused routing)
   uint32_t* err;
+  const int2* part;             // [grid + 1][nx] (gate/up tile, down tile) start of each CTA, per expert count
+  int nx;
   int grid;
+  // fused routing (every key resident): router, slot table, LRU stamps, counters
+  int fused;
+  const uint16_t* wr;           // [E][d] bf16 (this layer)
+  const float* bias;            // [E] (this layer)
+  float* logits;                // [T][E] scratch
+  int E, layer;
+  const int32_t* table;         // [L*E]
+  int64_t* stamp;               // [C]
+  int64_t* stats;               // this layer's counters
+  int64_t* clock;
 };
 
 struct RouterGemmArgs {
@@ -191,6 +202,8 @@ cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16
 cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid);
 cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
                                 cudaStream_t s, int grid);
-cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl, int num_sms);
+cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
+// CTA work bounds of the decode kernel for grid G and expert counts 0..nx-1
+void decode_partition(int G, int nx, int d, int f, int2* out);
 
 }  // namespace moe

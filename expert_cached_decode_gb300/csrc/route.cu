@@ -22,6 +22,7 @@
 #include "moe_gb300.h"
 #include "common.cuh"
 #include "internal.h"
+#include "select.cuh"
 
 namespace moe {
 
@@ -31,10 +32,6 @@ __device__ unsigned long long g_route_timeline[256][16];
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
-
-__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
 
 // exclusive prefix sum over the 256 threads of the CTA; returns the total
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
@@ -69,217 +66,66 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, blockIdx.x, 0);
   pdl_launch_dependents();
 
-  __shared__ uint32_t s_mask[kMaxE / 32];
-  __shared__ int s_word_base[kMaxE / 32];
-  __shared__ int s_sel_id[kMaxDecodeT][kMaxTopK];
-  __shared__ float s_sel_w[kMaxDecodeT][kMaxTopK];
-  __shared__ int s_act[kMaxPicks];
+  __shared__ SelSmem sel;
   __shared__ int s_slot[kMaxPicks];
   __shared__ int s_hit[kMaxPicks];
   __shared__ int s_miss_act[kMaxPicks];
   __shared__ int s_victim[kMaxPicks];
   __shared__ uint32_t s_bits[kMaxSlots / 32];
   __shared__ int s_scan[kRouteWarps + 1];
-  __shared__ int s_last, s_n_act, s_n_miss;
-  __shared__ long long s_clock;
+  __shared__ int s_last, s_n_miss;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.T, d = a.d, E = a.E, K = a.k;
+  const int T = a.T, E = a.E, K = a.k;
+  // the clock of this call, fetched early (only the last CTA uses it)
+  const long long clock0 = (a.mode == ROUTE_PLAN && threadIdx.x == 0) ? (long long)*a.clock : 0;
 
   // ---- router logits: one warp per expert row, all T tokens -------------
   const int e = blockIdx.x * kRouteWarps + warp;
-  if (e < E) {
-    float acc[kMaxDecodeT];
-#pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.f;
-    const uint16_t* wrow = a.wr + (size_t)e * d;
-    // all loads of a 2048-wide block issued before the arithmetic (lane chunk
-    // j = lane*8 + 256*u, accumulated in u order)
-    for (int jb = 0; jb < d; jb += 2048) {
-      uint4 wv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = jb + lane * 8 + 256 * u;
-        wv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(wrow + j)) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int t = 0; t < kMaxDecodeT; ++t) {
-        if (t < T) {
-          uint4 xv[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = jb + lane * 8 + 256 * u;
-            xv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * d + j)) : make_uint4(0u, 0u, 0u, 0u);
-          }
-          float s = acc[t];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 w4 = wv[u], x4 = xv[u];
-            s = fmaf(bf16_bits_to_float(x4.x & 0xffffu), bf16_bits_to_float(w4.x & 0xffffu), s);
-            s = fmaf(bf16_bits_to_float(x4.x >> 16), bf16_bits_to_float(w4.x >> 16), s);
-            s = fmaf(bf16_bits_to_float(x4.y & 0xffffu), bf16_bits_to_float(w4.y & 0xffffu), s);
-            s = fmaf(bf16_bits_to_float(x4.y >> 16), bf16_bits_to_float(w4.y >> 16), s);
-            s = fmaf(bf16_bits_to_float(x4.z & 0xffffu), bf16_bits_to_float(w4.z & 0xffffu), s);
-            s = fmaf(bf16_bits_to_float(x4.z >> 16), bf16_bits_to_float(w4.z >> 16), s);
-            s = fmaf(bf16_bits_to_float(x4.w & 0xffffu), bf16_bits_to_float(w4.w & 0xffffu), s);
-            s = fmaf(bf16_bits_to_float(x4.w >> 16), bf16_bits_to_float(w4.w >> 16), s);
-          }
-          acc[t] = s;
-        }
-      }
-    }
-    const float b = a.bias[e];
-#pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) {
-      if (t < T) {
-        float v = acc[t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
-      }
-    }
-  }
+  if (e < E) router_row(a.wr + (size_t)e * a.d, a.x, a.bias[e], T, a.d, E, e, lane, a.logits);
 
   // ---- last CTA to arrive does the selection -----------------------------
   __syncthreads();
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, blockIdx.x, 1);
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(a.cnt, 1u);
-    s_last = (prev == gridDim.x - 1);
-  }
+  if (threadIdx.x == 0) s_last = (atom_acq_rel_add(a.cnt, 1u) == gridDim.x - 1);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
-  if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 0);
-
-  for (int i = threadIdx.x; i < kMaxE / 32; i += kRouteThreads) s_mask[i] = 0;
   if (threadIdx.x == 0) {
+    MOE_TL(g_route_timeline, 200, 0);
     *a.cnt = 0;   // ready for the next launch (stream-ordered)
-    s_clock = (a.mode == ROUTE_ONLY) ? 0 : (long long)*a.clock;
   }
-  __syncthreads();
-
-  // top-k per token, one warp per token
-  for (int t = warp; t < T; t += kRouteWarps) {
-    float my_v;
-    int my_id;
-    if (E <= 512) {
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int id = lane + 32 * i;
-        v[i] = id < E ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
-      }
-      warp_topk<16>(v, E, K, lane, my_v, my_id);
-    } else {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int id = lane + 32 * i;
-        v[i] = id < E ? ld_cg_f32(a.logits + (size_t)t * E + id) : -INFINITY;
-      }
-      warp_topk<32>(v, E, K, lane, my_v, my_id);
-    }
-    const float top = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < K ? expf(my_v - top) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    int rank = 0;
-    for (int j = 0; j < K; ++j) {
-      const int oid = __shfl_sync(0xffffffffu, my_id, j);
-      rank += (oid < my_id) ? 1 : 0;
-    }
-    if (lane < K) {
-      s_sel_id[t][rank] = my_id;
-      s_sel_w[t][rank] = ex / sum;
-      atomicOr(&s_mask[my_id >> 5], 1u << (my_id & 31));
-    }
-  }
-  __syncthreads();
-
+  select_call(a.logits, T, E, K, &sel);
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 1);
-  // distinct experts U, ascending
-  const int n_words = (E + 31) / 32;
-  if (warp == 0) {
-    const uint32_t m = lane < n_words ? s_mask[lane] : 0u;
-    const int c = __popc(m);
-    int inc = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += n;
-    }
-    const int base = inc - c;
-    if (lane < n_words) s_word_base[lane] = base;
-    if (lane == 31) s_n_act = inc;
-    uint32_t mm = m;
-    int pos = base;
-    while (mm) {
-      const int bit = __ffs(mm) - 1;
-      mm &= mm - 1;
-      s_act[pos++] = lane * 32 + bit;
-    }
-  }
-  __syncthreads();
-  const int n_act = s_n_act;
+  const int n_act = sel.n_act;
   Plan* P = a.plan;
 
   if (a.mode == ROUTE_ONLY) {
     for (int i = threadIdx.x; i < T * K; i += kRouteThreads) {
-      a.out_idx[i] = s_sel_id[i / K][i % K];
-      a.out_w[i] = s_sel_w[i / K][i % K];
+      a.out_idx[i] = sel.sel_id[i / K][i % K];
+      a.out_w[i] = sel.sel_w[i / K][i % K];
     }
     return;
   }
 
   // plan: routing part
   for (int i = threadIdx.x; i < T * K; i += kRouteThreads) {
-    const int id = s_sel_id[i / K][i % K];
+    const int id = sel.sel_id[i / K][i % K];
     P->idx[i] = id;
-    P->w[i] = s_sel_w[i / K][i % K];
-    P->pick_act[i] = s_word_base[id >> 5] + __popc(s_mask[id >> 5] & ((1u << (id & 31)) - 1u));
+    P->w[i] = sel.sel_w[i / K][i % K];
+    P->pick_act[i] = sel_act_index(&sel, id);
     if (a.out_idx) {
       a.out_idx[i] = id;
-      a.out_w[i] = s_sel_w[i / K][i % K];
+      a.out_w[i] = sel.sel_w[i / K][i % K];
     }
   }
   for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
-    const int slot = a.table[(size_t)a.layer * E + s_act[i]];
+    const int slot = a.table[(size_t)a.layer * E + sel.act[i]];
     s_slot[i] = slot;
     s_hit[i] = slot >= 0;
-    P->act_expert[i] = s_act[i];
+    P->act_expert[i] = sel.act[i];
   }
   __syncthreads();
-
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 2);
-  if (a.mode == ROUTE_RESIDENT) {
-    for (int i = threadIdx.x; i < n_act; i += kRouteThreads) {
-      int slot = s_slot[i];
-      if (slot < 0) {
-        set_error(a.err, DEV_NOT_RESIDENT);
-        slot = 0;
-      }
-      a.stamp[slot] = s_clock;
-      P->act_slot[i] = slot;
-      P->act_hit[i] = 1;
-    }
-    if (threadIdx.x == 0) {
-      P->n_act = n_act;
-      P->n_miss = 0;
-      P->T = T;
-      P->clock = s_clock;
-      P->token_hits = (int64_t)T * K;
-      P->token_misses = 0;
-      a.stats[ST_CALLS] += 1;
-      a.stats[ST_TOK_HIT] += (int64_t)T * K;
-      a.stats[ST_DIST_HIT] += n_act;
-      *a.clock = s_clock + 1;
-      MOE_TL(g_route_timeline, 200, 3);
-    }
-    return;
-  }
 
   // ---- ROUTE_PLAN: LRU victims and the next LRU order (no state commit) ---
   const int C = a.C;
@@ -339,7 +185,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     const int ai = s_miss_act[j];
     const int v = s_victim[j];
     s_slot[ai] = v;
-    P->miss_expert[j] = s_act[ai];
+    P->miss_expert[j] = sel.act[ai];
     P->miss_slot[j] = v;
     P->evicted_key[j] = a.owner[v];
   }
@@ -350,15 +196,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   }
   if (threadIdx.x == 0) {
     int64_t th = 0;
-    for (int i = 0; i < T * K; ++i) {
-      const int id = s_sel_id[i / K][i % K];
-      const int ai = s_word_base[id >> 5] + __popc(s_mask[id >> 5] & ((1u << (id & 31)) - 1u));
-      th += s_hit[ai];
-    }
+    for (int i = 0; i < T * K; ++i) th += s_hit[sel_act_index(&sel, sel.sel_id[i / K][i % K])];
     P->n_act = n_act;
     P->n_miss = m;
     P->T = T;
-    P->clock = s_clock;
+    P->clock = clock0;
     P->token_hits = th;
     P->token_misses = (int64_t)T * K - th;
   }
