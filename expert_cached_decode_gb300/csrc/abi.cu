@@ -92,12 +92,9 @@ struct moe_ctx {
   Plan* plan_host = nullptr;  // pinned
   uint16_t* hbuf = nullptr;      // [max_exp][16][f] fp16
   float* obuf = nullptr;
-  uint32_t* counters = nullptr;  // h_ready | d_cnt | done | gbar
+  uint32_t* counters = nullptr;  // decode calls | 2 sets of (h_ready | d_cnt | gbar)
   size_t counters_n = 0;
-  uint32_t* h_ready = nullptr;
-  uint32_t* d_cnt = nullptr;
-  uint32_t* done = nullptr;
-  uint32_t* gbar = nullptr;
+  int set_words = 0;
   int2* part = nullptr;          // [num_sms + 1][nx] decode work bounds
   int nx = 0;
   uint32_t* err = nullptr;
@@ -283,7 +280,6 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   }
   // scratch
   c->max_exp = (kMaxDecodeT * c->k < c->E ? kMaxDecodeT * c->k : c->E) + 1;
-  const int RD = c->d / 32;
   CREATE_TRY(cudaMalloc(&c->logits, (size_t)kMaxDecodeT * c->E * sizeof(float)));
   CREATE_TRY(cudaMalloc(&c->route_cnt, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
@@ -292,13 +288,10 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
   CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
   CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
-  c->counters_n = (size_t)c->max_exp + RD + 2;
+  c->set_words = c->max_exp + 2;
+  c->counters_n = 1 + 2 * (size_t)c->set_words;
   CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
-  c->h_ready = c->counters;
-  c->d_cnt = c->h_ready + c->max_exp;
-  c->done = c->d_cnt + RD;
-  c->gbar = c->done + 1;
   {
     c->nx = c->max_exp + 1;
     std::vector<int2> part((size_t)(c->num_sms + 1) * c->nx);
@@ -510,7 +503,7 @@ static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
   CUDA_TRY(cudaMalloc(&c->p_wsort, (size_t)rows * sizeof(float)));
   CUDA_TRY(cudaMalloc(&c->p_cursor, (size_t)c->E * sizeof(int32_t)));
   CUDA_TRY(cudaMalloc(&c->p_group_slot, (size_t)(c->E + 1) * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->p_tiles_gu, (size_t)c->p_max_tiles * (c->f / 128) * sizeof(PrefillTile)));
+  CUDA_TRY(cudaMalloc(&c->p_tiles_gu, (size_t)c->p_max_tiles * (c->f / 64) * sizeof(PrefillTile)));
   CUDA_TRY(cudaMalloc(&c->p_tiles_dn, (size_t)c->p_max_tiles * (c->d / 128) * sizeof(PrefillTile)));
   CUDA_TRY(cudaMalloc(&c->p_ntiles, 2 * sizeof(int32_t)));
   return MOE_OK;
@@ -575,10 +568,9 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.plan = c->plan;
   fa.hbuf = c->hbuf;
   fa.obuf = c->obuf;
-  fa.h_ready = c->h_ready;
-  fa.d_cnt = c->d_cnt;
-  fa.done = c->done;
-  fa.gbar = c->gbar;
+  fa.counters = c->counters;
+  fa.set_words = c->set_words;
+  fa.max_exp = c->max_exp;
   fa.err = c->err;
   fa.part = c->part;
   fa.nx = c->nx;
@@ -756,6 +748,8 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   CUDA_TRY(cudaStreamWaitEvent(s, c->ev_copy, 0));
   CommitArgs ca{};
   ca.plan = c->plan;
+  ca.counters = c->counters;
+  ca.set_words = c->set_words;
   ca.table = c->table;
   ca.owner = c->owner;
   ca.stamp = c->stamp;

@@ -114,6 +114,16 @@ __device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
   return old;
 }
 
+// CTA-scope release store / acquire load on shared memory
+__device__ __forceinline__ void st_release_cta_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 // Wait until *flag >= target (acquire); false if the wait gave up.
 __device__ __forceinline__ bool wait_flag_geq(const uint32_t* flag, uint32_t target) {
   if (ld_acquire_u32(flag) >= target) return true;
@@ -256,56 +266,119 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// One warp selects the K largest of its E values (lane holds entries
-// id = lane + 32*i, i < VPL; ties go to the lower id).  Each lane first sorts
-// its own (key, ~id) pairs descending with a bitonic network; then each of
-// the K rounds takes the warp maximum of the lane heads with two redux.sync
-// reductions (largest key, then smallest id among equal keys) and the owner
-// pops its head.  Lane r < K receives the r-th largest value and its id.
-template <int VPL>
-__device__ __forceinline__ void warp_topk(const float (&v)[VPL], int E, int K, int lane, float& out_v, int& out_id) {
-  uint64_t s[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int id = lane + 32 * i;
-    s[i] = id < E ? ((uint64_t)float_key(v[i]) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
-  }
-  // bitonic sort, descending
-#pragma unroll
-  for (int k = 2; k <= VPL; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int l = i ^ j;
-        if (l > i) {
-          const bool desc = (i & k) == 0;
-          const uint64_t a = s[i], b = s[l];
-          const bool swap = desc ? (a < b) : (a > b);
-          s[i] = swap ? b : a;
-          s[l] = swap ? a : b;
-        }
-      }
-    }
-  }
-  out_v = -INFINITY;
-  out_id = 0x7fffffff;
-  for (int r = 0; r < K; ++r) {
-    const uint32_t hk = (uint32_t)(s[0] >> 32);
-    const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
-    const uint32_t hid = ~(uint32_t)s[0];
-    const uint32_t win = __reduce_min_sync(0xffffffffu, hk == m ? hid : 0xffffffffu);
-    if (lane == r) {
-      out_v = key_float(m);
-      out_id = (int)win;
-    }
-    if (hk == m && hid == win) {
-#pragma unroll
-      for (int i = 0; i + 1 < VPL; ++i) s[i] = s[i + 1];
-      s[VPL - 1] = 0ull;
-    }
-  }
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+  const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+  return ((uint64_t)hi << 32) | lo;
 }
 
+// u64 entries of per-warp scratch that warp_topk needs
+constexpr int kTopkScratch = 80;
+constexpr int kTopkMaxCand = 64;
+
+// Key of entry `id` of a logits row: (value key, ~id), so larger values and,
+// among equal values, lower ids compare larger; all keys of a row differ.
+__device__ __forceinline__ uint64_t topk_key(const float* row, int id) {
+  return ((uint64_t)float_key(row[id]) << 32) | (uint32_t)(~(uint32_t)id);
+}
+
+// One warp selects the K largest (K <= 16, K < E <= 1024) entries of `row`
+// (shared memory; ties go to the lower id).  Lane l owns entries l, l+32, ...
+// The K-th largest of the 32 lane maxima is a threshold that at least K
+// entries reach and that every one of the K largest reaches; the few entries
+// at or above it are ranked against each other in `scratch` (kTopkScratch
+// entries of this warp).  More than kTopkMaxCand candidates (possible only
+// when the largest values crowd into few lanes) take the general route: K
+// rounds of the warp maximum of the remaining entries (two redux.sync
+// reductions: largest key, then smallest id).  Lane r < K receives the r-th
+// largest value and its id.  Loops stay short: this runs once per call, so
+// code size matters more than instruction count.
+__device__ __forceinline__ void warp_topk(const float* row, int E, int K, int lane, uint64_t* scratch, float& out_v,
+                                          int& out_id) {
+  uint64_t m = 0;
+#pragma unroll 4
+  for (int id = lane; id < E; id += 32) {
+    const uint64_t k = topk_key(row, id);
+    m = k > m ? k : m;
+  }
+  // bitonic sort of the lane maxima across the warp, descending
+  uint64_t t = m;
+#pragma unroll 1
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = shfl_xor_u64(t, j);
+      const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
+      t = keep_max ? (o > t ? o : t) : (o < t ? o : t);
+    }
+  }
+  const uint64_t tau = shfl_u64(t, K - 1);
+  int cnt = 0;
+#pragma unroll 4
+  for (int id = lane; id < E; id += 32) cnt += topk_key(row, id) >= tau ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const int n_c = __shfl_sync(0xffffffffu, incl, 31);
+  out_v = -INFINITY;
+  out_id = 0x7fffffff;
+  if (n_c <= kTopkMaxCand) {
+    int pos = incl - cnt;
+#pragma unroll 1
+    for (int id = lane; id < E; id += 32) {
+      const uint64_t k = topk_key(row, id);
+      if (k >= tau) scratch[pos++] = k;
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int q = lane; q < n_c; q += 32) {
+      const uint64_t me = scratch[q];
+      int r = 0;
+#pragma unroll 4
+      for (int j2 = 0; j2 < n_c; ++j2) r += scratch[j2] > me ? 1 : 0;
+      if (r < K) scratch[kTopkMaxCand + r] = me;
+    }
+    __syncwarp();
+    if (lane < K) {
+      const uint64_t w = scratch[kTopkMaxCand + lane];
+      out_v = key_float((uint32_t)(w >> 32));
+      out_id = (int)~(uint32_t)w;
+    }
+    __syncwarp();   // scratch is reused by the warp's next selection
+    return;
+  }
+  // general route; `taken` marks this lane's entries already chosen
+  uint32_t taken = 0;
+#pragma unroll 1
+  for (int r = 0; r < K; ++r) {
+    uint64_t lm = 0;
+    int li = 0;
+#pragma unroll 1
+    for (int i = 0, id = lane; id < E; ++i, id += 32) {
+      const uint64_t k = topk_key(row, id);
+      if (!((taken >> i) & 1u) && k > lm) {
+        lm = k;
+        li = i;
+      }
+    }
+    const uint32_t hk = (uint32_t)(lm >> 32);
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t hid = ~(uint32_t)lm;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, hk == mx ? hid : 0xffffffffu);
+    if (lane == r) {
+      out_v = key_float(mx);
+      out_id = (int)win;
+    }
+    if (hk == mx && hid == win) taken |= 1u << li;
+  }
+}
 
 }  // namespace moe

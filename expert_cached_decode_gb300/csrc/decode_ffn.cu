@@ -42,11 +42,13 @@ __device__ unsigned long long g_ffn_timeline[512][16];
 #endif
 
 constexpr int kCW = 8;                        // consumer warps
-constexpr int kThreads = (kCW + 2) * 32;      // + producer warp + h-loader warp
+constexpr int kThreads = (kCW + 3) * 32;      // + producer, h-loader and publisher warps
 constexpr int kStageBlocks = 16;
 constexpr int kStageBytes = kStageBlocks * kBlockBytes;   // 7,168
 constexpr int kHSlots = 2;
 constexpr int kMaxRT = 4;                     // row blocks per down tile, at most
+constexpr int kTabPerThread = (kMaxE + kThreads - 1) / kThreads;   // slot-table entries per thread
+constexpr int kXPerThread = 4;                // 16-byte x chunks per thread loaded up front
 
 template <int NT>
 struct FfnCfg {
@@ -62,6 +64,10 @@ __host__ __device__ __forceinline__ int down_rows_per_tile(int f) {
 }
 
 __host__ __device__ __forceinline__ int h_row_bytes(int f) { return (f + 8) * 2; }
+
+// elements per staged x row: 32 bytes of padding put the 4 token rows that
+// one fragment-building load touches on distinct banks
+__host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
 
 // floats per lane of one warp's partials: gate/up 16 per token tile, down 8
 // per row block and token tile; +1 keeps the lanes on distinct banks
@@ -92,13 +98,13 @@ __device__ __forceinline__ void scales4(const uint8_t* bp, int lane, float s[4])
   s[3] = hi.y;   // row g+24
 }
 
-// One 32x32 block: acc[nt][mt][i] += scale(row) * (A_block . B_frag[nt])
+// One 32x32 block: D[nt][mt] = A_block . B_frag[nt] (fp32, unscaled) and the
+// scales of the lane's rows g, g+8, g+16, g+24.
 template <int NT>
-__device__ __forceinline__ void block_mma(const uint8_t* bp, int lane, const uint2 (&bx)[NT][2],
-                                          float (&acc)[NT][2][4]) {
+__device__ __forceinline__ void block_products(const uint8_t* bp, int lane, const uint2 (&bx)[NT][2],
+                                               float (&D)[NT][2][4], float (&s)[4]) {
   const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
   const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
-  float s[4];
   scales4(bp, lane, s);
   uint32_t A[16];
   dequant_block(w0, w1, w2, A);
@@ -107,16 +113,34 @@ __device__ __forceinline__ void block_mma(const uint8_t* bp, int lane, const uin
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      float D[4];
-      mma_16816(D, &A[mt * 8], bx[nt][0].x, bx[nt][0].y, zero);
-      mma_16816(D, &A[mt * 8 + 4], bx[nt][1].x, bx[nt][1].y, D);
-      const float sa = s[2 * mt], sb = s[2 * mt + 1];
-      acc[nt][mt][0] = fmaf(sa, D[0], acc[nt][mt][0]);
-      acc[nt][mt][1] = fmaf(sa, D[1], acc[nt][mt][1]);
-      acc[nt][mt][2] = fmaf(sb, D[2], acc[nt][mt][2]);
-      acc[nt][mt][3] = fmaf(sb, D[3], acc[nt][mt][3]);
+      mma_16816(D[nt][mt], &A[mt * 8], bx[nt][0].x, bx[nt][0].y, zero);
+      mma_16816(D[nt][mt], &A[mt * 8 + 4], bx[nt][1].x, bx[nt][1].y, D[nt][mt]);
     }
   }
+}
+
+// acc[nt][mt][i] += scale(row) * D[nt][mt][i]
+template <int NT>
+__device__ __forceinline__ void block_accum(const float (&D)[NT][2][4], const float (&s)[4], float (&acc)[NT][2][4]) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const float sa = s[2 * mt], sb = s[2 * mt + 1];
+      acc[nt][mt][0] = fmaf(sa, D[nt][mt][0], acc[nt][mt][0]);
+      acc[nt][mt][1] = fmaf(sa, D[nt][mt][1], acc[nt][mt][1]);
+      acc[nt][mt][2] = fmaf(sb, D[nt][mt][2], acc[nt][mt][2]);
+      acc[nt][mt][3] = fmaf(sb, D[nt][mt][3], acc[nt][mt][3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void block_mma(const uint8_t* bp, int lane, const uint2 (&bx)[NT][2],
+                                          float (&acc)[NT][2][4]) {
+  float D[NT][2][4], s[4];
+  block_products<NT>(bp, lane, bx, D, s);
+  block_accum<NT>(D, s, acc);
 }
 
 template <int NT>
@@ -183,10 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   __shared__ int s_act_slot[kMaxPicks];   // slot of each distinct routed expert
   __shared__ int s_pick_act[kMaxPicks];   // [T][k] index of each pick in the distinct list
   __shared__ float s_w[kMaxPicks];        // [T][k] routing weights
-  __shared__ int s_g0, s_g1, s_d0, s_d1, s_nexp, s_last;
+  __shared__ int s_g0, s_g1, s_d0, s_d1, s_nexp;
+  __shared__ uint32_t s_calls;
   __shared__ long long s_clock;
   __shared__ volatile int s_hexp[kHSlots];
-  __shared__ int s_comb[kMaxRT];
+  __shared__ uint32_t s_gu_done;          // gate/up tiles of this CTA whose h is written
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x, nx = a.nx;
@@ -201,36 +226,105 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       mbar_init(&hempty[i], 1);
       s_hexp[i] = -1;
     }
+    s_gu_done = 0;
     mbar_init_fence();
   }
-  // x, the slot table and the clock may be written by earlier work in the
-  // stream: the fused kernel waits for it before reading anything
+  // Every load of the prologue is issued before any of them is used, so the
+  // prologue costs about one memory round trip.  Static inputs first: work
+  // bounds of this CTA and the next for every expert count; with fused
+  // routing also the slot table row (every key is resident, so it does not
+  // change) and the first block of this warp's router row.
+  const int2 pv0 = tid < 2 * nx ? a.part[(size_t)cta * nx + tid] : make_int2(0, 0);
+  const int2 pv1 = tid + kThreads < 2 * nx ? a.part[(size_t)cta * nx + tid + kThreads] : make_int2(0, 0);
+  int tv[kTabPerThread];
+  uint4 wfirst[8];
+  float wbias = 0.f;
   if (FUSED) {
+#pragma unroll
+    for (int q = 0; q < kTabPerThread; ++q) {
+      const int i = tid + q * kThreads;
+      tv[q] = i < a.E ? a.table[(size_t)a.layer * a.E + i] : -1;
+    }
+    const int e = cta + G * warp;
+    if (e < a.E) {
+      router_load_block(a.wr + (size_t)e * d, 0, d, lane, wfirst);
+      wbias = a.bias[e];
+    }
     pdl_launch_dependents();
-    pdl_wait();
   }
-  // work bounds of this CTA and the next for every expert count
-  for (int i = tid; i < 2 * nx; i += kThreads) s_part[i] = a.part[(size_t)cta * nx + i];
+  // x, the clock and the counters may be written by earlier work in the
+  // stream
+  pdl_wait();
+  uint32_t calls = 0;
+  long long clk = 0;
+  if (tid == 0) {
+    calls = *a.counters;
+    if (FUSED && cta == 0) clk = (long long)*a.clock;
+  }
+  // x (bf16) staged once in shared memory, rows xs apart, in the h / partial
+  // area that is free until the first tile ends; the router and the gate/up
+  // fragments read it there
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(hbuf);
+  const int xs = x_row_elems(d);
+  const int cpr = d / 8;
+  uint4 xv[kXPerThread];
+#pragma unroll
+  for (int q = 0; q < kXPerThread; ++q) {
+    const int i = tid + q * kThreads;
+    if (i < T * cpr) {
+      const int n = i / cpr, c = i - n * cpr;
+      xv[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
+    }
+  }
+  // now the stores
+  if (tid < 2 * nx) s_part[tid] = pv0;
+  if (tid + kThreads < 2 * nx) s_part[tid + kThreads] = pv1;
   if (FUSED) {
-    for (int i = tid; i < a.E; i += kThreads) s_tab[i] = a.table[(size_t)a.layer * a.E + i];
-    if (tid == 0) s_clock = cta == 0 ? (long long)*a.clock : 0;
+#pragma unroll
+    for (int q = 0; q < kTabPerThread; ++q)
+      if (tid + q * kThreads < a.E) s_tab[tid + q * kThreads] = tv[q];
   }
+  if (tid == 0) {
+    s_calls = calls;
+    s_clock = clk;
+  }
+#pragma unroll
+  for (int q = 0; q < kXPerThread; ++q) {
+    const int i = tid + q * kThreads;
+    if (i < T * cpr) {
+      const int n = i / cpr, c = i - n * cpr;
+      *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) = xv[q];
+    }
+  }
+  for (int i = tid + kXPerThread * kThreads; i < T * cpr; i += kThreads) {   // large T*d only
+    const int n = i / cpr, c = i - n * cpr;
+    *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) =
+        __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
+  }
+  __syncthreads();
   // x fragments (B operand of the gate/up products), fp16, zero past T.
-  // Entry (nt, kstep, lane) holds tokens nt*8 + lane/4, inputs
-  // kstep*16 + 2*(lane%4) + {0, 1} (reg 0) and + {8, 9} (reg 1).
+  // Word (nt, kstep, lane, reg), in that order, holds token nt*8 + lane/4,
+  // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one.
   {
     uint32_t* xf = reinterpret_cast<uint32_t*>(xfrag);
-    const int cpr = d / 8;
-    for (int i = tid; i < NT * 8 * cpr; i += kThreads) {
-      const int n = i / cpr, k8 = (i % cpr) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (n < T) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + k8));
-      const int nt = n >> 3, kstep = k8 >> 4, reg = (k8 >> 3) & 1;
-      const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        xf[(((size_t)nt * nks + kstep) * 32 + (n & 7) * 4 + q) * 2 + reg] = pack_half2_from_bf16(in[q]);
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw);
+    for (int o = tid; o < NT * nks * 64; o += kThreads) {
+      const int reg = o & 1, lq = (o >> 1) & 31, ks_nt = o >> 6;
+      const int nt = ks_nt / nks, kstep = ks_nt - nt * nks;
+      const int n = nt * 8 + (lq >> 2), k = kstep * 16 + 2 * (lq & 3) + 8 * reg;
+      xf[o] = n < T ? pack_half2_from_bf16(xr[((size_t)n * xs + k) >> 1]) : 0u;
     }
+  }
+  __syncthreads();
+  // this call's counter set; the fused kernel's CTA 0 zeroes the other one
+  // (the previous call's, complete by now) for the next call
+  const uint32_t call_set = FUSED ? (s_calls & 1u) : ((s_calls - 1u) & 1u);
+  uint32_t* const h_ready = a.counters + 1 + (size_t)call_set * a.set_words;
+  uint32_t* const gbar = h_ready + a.max_exp;    // CTAs past the router phase
+  uint32_t* const gbar_end = gbar + 1;           // CTAs whose expert outputs are written
+  if (FUSED && cta == 0) {
+    uint32_t* other = a.counters + 1 + (size_t)(call_set ^ 1u) * a.set_words;
+    for (int i = tid; i < a.set_words; i += kThreads) other[i] = 0;
   }
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 1);
 
@@ -240,14 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     for (int j = warp;; j += kThreads / 32) {
       const int e = cta + G * j;
       if (e >= E) break;
-      router_row(a.wr + (size_t)e * d, a.x, a.bias[e], T, d, E, e, lane, a.logits);
+      const uint16_t* wrow = a.wr + (size_t)e * d;
+      if (j != warp) {
+        router_load_block(wrow, 0, d, lane, wfirst);
+        wbias = a.bias[e];
+      }
+      router_row(wrow, wfirst, xraw, xs, wbias, T, d, E, e, lane, a.logits);
     }
     __syncthreads();
     if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
     // ---- every CTA's logits are written -----------------------------------
     if (tid == 0) {
-      red_release_add(a.gbar, 1u);
-      if (!wait_flag_geq(a.gbar, (uint32_t)G)) set_error(a.err, DEV_TIMEOUT_FLAG);
+      red_release_add(gbar, 1u);
+      if (!wait_flag_geq(gbar, (uint32_t)G)) set_error(a.err, DEV_TIMEOUT_FLAG);
       MOE_TL(g_ffn_timeline, cta, 7);
     }
     __syncthreads();
@@ -294,11 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         a.stats[ST_TOK_HIT] += (int64_t)T * K;
         a.stats[ST_DIST_HIT] += n_act;
         *a.clock = clk + 1;
+        *a.counters = s_calls + 1;   // every CTA read the count before the grid barrier
       }
     }
   } else {
-    pdl_wait();   // the routing plan is complete and visible
-    const Plan* P = a.plan;
+    const Plan* P = a.plan;   // the routing plan is complete and visible
     for (int i = tid; i < kMaxPicks; i += kThreads) s_act_slot[i] = P->act_slot[i];
     for (int i = tid; i < T * K; i += kThreads) {
       s_pick_act[i] = P->pick_act[i];
@@ -319,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   }
   __syncthreads();
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 3);
-  const int g0 = s_g0, g1 = s_g1, d0 = s_d0, d1 = s_d1, n_exp = s_nexp;
+  const int g0 = s_g0, g1 = s_g1, d0 = s_d0, d1 = s_d1;
   const int n_gt = g1 - g0, n_dt = d1 - d0;
   const int DPE = RD / RT;               // down tiles per expert
   auto expert_base = [&](int ai) -> const uint8_t* {
@@ -357,14 +456,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           }
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           bulk_g2s(ring + (size_t)s * kStageBytes, tbase + (size_t)st * kStageBytes, kStageBytes, &full[s]);
+          if (it == 0) MOE_TL(g_ffn_timeline, cta, 15);
         }
         if (ti == 0) MOE_TL(g_ffn_timeline, cta, 4);
       }
       MOE_TL(g_ffn_timeline, cta, 5);
+      // no copy may still be in flight when the CTA exits (consumers that
+      // gave up on a wait skip theirs): wait, bounded, for the last ones
+      for (uint32_t k = it > (uint32_t)NS ? it - NS : 0; k < it; ++k)
+        if (!mbar_wait(&full[k % NS], (k / NS) & 1)) set_error(a.err, DEV_TIMEOUT_BARRIER);
     }
   } else if (warp == kCW + 1) {
     // ---------------- h loader: one bulk copy of h_a per expert ------------
     if (lane == 0) {
+      fence_proxy_async_smem();   // the h area held x through the generic proxy
+      int armed = 0;
       for (int ai = a_first, i = 0; ai <= a_last; ++ai, ++i) {
         const int hs = i % kHSlots;
         const int use = i / kHSlots;
@@ -372,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           break;
         }
-        if (!wait_flag_geq(&a.h_ready[ai], (uint32_t)RG)) {
+        if (!wait_flag_geq(&h_ready[ai], (uint32_t)RG)) {
           set_error(a.err, DEV_TIMEOUT_FLAG);
           break;
         }
@@ -385,7 +491,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         mbar_arrive_expect_tx(&hfull[hs], (uint32_t)(T * f * 2));
         for (int t = 0; t < T; ++t)
           bulk_g2s(dst + (size_t)t * hrow, a.hbuf + ((size_t)ai * T + t) * f, (uint32_t)(f * 2), &hfull[hs]);
+        armed = i + 1;
       }
+      MOE_TL(g_ffn_timeline, cta, 14);
+      for (int k = armed > kHSlots ? armed - kHSlots : 0; k < armed; ++k)
+        if (!mbar_wait(&hfull[k % kHSlots], (uint32_t)((k / kHSlots) & 1))) set_error(a.err, DEV_TIMEOUT_BARRIER);
+    }
+  } else if (warp == kCW + 2) {
+    // ---------------- publisher: makes finished h visible to other CTAs ----
+    // (the gpu-scope release waits for the writes; consumers never block on it)
+    if (lane == 0) {
+      int k = 0;
+      while (k < n_gt) {
+        uint32_t done = ld_acquire_cta_u32(&s_gu_done);
+        if (done <= (uint32_t)k) {
+          const uint64_t t0 = globaltimer();
+          while ((done = ld_acquire_cta_u32(&s_gu_done)) <= (uint32_t)k) {
+            __nanosleep(32);
+            if (globaltimer() - t0 > kWaitLimitNs) break;
+          }
+          if (done <= (uint32_t)k) {
+            set_error(a.err, DEV_TIMEOUT_FLAG);
+            break;
+          }
+        }
+        while (k < (int)done) {
+          const int ai = (g0 + k) / RG;
+          uint32_t cnt = 0;
+          while (k < (int)done && (g0 + k) / RG == ai) {
+            ++cnt;
+            ++k;
+          }
+          red_release_add(&h_ready[ai], cnt);
+        }
+      }
+      MOE_TL(g_ffn_timeline, cta, 9);
     }
   } else {
     // ---------------- consumers: 8 warps on every stage --------------------
@@ -457,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           }
         }
         named_bar(1, kCW * 32);
-        if (ctid == 0) red_release_add(&a.h_ready[ai], 1u);
+        if (ctid == 0) st_release_cta_u32(&s_gu_done, (uint32_t)(ti + 1));
       } else {
         // ===== down tile: RT row blocks of Wd for expert ai =====
         const int td = d0 + ti - n_gt, ai = td / DPE, rp = td % DPE;
@@ -476,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           ok = false;
         }
+        if (ctid == 0 && ti == n_gt) MOE_TL(g_ffn_timeline, cta, 10);
         const uint8_t* hb = hbuf + (size_t)hs * NT * 8 * hrow;
         float acc[kMaxRT][NT][2][4];
 #pragma unroll
@@ -487,16 +628,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
             ok = false;
           }
           if (ok) {
+            // this warp's two blocks of the stage: products first (independent,
+            // so they overlap), then each is added to its row block's sums
             const uint8_t* sp = ring + (size_t)s * kStageBytes;
+            const int b0 = st * kStageBlocks + warp, b1 = b0 + kCW;   // blocks of the tile
+            const int rl0 = b0 / DG, rl1 = b1 / DG;
+            uint2 bx0[NT][2], bx1[NT][2];
+            h_frags<NT>(hb, hrow, T, b0 - rl0 * DG, lane, bx0);
+            h_frags<NT>(hb, hrow, T, b1 - rl1 * DG, lane, bx1);
+            float D0[NT][2][4], D1[NT][2][4], s0[4], s1[4];
+            block_products<NT>(sp + warp * kBlockBytes, lane, bx0, D0, s0);
+            block_products<NT>(sp + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int b = st * kStageBlocks + warp + half * kCW;   // block of the tile
-              const int rl = b / DG, gi = b % DG;
-              uint2 bx[NT][2];
-              h_frags<NT>(hb, hrow, T, gi, lane, bx);
-#pragma unroll
-              for (int r = 0; r < kMaxRT; ++r)
-                if (r == rl) block_mma<NT>(sp + (warp + half * kCW) * kBlockBytes, lane, bx, acc[r]);
+            for (int r = 0; r < kMaxRT; ++r) {
+              if (r == rl0) block_accum<NT>(D0, s0, acc[r]);
+              if (r == rl1) block_accum<NT>(D1, s1, acc[r]);
             }
           }
           __syncwarp();
@@ -535,44 +681,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
             }
           }
         }
-        named_bar(1, kCW * 32);
-        if (ctid < RT)
-          s_comb[ctid] = atom_acq_rel_add(&a.d_cnt[rp * RT + ctid], 1u) == (uint32_t)(n_exp - 1) ? 1 : 0;
-        named_bar(1, kCW * 32);
-        // combine the row blocks whose last expert this was (fixed order); the
-        // loads of one (row block, token) are all issued before the sum
-        for (int q = warp; q < RT * T; q += kCW) {
-          const int r = q / T, t = q - r * T;
-          if (!s_comb[r]) continue;
-          const int row = (rp * RT + r) * 32 + lane;
-          float ov[kMaxTopK];
-#pragma unroll
-          for (int k2 = 0; k2 < kMaxTopK; ++k2)
-            ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + row) : 0.f;
-          float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + row);
-#pragma unroll
-          for (int k2 = 0; k2 < kMaxTopK; ++k2)
-            if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
-          a.y[(size_t)t * d + row] = yv;
-        }
-        named_bar(1, kCW * 32);   // s_comb is reused by the next tile
+        named_bar(1, kCW * 32);   // the partial buffer is reused by the next tile
       }
     }
-  }
-
-  // ---- the last CTA to finish clears the per-call counters ---------------
-  __syncthreads();
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 11);
-  if (tid == 0) s_last = (atom_acq_rel_add(a.done, 1u) == (uint32_t)G - 1);
-  __syncthreads();
-  if (s_last) {
-    for (int i = tid; i < n_exp; i += kThreads) a.h_ready[i] = 0;
-    for (int i = tid; i < RD; i += kThreads) a.d_cnt[i] = 0;
-    if (tid == 0) {
-      *a.done = 0;
-      *a.gbar = 0;
+    if (ctid == 0) MOE_TL(g_ffn_timeline, cta, 11);
+    // ---- every CTA's expert outputs are written: combine this CTA's slice
+    // of y in a fixed order (shared expert, then the picks in ascending id);
+    // the loads of one output are all issued before the sum
+    named_bar(1, kCW * 32);
+    if (ctid == 0) {
+      red_release_add(gbar_end, 1u);
+      if (!wait_flag_geq(gbar_end, (uint32_t)G)) set_error(a.err, DEV_TIMEOUT_FLAG);
+      MOE_TL(g_ffn_timeline, cta, 12);
     }
-    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 12);
+    named_bar(1, kCW * 32);
+    const int total = T * d;
+    const int q1 = (int)((long long)(cta + 1) * total / G);
+    for (int q = (int)((long long)cta * total / G) + ctid; q < q1; q += kCW * 32) {
+      const int t = q / d, r = q - t * d;
+      float ov[kMaxTopK];
+#pragma unroll
+      for (int k2 = 0; k2 < kMaxTopK; ++k2)
+        ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + r) : 0.f;
+      float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + r);
+#pragma unroll
+      for (int k2 = 0; k2 < kMaxTopK; ++k2)
+        if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
+      a.y[q] = yv;
+    }
+    if (ctid == 0) MOE_TL(g_ffn_timeline, cta, 13);
   }
 }
 
@@ -585,7 +722,12 @@ extern "C" int moe_debug_timeline_ffn(unsigned long long* out) {
 template <int NT, bool FUSED>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   const size_t smem = ffn_smem_bytes<NT>(a.d, a.f);
-  if (route_scratch_bytes(FUSED ? a.E : 0, a.nx) > (size_t)FfnCfg<NT>::kStages * kStageBytes)
+  if (route_scratch_bytes(FUSED ? a.E : 0, a.nx) > (size_t)FfnCfg<NT>::kStages * kStageBytes ||
+      a.nx > kThreads || (FUSED && a.E > kTabPerThread * kThreads))
+    return cudaErrorInvalidValue;
+  // x is staged in the h + partial area
+  if ((size_t)a.T * x_row_elems(a.d) * 2 >
+      (size_t)kHSlots * NT * 8 * h_row_bytes(a.f) + (size_t)kCW * 32 * red_per_lane(a.f, NT) * 4)
     return cudaErrorInvalidValue;
   // raise the dynamic shared-memory limit once per size (not during stream capture)
   static size_t configured = 0;

@@ -66,6 +66,8 @@ struct RouteArgs {
 
 struct CommitArgs {
   const Plan* plan;
+  uint32_t* counters;       // decode counters (see FfnArgs)
+  int set_words;
   int32_t* table;
   int32_t* owner;
   int64_t* stamp;
@@ -96,10 +98,13 @@ struct FfnArgs {
   Plan* plan;                   // read (after the routing kernel) or written (fused routing)
   uint16_t* hbuf;               // [max_exp][T][f] fp16 h of each expert
   float* obuf;                  // [max_exp][T][d] fp32 output of each expert
-  uint32_t* h_ready;            // [max_exp] gate/up tiles finished per expert
-  uint32_t* d_cnt;              // [d/32] experts finished per down row block
-  uint32_t* done;               // CTAs finished
-  uint32_t* gbar;               // CTAs past the router phase (fused routing)
+  // per-call counters: word 0 counts decode calls; then two sets of
+  // set_words words (h_ready[max_exp] | router barrier | output barrier), used by
+  // alternate calls.  A call uses set (calls before it) & 1, and the set of
+  // the call before it is zeroed during the call (by the fused kernel's CTA 0,
+  // or by the commit kernel on the miss path).
+  uint32_t* counters;
+  int set_words, max_exp;
   uint32_t* err;
   const int2* part;             // [grid + 1][nx] (gate/up tile, down tile) start of each CTA, per expert count
   int nx;

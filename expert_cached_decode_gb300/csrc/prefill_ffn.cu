@@ -10,11 +10,13 @@
 // h is carried as an fp16 pair (hi = RN(h), lo = RN(h - hi)) and the down
 // GEMM accumulates Wd.hi + Wd.lo, so h keeps ~22 bits; the fp16 weight
 // RN(q * scale) is the only rounding of an operand.
-// Weights sit on the MMA M side (128 rows per tile), tokens on N (<= 256 per
-// tile, rounded up to 16).  Producer warps expand the 3-bit blocks of the
-// slot to fp16 RN(q * scale) straight into the 128-byte-swizzled K-major
-// operand tile; the token tile comes by TMA; one thread issues tcgen05.mma
-// into tensor memory; four epilogue warps read the accumulators back.
+// Weights sit on the MMA M side (128 rows per tile: 64 rows of Wg over the
+// same 64 rows of Wu for gate/up, 128 rows of Wd for down), tokens on N
+// (<= 256 per tile, rounded up to 16).  Eight producer warps expand the
+// 3-bit blocks of the slot to fp16 RN(q * scale) straight into the
+// 128-byte-swizzled K-major operand tile; the token tile comes by TMA; one
+// thread issues tcgen05.mma into a double-buffered tensor-memory accumulator;
+// four epilogue warps read it back while the next tile accumulates.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -71,7 +73,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillPlanArgs a) {
     __syncthreads();
   }
   const int n_ntiles = s_nt[n_groups];
-  const int MG = a.f / 128, MD = a.d / 128;
+  const int MG = a.f / 64, MD = a.d / 128;   // gate/up tiles cover 64 f rows (Wg and Wu)
   for (int g = tid; g < n_groups; g += 1024) {
     const int off = s_off[g];
     const int n = s_off[g + 1] - off;
@@ -155,54 +157,71 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, 
 // ---------------------------------------------------------- grouped GEMMs ---
 namespace pg {
 constexpr int BM = 128, BN = kPrefillBN, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB per weight matrix tile
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int NPROD = 4;               // dequant warps, one 32-row block each
-constexpr int PSTAGES = 3;             // packed-weight staging depth per producer
-constexpr int THREADS = 10 * 32;       // 0 TMA, 1 MMA, 2-5 producers, 6-9 epilogue
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB weight tile
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB token tile
+constexpr int NPROD = 8;               // dequant warps
+constexpr int PSTAGES = 4;             // packed-weight staging depth per producer
+constexpr int PCHUNK = 2 * kBlockBytes;   // packed bytes per producer and k block
+constexpr int EPI0 = 2 + NPROD;        // first epilogue warp
+constexpr int THREADS = (EPI0 + 4) * 32;   // 0 TMA, 1 MMA, 2-9 producers, 10-13 epilogue
+constexpr int GU_ROWS = BM / 2;        // f rows per gate/up tile (Wg rows, then the same Wu rows)
 }  // namespace pg
 
-// Expand one 32x32 block (448 B at `bp`, shared memory) into rows
-// [row_base, row_base+32) and k columns [k_base, k_base+32) of a swizzled
-// K-major fp16 tile, as RN(q * scale).
-__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint8_t* tile, int row_base,
-                                                      int k_base) {
+// Expand one 32x32 block (448 B at `bp`, shared memory) into 32 rows and 32
+// k columns of a 128-byte-swizzled K-major fp16 tile, as RN(q * scale).
+// `lane_base` is this lane's byte address in the tile for row offset 0 of
+// the block and chunk 0 before the swizzle (tile + row0*128 + g*128 + 4c);
+// gx = g << 4; KC = the first 16-byte chunk of the block's k columns (0 or 4).
+template <int KC>
+__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint32_t lane_base, uint32_t gx) {
   const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
   const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
   const uint2 sc = *reinterpret_cast<const uint2*>(bp + kBlockCodeBytes + (lane >> 2) * 8);
-  const uint32_t s2[4] = {(sc.x & 0xffffu) * 0x10001u, (sc.x >> 16) * 0x10001u, (sc.y & 0xffffu) * 0x10001u,
-                          (sc.y >> 16) * 0x10001u};
+  // scale of rows g, g+8, g+16, g+24, duplicated into both halves
+  const uint32_t s2[4] = {__byte_perm(sc.x, 0, 0x1010), __byte_perm(sc.x, 0, 0x3232), __byte_perm(sc.y, 0, 0x1010),
+                          __byte_perm(sc.y, 0, 0x3232)};
   uint32_t A[16];
   dequant_block(w0, w1, w2, A);
-  const int g = lane >> 2, c = lane & 3;
+  // register p = mt*8 + ks*4 + r holds rows mt*16 + g + 8*(r&1), k pair
+  // ks*16 + 2c + 8*(r>>1): 16-byte chunk KC + 2ks + (r>>1), bytes 4c
 #pragma unroll
-  for (int p = 0; p < 16; ++p) {
-    const int mt = p >> 3, ks = (p >> 2) & 1, r = p & 3;
-    const int row = row_base + mt * 16 + g + 8 * (r & 1);
-    const int k0 = k_base + ks * 16 + 2 * c + 8 * (r >> 1);
-    uint32_t v;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(A[p]), "r"(s2[2 * mt + (r & 1)]));
-    *reinterpret_cast<uint32_t*>(tile + sw128_offset(row, k0 >> 3) + (k0 & 7) * 2) = v;
+  for (int ch = 0; ch < 4; ++ch) {
+    const uint32_t addr = lane_base + ((uint32_t)((KC + ch) << 4) ^ gx);
+    const int ks = ch >> 1, rh = ch & 1;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int rl = 0; rl < 2; ++rl) {
+        const int pidx = mt * 8 + ks * 4 + rh * 2 + rl;
+        uint32_t v;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(A[pidx]), "r"(s2[2 * mt + rl]));
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr + (uint32_t)((mt * 2 + rl) * 1024)), "r"(v) : "memory");
+      }
+    }
   }
 }
 
-// DOWN = false: gate/up tiles (A = Wg and Wu blocks, two accumulators,
-// SwiGLU epilogue writing Hg).  DOWN = true: down tiles (A = Wd blocks, one
-// double-buffered accumulator, weighted atomic combine into y).
+// DOWN = false: gate/up tiles.  The 128-row weight tile holds 64 rows of Wg
+// (M rows 0-63) and the same 64 rows of Wu (M rows 64-127), so one
+// accumulator of 256 columns carries g and u side by side in tensor-memory
+// lanes, and two accumulators (double buffer) fit the 512 columns; the SwiGLU
+// epilogue writes Hg.  DOWN = true: 128 rows of Wd, weighted atomic combine
+// into y.  Producer warp p expands, for every k block of parity p/4, the two
+// blocks of its 32-row band p%4 (gate/up: band b is row block 2m + b%2 of Wg
+// for b < 2, of Wu otherwise, and the producer takes input group 2kb + b/2...
+// see psrc).
 template <bool DOWN>
 __global__ void __launch_bounds__(pg::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                         PrefillGemmArgs a) {
   using namespace pg;
-  constexpr int NMAT = DOWN ? 1 : 2;           // weight tiles per stage
   constexpr int NB = DOWN ? 2 : 1;             // token tiles per stage (down: h hi and lo)
   constexpr int STAGES = DOWN ? 2 : 3;
-  constexpr int STAGE_BYTES = NMAT * A_BYTES + NB * B_BYTES;
-  constexpr int PCHUNK = NMAT * 2 * kBlockBytes;    // packed bytes per producer per k block
+  constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  constexpr int EPI_BYTES = DOWN ? 32 * BM * 4 : 32 * BM * 2;     // fp32 / fp16 staging
+  constexpr int EPI_BYTES = DOWN ? 32 * BM * 4 : 32 * GU_ROWS * 4 + 2 * 32 * GU_ROWS * 2;
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint8_t* pstage = epi + EPI_BYTES;                               // NPROD * PSTAGES * PCHUNK
   uint64_t* bars = reinterpret_cast<uint64_t*>(pstage + NPROD * PSTAGES * PCHUNK);
@@ -219,12 +238,12 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = a.n_tiles[DOWN ? 1 : 0];
   const int K = DOWN ? a.f : a.d;
-  const int n_kb = K / BK;
+  const int n_kb = K / BK;   // even (K is a multiple of 128)
   const PrefillTile* tiles = DOWN ? a.tiles_dn : a.tiles_gu;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_a[i], NPROD);
+      mbar_init(&full_a[i], NPROD / 2);
       mbar_init(&full_b[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -249,11 +268,12 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   auto weights = [&](int group) -> const uint8_t* {
     return group < a.E ? a.slots + (int64_t)a.group_slot[group] * a.expert_bytes : a.shared_expert;
   };
-  // packed source of producer p for (tile, kb): contiguous PCHUNK bytes
+  // packed source of producer p for (tile, kb): two blocks, contiguous
+  //   down:    Wd row block 4m + p%4, input groups 2kb and 2kb+1;
+  //   gate/up: row block 2m + p%2, input group 2kb + (p/2)%2, Wg then Wu.
   auto psrc = [&](const PrefillTile& tl, int p, int kb) -> const uint8_t* {
-    const int rb = tl.m * 4 + p;
-    if (DOWN) return weights(tl.group) + down_block_offset(rb, 2 * kb, a.d, a.f);
-    return weights(tl.group) + gu_block_offset(rb, 2 * kb, 0, a.d);
+    if (DOWN) return weights(tl.group) + down_block_offset(tl.m * 4 + (p & 3), 2 * kb, a.d, a.f);
+    return weights(tl.group) + gu_block_offset(tl.m * 2 + (p & 1), 2 * kb + ((p >> 1) & 1), 0, a.d);
   };
 
   if (warp == 0) {
@@ -271,8 +291,8 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
           }
           uint8_t* st = stages + s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full_b[s], NB * B_BYTES);
-          tma_load_2d(st + NMAT * A_BYTES, &tmB, kb * BK, tl.row0, &full_b[s]);
-          if (DOWN) tma_load_2d(st + NMAT * A_BYTES + B_BYTES, &tmB2, kb * BK, tl.row0, &full_b[s]);
+          tma_load_2d(st + A_BYTES, &tmB, kb * BK, tl.row0, &full_b[s]);
+          if (DOWN) tma_load_2d(st + A_BYTES + B_BYTES, &tmB2, kb * BK, tl.row0, &full_b[s]);
         }
       }
     }
@@ -284,13 +304,14 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         const PrefillTile tl = tiles[ti];
         const int nmma = (tl.nlen + 15) & ~15;
         const uint32_t idesc = idesc_f16(BM, nmma, 0);
-        const int ab = DOWN ? (lt & 1) : 0;
-        const uint32_t use_b = DOWN ? (lt >> 1) : lt;
+        const int ab = lt & 1;
+        const uint32_t use_b = lt >> 1;
         if (use_b > 0 && !mbar_wait(&tempty[ab], (use_b - 1) & 1)) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           goto done;
         }
         tc_fence_after();
+        const uint32_t d_tmem = tmem + ab * BN;
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t par = (it / STAGES) & 1;
@@ -300,18 +321,14 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
           }
           tc_fence_after();
           uint8_t* st = stages + s * STAGE_BYTES;
-          const uint64_t db = smem_desc_sw128(st + NMAT * A_BYTES);
+          const uint64_t da = smem_desc_sw128(st);
+          const uint64_t db = smem_desc_sw128(st + A_BYTES);
 #pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) {
-            const uint64_t da = smem_desc_sw128(st + mat * A_BYTES);
-            const uint32_t d_tmem = tmem + (DOWN ? ab * BN : mat * BN);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              umma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
-              if (DOWN) {
-                const uint64_t db_lo = smem_desc_sw128(st + NMAT * A_BYTES + B_BYTES);
-                umma_f16(d_tmem, da + 2 * kk, db_lo + 2 * kk, idesc, 1u);
-              }
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            umma_f16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+            if (DOWN) {
+              const uint64_t db_lo = smem_desc_sw128(st + A_BYTES + B_BYTES);
+              umma_f16(d_tmem, da + 2 * kk, db_lo + 2 * kk, idesc, 1u);
             }
           }
           umma_commit(&empty[s]);
@@ -319,13 +336,23 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         umma_commit(&tfull[ab]);
       }
     }
-  } else if (warp < 2 + NPROD) {
+  } else if (warp < EPI0) {
     // ---- weight producers: 3-bit blocks -> fp16 swizzled tiles -------------
-    const int p = warp - 2;
+    // producer p takes the k blocks of parity p/4; per k block the 4
+    // producers of that parity expand 2 blocks each (the 8 blocks of the
+    // 128 x 64 tile)
+    const int p = warp - 2, par = p >> 2;
     uint8_t* my_stage = pstage + p * PSTAGES * PCHUNK;
     uint64_t* my_bar = pbar + p * PSTAGES;
-    // enumerate (tile, kb) items of this CTA
-    int ti_issue = blockIdx.x, kb_issue = 0;
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t gx = (uint32_t)g << 4;
+    // tile rows of this producer's first block, and the k chunk of each block
+    //   down:    rows (p%4)*32, k chunks 0 and 4 (input groups 2kb, 2kb+1);
+    //   gate/up: Wg rows (p%2)*32, Wu rows 64 + (p%2)*32, k chunk 4*((p/2)%2).
+    const int row0 = DOWN ? (p & 3) * 32 : (p & 1) * 32;
+    const uint32_t lane_off = (uint32_t)(row0 * 128 + g * 128 + 4 * c);
+    const bool hi_group = !DOWN && ((p >> 1) & 1);
+    int ti_issue = blockIdx.x, kb_issue = par;
     uint32_t n_issued = 0;
     auto issue_next = [&]() {
       if (ti_issue >= n_tiles) return;
@@ -336,39 +363,41 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         bulk_g2s(my_stage + ps * PCHUNK, psrc(tl, p, kb_issue), PCHUNK, &my_bar[ps]);
       }
       ++n_issued;
-      if (++kb_issue == n_kb) {
-        kb_issue = 0;
+      kb_issue += 2;
+      if (kb_issue >= n_kb) {
+        kb_issue = par;
         ti_issue += gridDim.x;
       }
     };
     for (int i = 0; i < PSTAGES - 1; ++i) issue_next();
-    uint32_t it = 0;
-    for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
-      for (int kb = 0; kb < n_kb; ++kb, ++it) {
+    uint32_t j = 0, lt = 0;
+    for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
+      for (int kb = par; kb < n_kb; kb += 2, ++j) {
         __syncwarp();
-        issue_next();   // refills the slot consumed two items ago
-        const int ps = it % PSTAGES;
-        if (!mbar_wait(&my_bar[ps], (it / PSTAGES) & 1)) {
+        issue_next();   // refills the slot consumed PSTAGES-1 items ago
+        const int ps = j % PSTAGES;
+        if (!mbar_wait(&my_bar[ps], (j / PSTAGES) & 1)) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           goto done;
         }
+        const uint32_t it = lt * n_kb + kb;
         const int s = it % STAGES;
         const uint32_t use = it / STAGES;
         if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           goto done;
         }
-        uint8_t* st = stages + s * STAGE_BYTES;
+        const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
         const uint8_t* src = my_stage + ps * PCHUNK;
         if (DOWN) {
-          dequant_block_to_tile(src, lane, st, p * 32, 0);
-          dequant_block_to_tile(src + kBlockBytes, lane, st, p * 32, 32);
+          dequant_block_to_tile<0>(src, lane, tile_lane, gx);
+          dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane, gx);
+        } else if (!hi_group) {
+          dequant_block_to_tile<0>(src, lane, tile_lane, gx);                                // Wg
+          dequant_block_to_tile<0>(src + kBlockBytes, lane, tile_lane + GU_ROWS * 128, gx);  // Wu
         } else {
-          // blocks in order: (g0, Wg), (g0, Wu), (g1, Wg), (g1, Wu)
-          dequant_block_to_tile(src, lane, st, p * 32, 0);
-          dequant_block_to_tile(src + kBlockBytes, lane, st + A_BYTES, p * 32, 0);
-          dequant_block_to_tile(src + 2 * kBlockBytes, lane, st, p * 32, 32);
-          dequant_block_to_tile(src + 3 * kBlockBytes, lane, st + A_BYTES, p * 32, 32);
+          dequant_block_to_tile<4>(src, lane, tile_lane, gx);
+          dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane + GU_ROWS * 128, gx);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -376,73 +405,75 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       }
     }
   } else {
-    // ---- epilogue: warps 6-9 cover the four 32-lane quarters of TMEM -------
+    // ---- epilogue: warps EPI0.. cover the four 32-lane quarters of TMEM ----
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;          // M row of the tile
-    const int et = threadIdx.x - (2 + NPROD) * 32; // 0..127
+    const int row = quarter * 32 + lane;            // M row of the tile
+    const int et = threadIdx.x - EPI0 * 32;         // 0..127
     uint32_t lt = 0;
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
       const PrefillTile tl = tiles[ti];
-      const int ab = DOWN ? (lt & 1) : 0;
-      const uint32_t use_b = DOWN ? (lt >> 1) : lt;
-      if (!mbar_wait(&tfull[ab], use_b & 1)) {
+      const int ab = lt & 1;
+      if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
         set_error(a.err, DEV_TIMEOUT_BARRIER);
         goto done;
       }
       tc_fence_after();
       const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-      for (int c = 0; c * 32 < tl.nlen; ++c) {
-        const int nrow = min(32, tl.nlen - c * 32);
+      for (int cc = 0; cc * 32 < tl.nlen; ++cc) {
+        const int nrow = min(32, tl.nlen - cc * 32);
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + ab * BN + cc * 32, r);
+        tmem_ld_wait();
         if (!DOWN) {
-          uint32_t rg[32], ru[32];
-          tmem_ld32(tmem + lane_addr + c * 32, rg);
-          tmem_ld32(tmem + lane_addr + BN + c * 32, ru);
-          tmem_ld_wait();
-          __half* eh = reinterpret_cast<__half*>(epi);
-          float hv[32];
+          // M rows 64-127 (u) go through shared memory to the warps holding
+          // the matching g rows 0-63; those write h = silu(g) * u as an fp16
+          // pair (hi = RN(h), lo = RN(h - hi)) staged [token][64 f rows]
+          float* eu = reinterpret_cast<float*>(epi);                       // [32 tokens][64]
+          __half* ehi = reinterpret_cast<__half*>(epi + 32 * GU_ROWS * 4);  // [32][64]
+          __half* elo = ehi + 32 * GU_ROWS;
+          if (quarter >= 2) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float g = __uint_as_float(rg[j]), u = __uint_as_float(ru[j]);
-            hv[j] = g / (1.f + expf(-g)) * u;
+            for (int jj = 0; jj < 32; ++jj) eu[jj * GU_ROWS + row - GU_ROWS] = __uint_as_float(r[jj]);
           }
-          // pass 0 writes hi = RN(h) to Hg, pass 1 writes lo = RN(h - hi) to Hg_lo
-          for (int pass = 0; pass < 2; ++pass) {
+          named_bar(1, 128);
+          if (quarter < 2) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const __half hi = __float2half_rn(hv[j]);
-              eh[j * BM + row] = pass == 0 ? hi : __float2half_rn(hv[j] - __half2float(hi));
+            for (int jj = 0; jj < 32; ++jj) {
+              const float gv = __uint_as_float(r[jj]), uv = eu[jj * GU_ROWS + row];
+              const float hv = gv / (1.f + expf(-gv)) * uv;
+              const __half hi = __float2half_rn(hv);
+              ehi[jj * GU_ROWS + row] = hi;
+              elo[jj * GU_ROWS + row] = __float2half_rn(hv - __half2float(hi));
             }
-            named_bar(1, 128);
-            uint16_t* dst = pass == 0 ? a.hg : a.hg_lo;
-            // 32 token rows x 128 f values (256 B)
-            for (int q = et; q < 32 * 16; q += 128) {
-              const int j = q >> 4, ch = q & 15;
-              if (j < nrow) {
-                const uint4 v = *reinterpret_cast<const uint4*>(epi + j * 256 + ch * 16);
-                *reinterpret_cast<uint4*>(dst + (size_t)(tl.row0 + c * 32 + j) * a.f + tl.m * BM + ch * 8) = v;
-              }
-            }
-            named_bar(1, 128);
           }
+          named_bar(1, 128);
+          // 32 token rows x 64 f values (128 B) of hi, then of lo
+          for (int q = et; q < 2 * 32 * 8; q += 128) {
+            const int part = q >> 8, jj = (q >> 3) & 31, ch = q & 7;
+            if (jj < nrow) {
+              const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(part ? elo : ehi) +
+                                                              jj * 128 + ch * 16);
+              uint16_t* dst = part ? a.hg_lo : a.hg;
+              *reinterpret_cast<uint4*>(dst + (size_t)(tl.row0 + cc * 32 + jj) * a.f + tl.m * GU_ROWS + ch * 8) = v;
+            }
+          }
+          named_bar(1, 128);
         } else {
           if (et < 32) {
-            const int j = et;
-            s_w[j] = j < nrow ? a.wsort[tl.row0 + c * 32 + j] : 0.f;
-            s_tok[j] = j < nrow ? a.perm[tl.row0 + c * 32 + j] : 0;
+            const int jj = et;
+            s_w[jj] = jj < nrow ? a.wsort[tl.row0 + cc * 32 + jj] : 0.f;
+            s_tok[jj] = jj < nrow ? a.perm[tl.row0 + cc * 32 + jj] : 0;
           }
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + ab * BN + c * 32, r);
-          tmem_ld_wait();
           named_bar(1, 128);
           float* ef = reinterpret_cast<float*>(epi);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) ef[j * BM + row] = __uint_as_float(r[j]) * s_w[j];
+          for (int jj = 0; jj < 32; ++jj) ef[jj * BM + row] = __uint_as_float(r[jj]) * s_w[jj];
           named_bar(1, 128);
           for (int q = et; q < 32 * 32; q += 128) {
-            const int j = q >> 5, r4 = q & 31;
-            if (j < nrow) {
-              const float4 v = *reinterpret_cast<const float4*>(ef + j * BM + r4 * 4);
-              red_add_v4(a.y + (size_t)s_tok[j] * a.d + tl.m * BM + r4 * 4, v.x, v.y, v.z, v.w);
+            const int jj = q >> 5, r4 = q & 31;
+            if (jj < nrow) {
+              const float4 v = *reinterpret_cast<const float4*>(ef + jj * BM + r4 * 4);
+              red_add_v4(a.y + (size_t)s_tok[jj] * a.d + tl.m * BM + r4 * 4, v.x, v.y, v.z, v.w);
             }
           }
           named_bar(1, 128);
@@ -463,13 +494,11 @@ done:
 
 template <bool DOWN>
 static size_t gemm_smem() {
-  constexpr int NMAT = DOWN ? 1 : 2;
   constexpr int NB = DOWN ? 2 : 1;
   constexpr int STAGES = DOWN ? 2 : 3;
-  constexpr int STAGE_BYTES = NMAT * pg::A_BYTES + NB * pg::B_BYTES;
-  constexpr int PCHUNK = NMAT * 2 * kBlockBytes;
-  constexpr int EPI_BYTES = DOWN ? 32 * pg::BM * 4 : 32 * pg::BM * 2;
-  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + pg::NPROD * pg::PSTAGES * PCHUNK +
+  constexpr int STAGE_BYTES = pg::A_BYTES + NB * pg::B_BYTES;
+  constexpr int EPI_BYTES = DOWN ? 32 * pg::BM * 4 : 32 * pg::GU_ROWS * 4 + 2 * 32 * pg::GU_ROWS * 2;
+  return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + pg::NPROD * pg::PSTAGES * pg::PCHUNK +
          (3 * STAGES + 4 + pg::NPROD * pg::PSTAGES) * 8 + 16;
 }
 

@@ -157,28 +157,18 @@ __global__ void __launch_bounds__(rg::THREADS, 1)
 
 // One warp per token: top-k of the logits row, weights, per-expert counts.
 __global__ void __launch_bounds__(256) prefill_topk_kernel(PrefillTopkArgs a) {
+  __shared__ uint64_t scratch[8][kTopkScratch];
+  __shared__ float rows[8][kMaxE];
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= a.T) return;
   const int t = warp, E = a.E, K = a.k;
+  float* row = rows[threadIdx.x >> 5];
+#pragma unroll 8
+  for (int id = lane; id < E; id += 32) row[id] = a.logits[(size_t)t * E + id];
+  __syncwarp();
   float my_v;
   int my_id;
-  if (E <= 512) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int id = lane + 32 * i;
-      v[i] = id < E ? a.logits[(size_t)t * E + id] : -INFINITY;
-    }
-    warp_topk<16>(v, E, K, lane, my_v, my_id);
-  } else {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int id = lane + 32 * i;
-      v[i] = id < E ? a.logits[(size_t)t * E + id] : -INFINITY;
-    }
-    warp_topk<32>(v, E, K, lane, my_v, my_id);
-  }
+  warp_topk(row, E, K, lane, scratch[threadIdx.x >> 5], my_v, my_id);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = lane < K ? expf(my_v - top) : 0.f;
   float sum = ex;

@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, blockIdx.x, 0);
   pdl_launch_dependents();
 
-  __shared__ SelSmem sel;
+  extern __shared__ __align__(16) uint8_t route_dyn_smem[];
+  SelSmem& sel = *reinterpret_cast<SelSmem*>(route_dyn_smem);
   __shared__ int s_slot[kMaxPicks];
   __shared__ int s_hit[kMaxPicks];
   __shared__ int s_miss_act[kMaxPicks];
@@ -82,7 +83,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
 
   // ---- router logits: one warp per expert row, all T tokens -------------
   const int e = blockIdx.x * kRouteWarps + warp;
-  if (e < E) router_row(a.wr + (size_t)e * a.d, a.x, a.bias[e], T, a.d, E, e, lane, a.logits);
+  if (e < E) {
+    const uint16_t* wrow = a.wr + (size_t)e * a.d;
+    uint4 first[8];
+    router_load_block(wrow, 0, a.d, lane, first);
+    router_row(wrow, first, a.x, a.d, a.bias[e], T, a.d, E, e, lane, a.logits);
+  }
 
   // ---- last CTA to arrive does the selection -----------------------------
   __syncthreads();
@@ -206,14 +212,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   }
 }
 
-// Applies a ROUTE_PLAN plan once its miss copies are enqueued.
+// Applies a ROUTE_PLAN plan once its miss copies are enqueued, and readies
+// the decode counters of the call's expert kernel.
 __global__ void __launch_bounds__(256) commit_kernel(CommitArgs a) {
   const Plan* P = a.plan;
   const int n_act = P->n_act, m = P->n_miss;
   const int64_t clk = P->clock;
+  // the expert kernel reads the bumped call count and uses the counter set
+  // of the count before it; the set of the call before it is zeroed here
+  const uint32_t calls = *a.counters;
   __shared__ int s_evict;
   if (threadIdx.x == 0) s_evict = 0;
   __syncthreads();
+  uint32_t* prev_set = a.counters + 1 + (size_t)((calls + 1) & 1) * a.set_words;
+  for (int i = threadIdx.x; i < a.set_words; i += blockDim.x) prev_set[i] = 0;
   for (int i = threadIdx.x; i < n_act; i += blockDim.x)
     if (P->act_hit[i]) a.stamp[P->act_slot[i]] = clk;
   for (int j = threadIdx.x; j < m; j += blockDim.x) {
@@ -232,6 +244,7 @@ __global__ void __launch_bounds__(256) commit_kernel(CommitArgs a) {
     a.stamp[v] = clk;
   }
   if (threadIdx.x == 0) {
+    *a.counters = calls + 1;
     a.stats[ST_CALLS] += 1;
     a.stats[ST_TOK_HIT] += P->token_hits;
     a.stats[ST_TOK_MISS] += P->token_misses;
@@ -250,8 +263,16 @@ extern "C" int moe_debug_timeline_route(unsigned long long* out) {
 #endif
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+  // the selection scratch is dynamic shared memory (static + dynamic > 48 KB)
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   const int grid = (a.E + kRouteWarps - 1) / kRouteWarps;
-  route_kernel<<<grid, kRouteThreads, 0, s>>>(a);
+  route_kernel<<<grid, kRouteThreads, sizeof(SelSmem), s>>>(a);
   return cudaGetLastError();
 }
 

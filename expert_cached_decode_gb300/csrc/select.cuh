@@ -15,60 +15,73 @@
 
 namespace moe {
 
-// One warp: logits of expert row `wrow` for the T tokens of x.  Lane chunk
-// j = lane*8 + 256*u of every 2048-wide block, accumulated in u order, then a
-// butterfly sum; lane 0 stores l[t, e] = dot + bias at logits[t*E + e].
-__device__ __forceinline__ void router_row(const uint16_t* __restrict__ wrow, const uint16_t* __restrict__ x,
-                                           float bias, int T, int d, int E, int e, int lane, float* logits) {
-  float acc[kMaxDecodeT];
+// Lane chunks j = jb + lane*8 + 256*u (u < 8) of a 2048-wide block of a
+// router row (zero past d).
+__device__ __forceinline__ void router_load_block(const uint16_t* __restrict__ wrow, int jb, int d, int lane,
+                                                  uint4 (&wv)[8]) {
 #pragma unroll
-  for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.f;
-  for (int jb = 0; jb < d; jb += 2048) {
-    uint4 wv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int j = jb + lane * 8 + 256 * u;
-      wv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(wrow + j)) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) {
-      if (t < T) {
-        uint4 xv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = jb + lane * 8 + 256 * u;
-          xv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d + j)) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        float s = acc[t];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 w4 = wv[u], x4 = xv[u];
-          s = fmaf(bf16_bits_to_float(x4.x & 0xffffu), bf16_bits_to_float(w4.x & 0xffffu), s);
-          s = fmaf(bf16_bits_to_float(x4.x >> 16), bf16_bits_to_float(w4.x >> 16), s);
-          s = fmaf(bf16_bits_to_float(x4.y & 0xffffu), bf16_bits_to_float(w4.y & 0xffffu), s);
-          s = fmaf(bf16_bits_to_float(x4.y >> 16), bf16_bits_to_float(w4.y >> 16), s);
-          s = fmaf(bf16_bits_to_float(x4.z & 0xffffu), bf16_bits_to_float(w4.z & 0xffffu), s);
-          s = fmaf(bf16_bits_to_float(x4.z >> 16), bf16_bits_to_float(w4.z >> 16), s);
-          s = fmaf(bf16_bits_to_float(x4.w & 0xffffu), bf16_bits_to_float(w4.w & 0xffffu), s);
-          s = fmaf(bf16_bits_to_float(x4.w >> 16), bf16_bits_to_float(w4.w >> 16), s);
-        }
-        acc[t] = s;
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kMaxDecodeT; ++t) {
-    if (t < T) {
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) logits[(size_t)t * E + e] = v + bias;
-    }
+  for (int u = 0; u < 8; ++u) {
+    const int j = jb + lane * 8 + 256 * u;
+    wv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(wrow + j)) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
+// s += the 8 products of one 16-byte chunk of x and of a router row, in order
+__device__ __forceinline__ float dot8_bf16(uint4 w4, uint4 x4, float s) {
+  s = fmaf(bf16_bits_to_float(x4.x & 0xffffu), bf16_bits_to_float(w4.x & 0xffffu), s);
+  s = fmaf(bf16_bits_to_float(x4.x >> 16), bf16_bits_to_float(w4.x >> 16), s);
+  s = fmaf(bf16_bits_to_float(x4.y & 0xffffu), bf16_bits_to_float(w4.y & 0xffffu), s);
+  s = fmaf(bf16_bits_to_float(x4.y >> 16), bf16_bits_to_float(w4.y >> 16), s);
+  s = fmaf(bf16_bits_to_float(x4.z & 0xffffu), bf16_bits_to_float(w4.z & 0xffffu), s);
+  s = fmaf(bf16_bits_to_float(x4.z >> 16), bf16_bits_to_float(w4.z >> 16), s);
+  s = fmaf(bf16_bits_to_float(x4.w & 0xffffu), bf16_bits_to_float(w4.w & 0xffffu), s);
+  s = fmaf(bf16_bits_to_float(x4.w >> 16), bf16_bits_to_float(w4.w >> 16), s);
+  return s;
+}
+
+// One warp: logits of expert row `wrow` for the T tokens of x (bf16 rows
+// xstride elements apart, 16-byte aligned, global or shared memory), given
+// the row's first 2048-wide block in `first` (router_load_block at jb = 0).
+// Per token, lane chunks accumulate in u order within each 2048-wide block,
+// blocks in order, then a butterfly sum; lane 0 stores l[t, e] = dot + bias
+// at logits[t*E + e].  Tokens run in a loop (this code runs once per call,
+// so it is kept short).
+__device__ __forceinline__ void router_row(const uint16_t* __restrict__ wrow, const uint4 (&first)[8],
+                                           const uint16_t* __restrict__ x, int xstride, float bias, int T, int d,
+                                           int E, int e, int lane, float* logits) {
+#pragma unroll 1
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* xr = x + (size_t)t * xstride;
+    float s = 0.f;
+#pragma unroll 1
+    for (int jb = 0; jb < d; jb += 2048) {
+      uint4 wv[8];
+      if (jb == 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = first[u];
+      } else {
+        router_load_block(wrow, jb, d, lane, wv);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int jj = jb + lane * 8 + 256 * u;
+        if (jj < d) s = dot8_bf16(wv[u], *reinterpret_cast<const uint4*>(xr + jj), s);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) logits[(size_t)t * E + e] = s + bias;
+  }
+}
+
+// warps of a block that take tokens in select_call (further warps only join
+// its barriers)
+constexpr int kSelWarps = 8;
+
 // Selection of one call, in shared memory.
 struct SelSmem {
+  float row[kSelWarps][kMaxE];               // logits row of each selecting warp
+  uint64_t topk[kSelWarps][kTopkScratch];   // warp_topk scratch
   uint32_t mask[kMaxE / 32];          // chosen experts of the call
   int word_base[kMaxE / 32];          // distinct experts below word i
   int sel_id[kMaxDecodeT][kMaxTopK];  // per token, ascending id
@@ -82,34 +95,23 @@ __device__ __forceinline__ int sel_act_index(const SelSmem* s, int id) {
   return s->word_base[id >> 5] + __popc(s->mask[id >> 5] & ((1u << (id & 31)) - 1u));
 }
 
-// Every thread of the block calls this.  Reads the logits rows [T][E] from
-// global memory through L2 (they were written by other CTAs of this kernel
-// or of the same launch); warps take tokens in turn: top-k (ties to the lower
-// id), weights, ids ascending; then warp 0 forms U.
+// Every thread of the block calls this; warps below kSelWarps select.
+// Reads the logits rows [T][E] from global memory through L2 (they were
+// written by other CTAs of this kernel or of the same launch); warps take
+// tokens in turn: top-k (ties to the lower id), weights, ids ascending; then
+// warp 0 forms U.
 __device__ __forceinline__ void select_call(const float* logits, int T, int E, int K, SelSmem* s) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kMaxE / 32; i += blockDim.x) s->mask[i] = 0;
   __syncthreads();
-  for (int t = warp; t < T; t += nw) {
+  for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
+    float* row = s->row[warp];
+#pragma unroll 8
+    for (int id = lane; id < E; id += 32) row[id] = ld_cg_f32(logits + (size_t)t * E + id);
+    __syncwarp();
     float my_v;
     int my_id;
-    if (E <= 512) {
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int id = lane + 32 * i;
-        v[i] = id < E ? ld_cg_f32(logits + (size_t)t * E + id) : -INFINITY;
-      }
-      warp_topk<16>(v, E, K, lane, my_v, my_id);
-    } else {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int id = lane + 32 * i;
-        v[i] = id < E ? ld_cg_f32(logits + (size_t)t * E + id) : -INFINITY;
-      }
-      warp_topk<32>(v, E, K, lane, my_v, my_id);
-    }
+    warp_topk(row, E, K, lane, s->topk[warp], my_v, my_id);
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = lane < K ? expf(my_v - top) : 0.f;
     float sum = ex;
