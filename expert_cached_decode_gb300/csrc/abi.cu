@@ -95,8 +95,6 @@ struct moe_ctx {
   uint32_t* counters = nullptr;  // decode calls | 2 sets of (h_ready | d_cnt | gbar)
   size_t counters_n = 0;
   int set_words = 0;
-  int2* part = nullptr;          // [num_sms + 1][nx] decode work bounds
-  int nx = 0;
   uint32_t* err = nullptr;
   int max_exp = 0;
   // prefill scratch (allocated on first use, sized for kMaxPrefillT tokens)
@@ -288,17 +286,10 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
   CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
   CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
-  c->set_words = c->max_exp + 2;
+  c->set_words = c->max_exp + 1 + c->d / 32;
   c->counters_n = 1 + 2 * (size_t)c->set_words;
   CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
-  {
-    c->nx = c->max_exp + 1;
-    std::vector<int2> part((size_t)(c->num_sms + 1) * c->nx);
-    decode_partition(c->num_sms, c->nx, c->d, c->f, part.data());
-    CREATE_TRY(cudaMalloc(&c->part, part.size() * sizeof(int2)));
-    CREATE_TRY(cudaMemcpy(c->part, part.data(), part.size() * sizeof(int2), cudaMemcpyHostToDevice));
-  }
   CREATE_TRY(cudaMalloc(&c->err, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->err, 0, sizeof(uint32_t)));
   CREATE_TRY(cudaMalloc(&c->clock, sizeof(int64_t)));
@@ -334,7 +325,6 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->route_cnt);
   cudaFree(c->plan);
   if (c->plan_host) cudaFreeHost(c->plan_host);
-  cudaFree(c->part);
   cudaFree(c->hbuf);
   cudaFree(c->obuf);
   cudaFree(c->counters);
@@ -572,8 +562,6 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.set_words = c->set_words;
   fa.max_exp = c->max_exp;
   fa.err = c->err;
-  fa.part = c->part;
-  fa.nx = c->nx;
   fa.grid = c->num_sms;
   // fused routing (used when every key is resident)
   fa.wr = c->router_w + (size_t)layer * c->E * c->d;

@@ -266,11 +266,6 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
-  return ((uint64_t)hi << 32) | lo;
-}
 __device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
   const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
   const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
@@ -306,18 +301,14 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int K, int la
     const uint64_t k = topk_key(row, id);
     m = k > m ? k : m;
   }
-  // bitonic sort of the lane maxima across the warp, descending
-  uint64_t t = m;
-#pragma unroll 1
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll 1
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const uint64_t o = shfl_xor_u64(t, j);
-      const bool keep_max = ((lane & k) == 0) == ((lane & j) == 0);
-      t = keep_max ? (o > t ? o : t) : (o < t ? o : t);
-    }
-  }
-  const uint64_t tau = shfl_u64(t, K - 1);
+  // the K-th largest lane maximum: each lane counts the lane maxima above
+  // its own (all differ unless both are 0, and at least K + 1 lanes hold an
+  // entry); the lane whose count is K - 1 holds it
+  int above = 0;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) above += shfl_u64(m, j) > m ? 1 : 0;
+  const uint32_t holder = __ballot_sync(0xffffffffu, above == K - 1 && m != 0);
+  const uint64_t tau = shfl_u64(m, __ffs(holder) - 1);
   int cnt = 0;
 #pragma unroll 4
   for (int id = lane; id < E; id += 32) cnt += topk_key(row, id) >= tau ? 1 : 0;
@@ -332,7 +323,7 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int K, int la
   out_id = 0x7fffffff;
   if (n_c <= kTopkMaxCand) {
     int pos = incl - cnt;
-#pragma unroll 1
+#pragma unroll 4
     for (int id = lane; id < E; id += 32) {
       const uint64_t k = topk_key(row, id);
       if (k >= tau) scratch[pos++] = k;

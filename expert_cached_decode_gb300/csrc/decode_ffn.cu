@@ -18,19 +18,20 @@
 //     h = silu(g) * u for 32 rows of expert a (fp16, [expert][token][f]) and
 //     bumps h_ready[a];
 //   down tile (expert a, R consecutive 32-row blocks of d): R * f/32 Wd blocks
-//     (R = 2 at f = 768); it multiplies by h_a, writes o_a for its rows, and
-//     the last expert to finish a row block combines y for those rows in a
-//     fixed order (shared expert, then routed experts in ascending id).
-// One persistent CTA per SM takes a byte-balanced share (a host-computed
-// table per expert count): a contiguous range of gate/up tiles, then a
-// contiguous range of down tiles.  A producer thread streams every tile
-// through a ring of 16-block stages with bulk TMA copies (mbarrier
-// completion); an h-loader thread bulk-copies each expert's h into shared
-// memory once per CTA when it is ready.  All 8 consumer warps work on every
-// stage (2 blocks each): they expand the 3-bit codes to fp16 in registers and
-// multiply on the tensor cores (mma.sync m16n8k16, fp32 accumulate, per-group
-// scale in fp32); a tile's per-warp partial sums are reduced through shared
-// memory in a fixed order.  All waits are bounded.
+//     (R = 2 at f = 768); it multiplies by h_a and writes o_a for its rows.
+// One persistent CTA per SM takes an even share of each phase: a contiguous
+// range of gate/up tiles, then a contiguous range of down tiles.  A producer
+// thread streams every tile through a ring of 16-block stages with bulk TMA
+// copies (mbarrier completion); an h-loader thread bulk-copies each expert's
+// h into shared memory once per CTA when it is ready.  All 8 consumer warps
+// work on every stage (2 blocks each): they expand the 3-bit codes to fp16 in
+// registers and multiply on the tensor cores (mma.sync m16n8k16, fp32
+// accumulate, per-group scale in fp32), then hand each tile's partial sums
+// to a finalizer warp that adds them in a fixed order, writes h or o and
+// publishes it.  CTA c then combines the row blocks c, c + G, ... of y once
+// every expert's output there is written, in a fixed order (shared expert,
+// then routed experts in ascending id), so y is deterministic.  All waits are
+// bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -42,7 +43,7 @@ __device__ unsigned long long g_ffn_timeline[512][16];
 #endif
 
 constexpr int kCW = 8;                        // consumer warps
-constexpr int kThreads = (kCW + 3) * 32;      // + producer, h-loader and publisher warps
+constexpr int kThreads = (kCW + 3) * 32;      // + producer, h-loader and finalizer warps
 constexpr int kStageBlocks = 16;
 constexpr int kStageBytes = kStageBlocks * kBlockBytes;   // 7,168
 constexpr int kHSlots = 2;
@@ -80,7 +81,7 @@ template <int NT>
 __host__ __device__ __forceinline__ size_t ffn_smem_bytes(int d, int f) {
   return (size_t)NT * d * 16 + (size_t)FfnCfg<NT>::kStages * kStageBytes +
          (size_t)kHSlots * NT * 8 * h_row_bytes(f) + (size_t)kCW * 32 * red_per_lane(f, NT) * 4 +
-         (2 * FfnCfg<NT>::kStages + 2 * kHSlots) * 8 + 64;
+         (2 * FfnCfg<NT>::kStages + 2 * kHSlots + 2) * 8 + 64;
 }
 
 __device__ __forceinline__ uint32_t pack_half2_from_bf16(uint32_t two_bf16) {
@@ -174,8 +175,8 @@ __device__ __forceinline__ void h_frags(const uint8_t* hb, int hrow, int T, int 
 }
 
 // bytes of the routing-phase scratch kept in the (not yet used) stage ring
-__host__ __device__ __forceinline__ size_t route_scratch_bytes(int E, int nx) {
-  return ((sizeof(SelSmem) + 15) & ~size_t(15)) + (size_t)E * 4 + (size_t)2 * nx * 8;
+__host__ __device__ __forceinline__ size_t route_scratch_bytes(int E) {
+  return ((sizeof(SelSmem) + 15) & ~size_t(15)) + (size_t)E * 4;
 }
 
 template <int NT, bool FUSED>
@@ -200,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   uint64_t* empty = full + NS;
   uint64_t* hfull = empty + NS;
   uint64_t* hempty = hfull + kHSlots;
+  uint64_t& buf_full = hempty[kHSlots];       // 8 consumer warps put a tile's partials
+  uint64_t& buf_free = hempty[kHSlots + 1];   // the finalizer has read them
   // routing-phase scratch, overlaid on the stage ring (free until the first copy)
   SelSmem* sel = reinterpret_cast<SelSmem*>(ring);
   int* s_tab = reinterpret_cast<int*>(ring + ((sizeof(SelSmem) + 15) & ~size_t(15)));
-  int2* s_part = reinterpret_cast<int2*>(s_tab + (FUSED ? a.E : 0));
   __shared__ int s_act_slot[kMaxPicks];   // slot of each distinct routed expert
   __shared__ int s_pick_act[kMaxPicks];   // [T][k] index of each pick in the distinct list
   __shared__ float s_w[kMaxPicks];        // [T][k] routing weights
@@ -211,10 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   __shared__ uint32_t s_calls;
   __shared__ long long s_clock;
   __shared__ volatile int s_hexp[kHSlots];
-  __shared__ uint32_t s_gu_done;          // gate/up tiles of this CTA whose h is written
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = gridDim.x, cta = blockIdx.x, nx = a.nx;
+  const int G = gridDim.x, cta = blockIdx.x;
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 0);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -223,19 +224,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     }
     for (int i = 0; i < kHSlots; ++i) {
       mbar_init(&hfull[i], 1);
-      mbar_init(&hempty[i], 1);
+      mbar_init(&hempty[i], kCW);
       s_hexp[i] = -1;
     }
-    s_gu_done = 0;
+    mbar_init(&buf_full, kCW);
+    mbar_init(&buf_free, 1);
     mbar_init_fence();
   }
   // Every load of the prologue is issued before any of them is used, so the
-  // prologue costs about one memory round trip.  Static inputs first: work
-  // bounds of this CTA and the next for every expert count; with fused
-  // routing also the slot table row (every key is resident, so it does not
+  // prologue costs about one memory round trip.  Static inputs first: with
+  // fused routing the slot table row (every key is resident, so it does not
   // change) and the first block of this warp's router row.
-  const int2 pv0 = tid < 2 * nx ? a.part[(size_t)cta * nx + tid] : make_int2(0, 0);
-  const int2 pv1 = tid + kThreads < 2 * nx ? a.part[(size_t)cta * nx + tid + kThreads] : make_int2(0, 0);
   int tv[kTabPerThread];
   uint4 wfirst[8];
   float wbias = 0.f;
@@ -277,8 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     }
   }
   // now the stores
-  if (tid < 2 * nx) s_part[tid] = pv0;
-  if (tid + kThreads < 2 * nx) s_part[tid + kThreads] = pv1;
   if (FUSED) {
 #pragma unroll
     for (int q = 0; q < kTabPerThread; ++q)
@@ -321,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   const uint32_t call_set = FUSED ? (s_calls & 1u) : ((s_calls - 1u) & 1u);
   uint32_t* const h_ready = a.counters + 1 + (size_t)call_set * a.set_words;
   uint32_t* const gbar = h_ready + a.max_exp;    // CTAs past the router phase
-  uint32_t* const gbar_end = gbar + 1;           // CTAs whose expert outputs are written
+  uint32_t* const d_cnt = gbar + 1;              // [d/32] experts whose outputs of a row block are written
   if (FUSED && cta == 0) {
     uint32_t* other = a.counters + 1 + (size_t)(call_set ^ 1u) * a.set_words;
     for (int i = tid; i < a.set_words; i += kThreads) other[i] = 0;
@@ -408,13 +405,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 2);
   __syncthreads();
   // ---- this CTA's share: gate/up tiles [g0, g1), down tiles [d0, d1) ------
+  // Each phase is split evenly by tile count: every down tile waits for the
+  // gate/up phase, so balancing the phases separately ends both sooner than
+  // balancing a CTA's total bytes.
   if (tid == 0) {
     const int n = s_nexp;
-    const int2 lo = s_part[n], hi = s_part[nx + n];
-    s_g0 = lo.x;
-    s_d0 = lo.y;
-    s_g1 = hi.x;
-    s_d1 = hi.y;
+    const int NG = n * RG, ND = n * (RD / RT);
+    s_g0 = cta * NG / G;
+    s_g1 = (cta + 1) * NG / G;
+    s_d0 = cta * ND / G;
+    s_d1 = (cta + 1) * ND / G;
   }
   __syncthreads();
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 3);
@@ -498,48 +498,123 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         if (!mbar_wait(&hfull[k % kHSlots], (uint32_t)((k / kHSlots) & 1))) set_error(a.err, DEV_TIMEOUT_BARRIER);
     }
   } else if (warp == kCW + 2) {
-    // ---------------- publisher: makes finished h visible to other CTAs ----
-    // (the gpu-scope release waits for the writes; consumers never block on it)
-    if (lane == 0) {
-      int k = 0;
-      while (k < n_gt) {
-        uint32_t done = ld_acquire_cta_u32(&s_gu_done);
-        if (done <= (uint32_t)k) {
-          const uint64_t t0 = globaltimer();
-          while ((done = ld_acquire_cta_u32(&s_gu_done)) <= (uint32_t)k) {
-            __nanosleep(32);
-            if (globaltimer() - t0 > kWaitLimitNs) break;
-          }
-          if (done <= (uint32_t)k) {
-            set_error(a.err, DEV_TIMEOUT_FLAG);
-            break;
-          }
-        }
-        while (k < (int)done) {
-          const int ai = (g0 + k) / RG;
-          uint32_t cnt = 0;
-          while (k < (int)done && (g0 + k) / RG == ai) {
-            ++cnt;
-            ++k;
-          }
-          red_release_add(&h_ready[ai], cnt);
-        }
+    // ---------------- finalizer ----------------------------------------------
+    // Takes every tile's per-warp partial sums from the reduction buffer in
+    // tile order, adds them in a fixed order (warp 0..7) and writes the
+    // result: h = silu(g) * u (fp16) for a gate/up tile, the expert output o
+    // for a down tile.  Its own gpu-scope releases then publish them
+    // (h_ready per expert, d_cnt per row block of y), so the consumer warps
+    // never wait for a fence or for each other.
+    const int gq = lane >> 2, cq = lane & 3;
+    bool ok = true;
+    for (int ti = 0; ti < n_gt + n_dt && ok; ++ti) {
+      if (!mbar_wait(&buf_full, (uint32_t)(ti & 1))) {
+        set_error(a.err, DEV_TIMEOUT_BARRIER);
+        ok = false;
+        break;
       }
-      MOE_TL(g_ffn_timeline, cta, 9);
+      if (ti < n_gt) {
+        const int tg = g0 + ti, ai = tg / RG, rb = tg % RG;
+        // lane l adds fragment element e of lane l over the 8 warps
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float g = 0.f, u = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) {
+              const float* pw = red + ((size_t)w * 32 + lane) * RPL + nt * 16;
+              g += pw[e];
+              u += pw[8 + e];
+            }
+            const int mt = e >> 2, i = e & 3;
+            const int tok = nt * 8 + 2 * cq + (i & 1);
+            if (tok < T) {
+              const float hv = g / (1.f + expf(-g)) * u;
+              const int row = rb * 32 + mt * 16 + gq + 8 * (i >> 1);
+              a.hbuf[((size_t)ai * T + tok) * f + row] = __half_as_ushort(__float2half_rn(hv));
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&buf_free);
+          red_release_add(&h_ready[ai], 1u);   // covers this warp's h stores (after the warp sync)
+        }
+        if (ti + 1 == n_gt && lane == 0) MOE_TL(g_ffn_timeline, cta, 9);
+      } else {
+        const int td = d0 + ti - n_gt, ai = td / DPE, rp = td % DPE;
+        for (int r = 0; r < RT; ++r) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float o = 0.f;
+#pragma unroll
+              for (int w = 0; w < kCW; ++w) o += red[((size_t)w * 32 + lane) * RPL + (r * NT + nt) * 8 + e];
+              const int mt = e >> 2, i = e & 3;
+              const int tok = nt * 8 + 2 * cq + (i & 1);
+              if (tok < T) {
+                const int row = (rp * RT + r) * 32 + mt * 16 + gq + 8 * (i >> 1);
+                a.obuf[((size_t)ai * T + tok) * d + row] = o;
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&buf_free);
+        if (lane < RT) red_release_add(&d_cnt[rp * RT + lane], 1u);
+      }
     }
+    if (lane == 0) MOE_TL(g_ffn_timeline, cta, 11);
+    // ---- combine: CTA c owns row blocks c, c + G, ... of y.  Once all n_exp
+    // expert outputs of a row block are written it forms y there in a fixed
+    // order (shared expert, then the picks in ascending id), all loads of
+    // one output issued before the sum.
+    const int n_exp = s_nexp;
+    for (int rb = cta; ok && rb < RD; rb += G) {
+      uint32_t good = 1;
+      if (lane == 0 && !wait_flag_geq(&d_cnt[rb], (uint32_t)n_exp)) {
+        set_error(a.err, DEV_TIMEOUT_FLAG);
+        good = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      __syncwarp();   // the other lanes read after lane 0's acquire
+      const int row = rb * 32 + lane;
+#pragma unroll 1
+      for (int t = 0; t < T; ++t) {
+        float ov[kMaxTopK];
+#pragma unroll
+        for (int k2 = 0; k2 < kMaxTopK; ++k2)
+          ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + row) : 0.f;
+        float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + row);
+#pragma unroll
+        for (int k2 = 0; k2 < kMaxTopK; ++k2)
+          if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
+        a.y[(size_t)t * d + row] = yv;
+      }
+    }
+    if (lane == 0) MOE_TL(g_ffn_timeline, cta, 12);
   } else {
     // ---------------- consumers: 8 warps on every stage --------------------
-    const int gq = lane >> 2, cq = lane & 3;
-    const int ctid = tid;                 // 0..255
+    // After a tile each warp writes its partial sums to the reduction buffer
+    // (once the finalizer has read the previous tile's) and moves on.
     uint32_t it = 0;
     bool ok = true;
-    // one reduction buffer: every tile passes a barrier after its last read
-    // of the buffer before any warp writes the next tile's partials
-    float* rbuf = red;
+    float* mine = red + ((size_t)warp * 32 + lane) * RPL;
+    auto wait_buf_free = [&](int ti) {
+      if (ok && ti > 0 && !mbar_wait(&buf_free, (uint32_t)((ti - 1) & 1))) {
+        set_error(a.err, DEV_TIMEOUT_BARRIER);
+        ok = false;
+      }
+    };
+    auto signal_buf_full = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&buf_full);
+    };
     for (int ti = 0; ti < n_gt + n_dt; ++ti) {
       if (ti < n_gt) {
         // ===== gate/up tile: 32 rows of Wg and Wu over all inputs =====
-        const int tg = g0 + ti, ai = tg / RG, rb = tg % RG;
         float ag[NT][2][4], au[NT][2][4];
         zero_acc<NT>(ag);
         zero_acc<NT>(au);
@@ -564,43 +639,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // partials -> shared memory, reduced over the 8 warps in order
-        float* mine = rbuf + ((size_t)warp * 32 + lane) * RPL;
+        wait_buf_free(ti);
+        if (ok) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              mine[nt * 16 + mt * 4 + i] = ag[nt][mt][i];
-              mine[nt * 16 + 8 + mt * 4 + i] = au[nt][mt][i];
-            }
-        named_bar(1, kCW * 32);
-        // warp w finishes fragment element e = w of every lane
-        {
-          const int e = warp, mt = e >> 2, i = e & 3;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            float g = 0.f, u = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) {
-              const float* pw = rbuf + ((size_t)w * 32 + lane) * RPL + nt * 16;
-              g += pw[e];
-              u += pw[8 + e];
-            }
-            const int tok = nt * 8 + 2 * cq + (i & 1);
-            if (tok < T) {
-              const float hv = g / (1.f + expf(-g)) * u;
-              const int row = rb * 32 + mt * 16 + gq + 8 * (i >> 1);
-              a.hbuf[((size_t)ai * T + tok) * f + row] = __half_as_ushort(__float2half_rn(hv));
-            }
-          }
+              for (int i = 0; i < 4; ++i) {
+                mine[nt * 16 + mt * 4 + i] = ag[nt][mt][i];
+                mine[nt * 16 + 8 + mt * 4 + i] = au[nt][mt][i];
+              }
         }
-        named_bar(1, kCW * 32);
-        if (ctid == 0) st_release_cta_u32(&s_gu_done, (uint32_t)(ti + 1));
+        signal_buf_full();
       } else {
         // ===== down tile: RT row blocks of Wd for expert ai =====
-        const int td = d0 + ti - n_gt, ai = td / DPE, rp = td % DPE;
+        const int td = d0 + ti - n_gt, ai = td / DPE;
         const int hi_idx = ai - a_first, hs = hi_idx % kHSlots;
         if (ok && s_hexp[hs] != ai) {
           const uint64_t t0 = globaltimer();
@@ -616,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           ok = false;
         }
-        if (ctid == 0 && ti == n_gt) MOE_TL(g_ffn_timeline, cta, 10);
+        if (tid == 0 && ti == n_gt) MOE_TL(g_ffn_timeline, cta, 10);
         const uint8_t* hb = hbuf + (size_t)hs * NT * 8 * hrow;
         float acc[kMaxRT][NT][2][4];
 #pragma unroll
@@ -648,68 +702,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // the last down tile of expert ai in this CTA releases its h slot
+        // this warp is done reading expert ai's h slot after its last tile of ai
         const bool last_of_expert = (ti + 1 == n_gt + n_dt) || ((d0 + ti + 1 - n_gt) / DPE != ai);
-        // partials -> shared memory, reduced over the 8 warps in order
-        float* mine = rbuf + ((size_t)warp * 32 + lane) * RPL;
+        if (last_of_expert && lane == 0) mbar_arrive(&hempty[hs]);
+        wait_buf_free(ti);
+        if (ok) {
 #pragma unroll
-        for (int r = 0; r < kMaxRT; ++r)
+          for (int r = 0; r < kMaxRT; ++r)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+              for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                if (r < RT) mine[(r * NT + nt) * 8 + mt * 4 + i] = acc[r][nt][mt][i];
-        named_bar(1, kCW * 32);
-        if (ctid == 0 && last_of_expert) mbar_arrive(&hempty[hs]);
-        // warp w finishes fragment element e = w of every (row block, token tile)
-        {
-          const int e = warp, mt = e >> 2, i = e & 3;
-          for (int r = 0; r < RT; ++r) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              float o = 0.f;
-#pragma unroll
-              for (int w = 0; w < kCW; ++w)
-                o += rbuf[((size_t)w * 32 + lane) * RPL + (r * NT + nt) * 8 + e];
-              const int tok = nt * 8 + 2 * cq + (i & 1);
-              if (tok < T) {
-                const int row = (rp * RT + r) * 32 + mt * 16 + gq + 8 * (i >> 1);
-                a.obuf[((size_t)ai * T + tok) * d + row] = o;
-              }
-            }
-          }
+                for (int i = 0; i < 4; ++i)
+                  if (r < RT) mine[(r * NT + nt) * 8 + mt * 4 + i] = acc[r][nt][mt][i];
         }
-        named_bar(1, kCW * 32);   // the partial buffer is reused by the next tile
+        signal_buf_full();
       }
     }
-    if (ctid == 0) MOE_TL(g_ffn_timeline, cta, 11);
-    // ---- every CTA's expert outputs are written: combine this CTA's slice
-    // of y in a fixed order (shared expert, then the picks in ascending id);
-    // the loads of one output are all issued before the sum
-    named_bar(1, kCW * 32);
-    if (ctid == 0) {
-      red_release_add(gbar_end, 1u);
-      if (!wait_flag_geq(gbar_end, (uint32_t)G)) set_error(a.err, DEV_TIMEOUT_FLAG);
-      MOE_TL(g_ffn_timeline, cta, 12);
-    }
-    named_bar(1, kCW * 32);
-    const int total = T * d;
-    const int q1 = (int)((long long)(cta + 1) * total / G);
-    for (int q = (int)((long long)cta * total / G) + ctid; q < q1; q += kCW * 32) {
-      const int t = q / d, r = q - t * d;
-      float ov[kMaxTopK];
-#pragma unroll
-      for (int k2 = 0; k2 < kMaxTopK; ++k2)
-        ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + r) : 0.f;
-      float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + r);
-#pragma unroll
-      for (int k2 = 0; k2 < kMaxTopK; ++k2)
-        if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
-      a.y[q] = yv;
-    }
-    if (ctid == 0) MOE_TL(g_ffn_timeline, cta, 13);
+    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 13);
   }
 }
 
@@ -722,8 +733,8 @@ extern "C" int moe_debug_timeline_ffn(unsigned long long* out) {
 template <int NT, bool FUSED>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   const size_t smem = ffn_smem_bytes<NT>(a.d, a.f);
-  if (route_scratch_bytes(FUSED ? a.E : 0, a.nx) > (size_t)FfnCfg<NT>::kStages * kStageBytes ||
-      a.nx > kThreads || (FUSED && a.E > kTabPerThread * kThreads))
+  if (route_scratch_bytes(FUSED ? a.E : 0) > (size_t)FfnCfg<NT>::kStages * kStageBytes ||
+      (FUSED && a.E > kTabPerThread * kThreads))
     return cudaErrorInvalidValue;
   // x is staged in the h + partial area
   if ((size_t)a.T * x_row_elems(a.d) * 2 >
@@ -754,28 +765,6 @@ cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl) {
   if (a.grid <= 0) return cudaErrorInvalidValue;
   if (a.T <= 8) return a.fused ? launch_nt<1, true>(a, s, pdl, a.grid) : launch_nt<1, false>(a, s, pdl, a.grid);
   return a.fused ? launch_nt<2, true>(a, s, pdl, a.grid) : launch_nt<2, false>(a, s, pdl, a.grid);
-}
-
-// CTA c of G takes gate/up tiles [g_c, g_c+1) of the n*f/32 (n = experts of
-// the call, shared one included): g_c = floor(c*NG/G).  Its down tiles
-// [d_c, d_c+1) make up the rest of an equal share of the call's blocks:
-// d_c = the rounded count of down tiles that the bytes of CTAs 0..c-1 leave
-// after their gate/up tiles, made monotone by a running maximum; d_G = all.
-void decode_partition(int G, int nx, int d, int f, int2* out) {
-  const int RT = down_rows_per_tile(f);
-  const long long RG = f / 32, DPE = (d / 32) / RT;
-  const long long BG = 2LL * (d / 32), BD = (long long)RT * (f / 32);   // blocks per tile
-  for (int n = 0; n < nx; ++n) {
-    const long long NG = n * RG, ND = n * DPE, W = NG * BG + ND * BD;
-    long long m = 0;
-    for (int c = 0; c <= G; ++c) {
-      const long long g = (long long)c * NG / G;
-      long long v = ((long long)c * W / G - g * BG + BD / 2) / BD;
-      v = v < 0 ? 0 : (v > ND ? ND : v);
-      m = v > m ? v : m;
-      out[(size_t)c * nx + n] = make_int2((int)g, c == G ? (int)ND : (int)m);
-    }
-  }
 }
 
 }  // namespace moe

@@ -99,15 +99,13 @@ struct FfnArgs {
   uint16_t* hbuf;               // [max_exp][T][f] fp16 h of each expert
   float* obuf;                  // [max_exp][T][d] fp32 output of each expert
   // per-call counters: word 0 counts decode calls; then two sets of
-  // set_words words (h_ready[max_exp] | router barrier | output barrier), used by
+  // set_words words (h_ready[max_exp] | router barrier | d_cnt[d/32]), used by
   // alternate calls.  A call uses set (calls before it) & 1, and the set of
   // the call before it is zeroed during the call (by the fused kernel's CTA 0,
   // or by the commit kernel on the miss path).
   uint32_t* counters;
   int set_words, max_exp;
   uint32_t* err;
-  const int2* part;             // [grid + 1][nx] (gate/up tile, down tile) start of each CTA, per expert count
-  int nx;
   int grid;
   // fused routing (every key resident): router, slot table, LRU stamps, counters
   int fused;
@@ -208,7 +206,5 @@ cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs
 cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
                                 cudaStream_t s, int grid);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
-// CTA work bounds of the decode kernel for grid G and expert counts 0..nx-1
-void decode_partition(int G, int nx, int d, int f, int2* out);
 
 }  // namespace moe

@@ -155,6 +155,17 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, 
 }
 
 // ---------------------------------------------------------- grouped GEMMs ---
+// Optional per-CTA wait profile (build with -DMOE_TIMELINE): clock64 cycles
+// each role spent waiting or working, read back by moe_debug_prefill_profile.
+#ifdef MOE_TIMELINE
+__device__ unsigned long long g_prefill_prof[2][256][16];
+#define PF_T0() const long long pf_t0 = clock64()
+#define PF_ADD(kind, field) (g_prefill_prof[(kind)][blockIdx.x][(field)] += (unsigned long long)(clock64() - pf_t0))
+#else
+#define PF_T0() ((void)0)
+#define PF_ADD(kind, field) ((void)0)
+#endif
+
 namespace pg {
 constexpr int BM = 128, BN = kPrefillBN, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB weight tile
@@ -285,9 +296,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t use = it / STAGES;
-          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-            set_error(a.err, DEV_TIMEOUT_BARRIER);
-            goto done;
+          {
+            PF_T0();
+            if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+              set_error(a.err, DEV_TIMEOUT_BARRIER);
+              goto done;
+            }
+            PF_ADD(DOWN, 9);
           }
           uint8_t* st = stages + s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full_b[s], NB * B_BYTES);
@@ -299,6 +314,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   } else if (warp == 1) {
     // ---- MMA issue ----------------------------------------------------------
     if (lane == 0) {
+      PF_T0();
       uint32_t it = 0, lt = 0;
       for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
         const PrefillTile tl = tiles[ti];
@@ -306,18 +322,34 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         const uint32_t idesc = idesc_f16(BM, nmma, 0);
         const int ab = lt & 1;
         const uint32_t use_b = lt >> 1;
-        if (use_b > 0 && !mbar_wait(&tempty[ab], (use_b - 1) & 1)) {
-          set_error(a.err, DEV_TIMEOUT_BARRIER);
-          goto done;
+        {
+          PF_T0();
+          if (use_b > 0 && !mbar_wait(&tempty[ab], (use_b - 1) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            goto done;
+          }
+          PF_ADD(DOWN, 2);
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + ab * BN;
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t par = (it / STAGES) & 1;
-          if (!mbar_wait(&full_a[s], par) || !mbar_wait(&full_b[s], par)) {
-            set_error(a.err, DEV_TIMEOUT_BARRIER);
-            goto done;
+          {
+            PF_T0();
+            if (!mbar_wait(&full_a[s], par)) {
+              set_error(a.err, DEV_TIMEOUT_BARRIER);
+              goto done;
+            }
+            PF_ADD(DOWN, 0);
+          }
+          {
+            PF_T0();
+            if (!mbar_wait(&full_b[s], par)) {
+              set_error(a.err, DEV_TIMEOUT_BARRIER);
+              goto done;
+            }
+            PF_ADD(DOWN, 1);
           }
           tc_fence_after();
           uint8_t* st = stages + s * STAGE_BYTES;
@@ -335,6 +367,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         }
         umma_commit(&tfull[ab]);
       }
+      PF_ADD(DOWN, 3);
     }
   } else if (warp < EPI0) {
     // ---- weight producers: 3-bit blocks -> fp16 swizzled tiles -------------
@@ -376,17 +409,26 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         __syncwarp();
         issue_next();   // refills the slot consumed PSTAGES-1 items ago
         const int ps = j % PSTAGES;
-        if (!mbar_wait(&my_bar[ps], (j / PSTAGES) & 1)) {
-          set_error(a.err, DEV_TIMEOUT_BARRIER);
-          goto done;
+        {
+          PF_T0();
+          if (!mbar_wait(&my_bar[ps], (j / PSTAGES) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            goto done;
+          }
+          if (p == 0 && lane == 0) PF_ADD(DOWN, 6);
         }
         const uint32_t it = lt * n_kb + kb;
         const int s = it % STAGES;
         const uint32_t use = it / STAGES;
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
-          set_error(a.err, DEV_TIMEOUT_BARRIER);
-          goto done;
+        {
+          PF_T0();
+          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            goto done;
+          }
+          if (p == 0 && lane == 0) PF_ADD(DOWN, 7);
         }
+        PF_T0();
         const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
         const uint8_t* src = my_stage + ps * PCHUNK;
         if (DOWN) {
@@ -402,6 +444,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[s]);
+        if (p == 0 && lane == 0) PF_ADD(DOWN, 8);
       }
     }
   } else {
@@ -413,10 +456,15 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
       const PrefillTile tl = tiles[ti];
       const int ab = lt & 1;
-      if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
-        set_error(a.err, DEV_TIMEOUT_BARRIER);
-        goto done;
+      {
+        PF_T0();
+        if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
+          set_error(a.err, DEV_TIMEOUT_BARRIER);
+          goto done;
+        }
+        if (et == 0) PF_ADD(DOWN, 5);
       }
+      PF_T0();
       tc_fence_after();
       const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
       for (int cc = 0; cc * 32 < tl.nlen; ++cc) {
@@ -481,6 +529,12 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tempty[ab]);
+      if (et == 0) {
+        PF_ADD(DOWN, 4);
+#ifdef MOE_TIMELINE
+        g_prefill_prof[DOWN][blockIdx.x][10] += 1;
+#endif
+      }
     }
   }
 done:
@@ -491,6 +545,16 @@ done:
     tmem_dealloc(tmem, 512);
   }
 }
+
+#ifdef MOE_TIMELINE
+extern "C" int moe_debug_prefill_profile(unsigned long long* out, int reset) {
+  if (reset) {
+    static unsigned long long zero[2][256][16];
+    return (int)cudaMemcpyToSymbol(g_prefill_prof, zero, sizeof(zero));
+  }
+  return (int)cudaMemcpyFromSymbol(out, g_prefill_prof, sizeof(g_prefill_prof));
+}
+#endif
 
 template <bool DOWN>
 static size_t gemm_smem() {

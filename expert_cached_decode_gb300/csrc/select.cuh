@@ -106,7 +106,7 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
   __syncthreads();
   for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
     float* row = s->row[warp];
-#pragma unroll 8
+#pragma unroll 16
     for (int id = lane; id < E; id += 32) row[id] = ld_cg_f32(logits + (size_t)t * E + id);
     __syncwarp();
     float my_v;
