@@ -12,9 +12,12 @@ replayed per step).
 value: tokens/s per MoE layer (= calls/s at T=1) with inputs resident in
 HBM.  e2e: the same through the C ABI with the step's 10,000 tokens copied
 from pinned host memory before and the 10,000 outputs copied back after, in
-the timed region.  roofline: algorithmic bytes of one call, 11 experts x
-2,064,384 B = 22,708,224 B (router weights, 2 MiB, reported separately),
-over the average per-call duration, against the measured HBM copy bandwidth.
+the timed region.  roofline: algorithmic bytes of one call, the distinct
+experts it runs (11 at T=1, counted from the cache statistics) x 2,064,384 B
+= 22,708,224 B at T=1 (router weights, 2 MiB, reported separately), over the
+average per-call duration (one kernel launch per call), against the
+measured HBM copy bandwidth.  --tokens T runs verify batches of T tokens
+per call instead (value then counts all T tokens).
 cpu_baseline: the fp64 CPU oracle on a bounded sample of calls.
 
 --impl reference times the CPU oracle itself (the pages publish no code and
@@ -37,7 +40,6 @@ import numpy as np
 
 CALLS = 10_000
 EXPERT_BYTES = 2_064_384
-ALG_BYTES_PER_CALL = 11 * EXPERT_BYTES
 ROUTER_BYTES = 512 * 2048 * 2
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "MoE expert-stack tokens/s (decode & 12,288-chunk prefill); HBM GB/s vs roofline"
@@ -142,7 +144,12 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def build_decode_layer(calls, seed_cfg=2):
+def workload_name(calls, T):
+    name = WORKLOAD if T == 1 else WORKLOAD.replace("T=1 token per call", f"T={T} tokens per call (verify batch)")
+    return name if calls == CALLS else name + f" (profiling run: {calls} calls)"
+
+
+def build_decode_layer(calls, seed_cfg=2, T=1):
     import torch
     from moe_inputs import synth
     from expert_cached_decode_gb300.layer import MoELayer
@@ -158,7 +165,7 @@ def build_decode_layer(calls, seed_cfg=2):
                      shared, pool)
     layer._pool = pool
     layer.moe_cache_configure(wl.capacity, np.arange(wl.keys))
-    xs = s.tokens_many(0, list(range(calls)), T=1).reshape(calls, wl.d)
+    xs = s.tokens_many(0, list(range(calls)), T=T).reshape(calls, T, wl.d)
     return s, layer, xs
 
 
@@ -436,24 +443,25 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     CALLS = args.calls
-    s, layer, xs = build_decode_layer(CALLS)
+    T = args.tokens
+    s, layer, xs = build_decode_layer(CALLS, T=T)
     wl = s.wl
     d = wl.d
     x_host = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_host.cuda()
-    y_dev = torch.empty((CALLS, d), dtype=torch.float32, device="cuda")
-    y_host = torch.empty((CALLS, d), dtype=torch.float32).pin_memory()
+    y_dev = torch.empty((CALLS, T, d), dtype=torch.float32, device="cuda")
+    y_host = torch.empty((CALLS, T, d), dtype=torch.float32).pin_memory()
 
     stream = torch.cuda.Stream()
     # warm the kernels (function attributes, first launches) outside capture
     with torch.cuda.stream(stream):
         for i in range(8):
-            layer.moe_forward(0, x_dev[i:i + 1], y_dev[i:i + 1])
+            layer.moe_forward(0, x_dev[i], y_dev[i])
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(CALLS):
-            layer.moe_forward(0, x_dev[i:i + 1], y_dev[i:i + 1])
+            layer.moe_forward(0, x_dev[i], y_dev[i])
     torch.cuda.synchronize()
     layer.moe_sync()
 
@@ -463,6 +471,7 @@ def run_gpu(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    st0 = layer.moe_cache_stats()
     cur = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk = ClockSampler(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
@@ -481,8 +490,12 @@ def run_gpu(args):
         dist.barrier()
     ms = e0.elapsed_time(e1)
     layer.moe_sync()
+    st1 = layer.moe_cache_stats()
+    # distinct routed experts per call in the timed steps (+ the shared one)
+    exp_per_call = 1.0 + (st1["distinct_hits"] - st0["distinct_hits"]) / max(1, st1["layer_calls"] - st0["layer_calls"])
+    alg_bytes = exp_per_call * EXPERT_BYTES
     ms = reduce_max(ms, dist, "cuda")
-    value = whole_job_rate(CALLS * args.steps, ws, ms)
+    value = whole_job_rate(CALLS * T * args.steps, ws, ms)
     per_call_s = (ms / 1e3) / (CALLS * args.steps)
 
     # end to end: H2D of the step's inputs, the calls, D2H of the outputs
@@ -503,32 +516,35 @@ def run_gpu(args):
     e3.record(cur)
     torch.cuda.synchronize()
     ms_e2e = reduce_max(e2.elapsed_time(e3), dist, "cuda")
+    e2e_value = whole_job_rate(CALLS * T * args.steps, ws, ms_e2e)
     if dist:
         dist.barrier()
     stats = layer.moe_cache_stats()
 
     if rank == 0:
         hbm, peak_kind = peaks()
-        achieved = ALG_BYTES_PER_CALL / per_call_s / 1e9
+        achieved = alg_bytes / per_call_s / 1e9
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma operands, f32 accumulate (3-bit weights)",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD if CALLS == 10_000 else WORKLOAD + f" (profiling run: {CALLS} calls)",
-                       "calls_per_step": CALLS, "us_per_call": 1e6 * per_call_s, "tokens_per_call": 1, "layers": 1,
+            "config": {"workload": workload_name(CALLS, T),
+                       "calls_per_step": CALLS, "us_per_call": 1e6 * per_call_s, "tokens_per_call": T, "layers": 1,
+                       "experts_per_call": exp_per_call,
                        "l2": "inputs larger than L2: 512 resident experts = 1.06 GB > 129 MB L2 "
                              "(the shared expert and the router stay L2-resident across calls)",
                        "graph": "10,000 moe_forward calls captured once, replayed per step",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "stack_tokens_per_s_derived": value / 48.0},
-            "gpu_launches": 2 * CALLS * args.steps,
+            "gpu_launches": CALLS * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": recorded_traffic(),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                         "kernel": "route_kernel + decode_ffn_kernel per call (duration of the whole call)",
-                         "alg_bytes_per_launch": ALG_BYTES_PER_CALL, "router_bytes": ROUTER_BYTES},
-            "e2e": {"value": whole_job_rate(CALLS * args.steps, ws, ms_e2e), "unit": "tokens/s",
+                         "kernel": "decode_ffn_kernel with fused routing: one launch per call (average launch "
+                                   "duration = call duration, launch gaps included)",
+                         "alg_bytes_per_launch": alg_bytes, "router_bytes": ROUTER_BYTES},
+            "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(y_host.numel() * 4)},
             "clocks": clk.summary(local),
             "cache": {"token_hits": stats["token_hits"], "token_misses": stats["token_misses"]},
@@ -543,7 +559,7 @@ def run_gpu(args):
                 line["stack"] = [run_stack(c, args.stack_pool) for c in (3, 4)]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and T == 1:
             n = args.cpu_calls
             r = cpu_oracle_sample(n)
             line["cpu_baseline"] = {"value": n / r["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -572,6 +588,8 @@ def main():
                     help="host-pool entries for --stack (default: one per (layer, expert), 50.7 GB)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="time only the prefill path at T tokens (profiling runs)")
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="T",
+                    help="tokens per decode call (1 + draft tokens verified together; the workload is T=1)")
     ap.add_argument("--calls", type=int, default=CALLS,
                     help="calls per step (the workload is 10,000; smaller only for profiling)")
     args = ap.parse_args()

@@ -157,13 +157,21 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, 
 // ---------------------------------------------------------- grouped GEMMs ---
 // Optional per-CTA wait profile (build with -DMOE_TIMELINE): clock64 cycles
 // each role spent waiting or working, read back by moe_debug_prefill_profile.
+// Per-k-block amounts gather in registers (PF_ACC) and are stored once
+// (PF_PUT), so the profile does not add global round trips to the loops.
 #ifdef MOE_TIMELINE
 __device__ unsigned long long g_prefill_prof[2][256][16];
 #define PF_T0() const long long pf_t0 = clock64()
 #define PF_ADD(kind, field) (g_prefill_prof[(kind)][blockIdx.x][(field)] += (unsigned long long)(clock64() - pf_t0))
+#define PF_VAR(v) long long v = 0
+#define PF_ACC(v) (v += clock64() - pf_t0)
+#define PF_PUT(kind, field, v) (g_prefill_prof[(kind)][blockIdx.x][(field)] += (unsigned long long)(v))
 #else
 #define PF_T0() ((void)0)
 #define PF_ADD(kind, field) ((void)0)
+#define PF_VAR(v) ((void)0)
+#define PF_ACC(v) ((void)0)
+#define PF_PUT(kind, field, v) ((void)0)
 #endif
 
 namespace pg {
@@ -174,7 +182,8 @@ constexpr int NPROD = 8;               // dequant warps
 constexpr int PSTAGES = 4;             // packed-weight staging depth per producer
 constexpr int PCHUNK = 2 * kBlockBytes;   // packed bytes per producer and k block
 constexpr int EPI0 = 2 + NPROD;        // first epilogue warp
-constexpr int THREADS = (EPI0 + 4) * 32;   // 0 TMA, 1 MMA, 2-9 producers, 10-13 epilogue
+constexpr int NEPI = 8;                // epilogue warps: 4 TMEM quarters x 2 column halves
+constexpr int THREADS = (EPI0 + NEPI) * 32;   // 0 TMA, 1 MMA, 2-9 producers, 10-17 epilogue
 constexpr int GU_ROWS = BM / 2;        // f rows per gate/up tile (Wg rows, then the same Wu rows)
 }  // namespace pg
 
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  constexpr int EPI_BYTES = DOWN ? 32 * BM * 4 : 32 * GU_ROWS * 4 + 2 * 32 * GU_ROWS * 2;
+  constexpr int EPI_BYTES = DOWN ? 0 : 4 * 2 * 16 * 32 * 4;   // u exchange slots
   uint8_t* epi = smem + STAGES * STAGE_BYTES;
   uint8_t* pstage = epi + EPI_BYTES;                               // NPROD * PSTAGES * PCHUNK
   uint64_t* bars = reinterpret_cast<uint64_t*>(pstage + NPROD * PSTAGES * PCHUNK);
@@ -243,8 +252,6 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* pbar = tempty + 2;                                     // NPROD * PSTAGES
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pbar + NPROD * PSTAGES);
-  __shared__ float s_w[32];
-  __shared__ int s_tok[32];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = a.n_tiles[DOWN ? 1 : 0];
@@ -260,7 +267,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], NEPI);
     }
     for (int i = 0; i < NPROD * PSTAGES; ++i) mbar_init(&pbar[i], 1);
     mbar_init_fence();
@@ -290,6 +297,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   if (warp == 0) {
     // ---- token tiles by TMA -------------------------------------------------
     if (lane == 0) {
+      PF_VAR(pf_t9);
       uint32_t it = 0;
       for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
         const PrefillTile tl = tiles[ti];
@@ -302,7 +310,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               set_error(a.err, DEV_TIMEOUT_BARRIER);
               goto done;
             }
-            PF_ADD(DOWN, 9);
+            PF_ACC(pf_t9);
           }
           uint8_t* st = stages + s * STAGE_BYTES;
           mbar_arrive_expect_tx(&full_b[s], NB * B_BYTES);
@@ -310,11 +318,15 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
           if (DOWN) tma_load_2d(st + A_BYTES + B_BYTES, &tmB2, kb * BK, tl.row0, &full_b[s]);
         }
       }
+      PF_PUT(DOWN, 9, pf_t9);
     }
   } else if (warp == 1) {
     // ---- MMA issue ----------------------------------------------------------
     if (lane == 0) {
       PF_T0();
+      PF_VAR(pf_wa);
+      PF_VAR(pf_wb);
+      PF_VAR(pf_is);
       uint32_t it = 0, lt = 0;
       for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
         const PrefillTile tl = tiles[ti];
@@ -341,7 +353,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               set_error(a.err, DEV_TIMEOUT_BARRIER);
               goto done;
             }
-            PF_ADD(DOWN, 0);
+            PF_ACC(pf_wa);
           }
           {
             PF_T0();
@@ -349,8 +361,9 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               set_error(a.err, DEV_TIMEOUT_BARRIER);
               goto done;
             }
-            PF_ADD(DOWN, 1);
+            PF_ACC(pf_wb);
           }
+          PF_T0();
           tc_fence_after();
           uint8_t* st = stages + s * STAGE_BYTES;
           const uint64_t da = smem_desc_sw128(st);
@@ -364,10 +377,14 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             }
           }
           umma_commit(&empty[s]);
+          PF_ACC(pf_is);
         }
         umma_commit(&tfull[ab]);
       }
       PF_ADD(DOWN, 3);
+      PF_PUT(DOWN, 0, pf_wa);
+      PF_PUT(DOWN, 1, pf_wb);
+      PF_PUT(DOWN, 11, pf_is);
     }
   } else if (warp < EPI0) {
     // ---- weight producers: 3-bit blocks -> fp16 swizzled tiles -------------
@@ -403,6 +420,9 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       }
     };
     for (int i = 0; i < PSTAGES - 1; ++i) issue_next();
+    PF_VAR(pf_p6);
+    PF_VAR(pf_p7);
+    PF_VAR(pf_p8);
     uint32_t j = 0, lt = 0;
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
       for (int kb = par; kb < n_kb; kb += 2, ++j) {
@@ -415,7 +435,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             goto done;
           }
-          if (p == 0 && lane == 0) PF_ADD(DOWN, 6);
+          PF_ACC(pf_p6);
         }
         const uint32_t it = lt * n_kb + kb;
         const int s = it % STAGES;
@@ -426,7 +446,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             goto done;
           }
-          if (p == 0 && lane == 0) PF_ADD(DOWN, 7);
+          PF_ACC(pf_p7);
         }
         PF_T0();
         const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
@@ -444,92 +464,105 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_a[s]);
-        if (p == 0 && lane == 0) PF_ADD(DOWN, 8);
+        PF_ACC(pf_p8);
       }
     }
+    if (p == 0 && lane == 0) {
+      PF_PUT(DOWN, 6, pf_p6);
+      PF_PUT(DOWN, 7, pf_p7);
+      PF_PUT(DOWN, 8, pf_p8);
+    }
   } else {
-    // ---- epilogue: warps EPI0.. cover the four 32-lane quarters of TMEM ----
+    // ---- epilogue: 8 warps; warp (quarter q = warp % 4, half hf) reads TMEM
+    // lanes 32q..32q+31 (M rows) and, of every 32-column chunk, the 16
+    // columns (tokens) 16hf..16hf+15.  No block-wide barrier: each warp
+    // writes its own rows straight to global memory.
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;            // M row of the tile
-    const int et = threadIdx.x - EPI0 * 32;         // 0..127
-    uint32_t lt = 0;
+    const int hf = (warp - EPI0) >> 2;
+    const int ew = warp - EPI0;                     // 0..7
+    uint32_t lt = 0, chunk = 0;                     // chunk: running count across tiles
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
       const PrefillTile tl = tiles[ti];
       const int ab = lt & 1;
+      // down: the token and routing weight of every column this warp reads,
+      // loaded before the accumulator is ready (lane j of chunk cc holds
+      // column cc*32 + 16hf + j, j < 16)
+      int ctok[kPrefillBN / 32];
+      float cw[kPrefillBN / 32];
+      if (DOWN) {
+#pragma unroll
+        for (int cc = 0; cc < kPrefillBN / 32; ++cc) {
+          const int col = cc * 32 + hf * 16 + (lane & 15);
+          ctok[cc] = col < tl.nlen ? a.perm[tl.row0 + col] : 0;
+          cw[cc] = col < tl.nlen ? a.wsort[tl.row0 + col] : 0.f;
+        }
+      }
       {
         PF_T0();
         if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           goto done;
         }
-        if (et == 0) PF_ADD(DOWN, 5);
+        if (ew == 0 && lane == 0) PF_ADD(DOWN, 5);
       }
       PF_T0();
       tc_fence_after();
-      const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-      for (int cc = 0; cc * 32 < tl.nlen; ++cc) {
-        const int nrow = min(32, tl.nlen - cc * 32);
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + ab * BN + cc * 32, r);
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN + hf * 16;
+#pragma unroll 1
+      for (int cc = 0; cc * 32 < tl.nlen; ++cc, ++chunk) {
+        const int col0 = cc * 32 + hf * 16;          // first column (token) of this warp
+        uint32_t r[16];
+        tmem_ld16(taddr + cc * 32, r);
         tmem_ld_wait();
         if (!DOWN) {
-          // M rows 64-127 (u) go through shared memory to the warps holding
-          // the matching g rows 0-63; those write h = silu(g) * u as an fp16
-          // pair (hi = RN(h), lo = RN(h - hi)) staged [token][64 f rows]
-          float* eu = reinterpret_cast<float*>(epi);                       // [32 tokens][64]
-          __half* ehi = reinterpret_cast<__half*>(epi + 32 * GU_ROWS * 4);  // [32][64]
-          __half* elo = ehi + 32 * GU_ROWS;
+          // g rows sit in quarters 0-1, the same f rows of u in quarters 2-3:
+          // the u warp hands its values to its g warp through a two-slot
+          // exchange buffer and a 64-thread barrier (ids 1-4, one per pair);
+          // slots alternate by the running chunk count, so a slot is written
+          // again only after the g warp has passed the barrier of the chunk
+          // after the one that read it
+          const int pair = (quarter & 1) + 2 * hf;
+          float* slot = reinterpret_cast<float*>(epi) + ((size_t)pair * 2 + (chunk & 1)) * 16 * 32;
           if (quarter >= 2) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) eu[jj * GU_ROWS + row - GU_ROWS] = __uint_as_float(r[jj]);
-          }
-          named_bar(1, 128);
-          if (quarter < 2) {
+            for (int jj = 0; jj < 16; ++jj) slot[jj * 32 + lane] = __uint_as_float(r[jj]);
+            named_bar(1 + pair, 64);
+          } else {
+            named_bar(1 + pair, 64);
+            const int frow = tl.m * GU_ROWS + quarter * 32 + lane;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const float gv = __uint_as_float(r[jj]), uv = eu[jj * GU_ROWS + row];
-              const float hv = gv / (1.f + expf(-gv)) * uv;
-              const __half hi = __float2half_rn(hv);
-              ehi[jj * GU_ROWS + row] = hi;
-              elo[jj * GU_ROWS + row] = __float2half_rn(hv - __half2float(hi));
+            for (int jj = 0; jj < 16; ++jj) {
+              if (col0 + jj < tl.nlen) {
+                const float gv = __uint_as_float(r[jj]), uv = slot[jj * 32 + lane];
+                const float hv = gv / (1.f + expf(-gv)) * uv;
+                const __half hi = __float2half_rn(hv);
+                const size_t o = (size_t)(tl.row0 + col0 + jj) * a.f + frow;
+                a.hg[o] = __half_as_ushort(hi);
+                a.hg_lo[o] = __half_as_ushort(__float2half_rn(hv - __half2float(hi)));
+              }
             }
           }
-          named_bar(1, 128);
-          // 32 token rows x 64 f values (128 B) of hi, then of lo
-          for (int q = et; q < 2 * 32 * 8; q += 128) {
-            const int part = q >> 8, jj = (q >> 3) & 31, ch = q & 7;
-            if (jj < nrow) {
-              const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(part ? elo : ehi) +
-                                                              jj * 128 + ch * 16);
-              uint16_t* dst = part ? a.hg_lo : a.hg;
-              *reinterpret_cast<uint4*>(dst + (size_t)(tl.row0 + cc * 32 + jj) * a.f + tl.m * GU_ROWS + ch * 8) = v;
-            }
-          }
-          named_bar(1, 128);
         } else {
-          if (et < 32) {
-            const int jj = et;
-            s_w[jj] = jj < nrow ? a.wsort[tl.row0 + cc * 32 + jj] : 0.f;
-            s_tok[jj] = jj < nrow ? a.perm[tl.row0 + cc * 32 + jj] : 0;
-          }
-          named_bar(1, 128);
-          float* ef = reinterpret_cast<float*>(epi);
+          int tokc = 0;
+          float wc = 0.f;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) ef[jj * BM + row] = __uint_as_float(r[jj]) * s_w[jj];
-          named_bar(1, 128);
-          for (int q = et; q < 32 * 32; q += 128) {
-            const int jj = q >> 5, r4 = q & 31;
-            if (jj < nrow) {
-              const float4 v = *reinterpret_cast<const float4*>(ef + jj * BM + r4 * 4);
-              red_add_v4(a.y + (size_t)s_tok[jj] * a.d + tl.m * BM + r4 * 4, v.x, v.y, v.z, v.w);
+          for (int q = 0; q < kPrefillBN / 32; ++q)
+            if (q == cc) {
+              tokc = ctok[q];
+              wc = cw[q];
             }
+          float* ycol = a.y + tl.m * BM + quarter * 32 + lane;
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int tok = __shfl_sync(0xffffffffu, tokc, jj);
+            const float w = __shfl_sync(0xffffffffu, wc, jj);
+            if (col0 + jj < tl.nlen) red_add_f32(ycol + (size_t)tok * a.d, __uint_as_float(r[jj]) * w);
           }
-          named_bar(1, 128);
         }
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tempty[ab]);
-      if (et == 0) {
+      if (ew == 0 && lane == 0) {
         PF_ADD(DOWN, 4);
 #ifdef MOE_TIMELINE
         g_prefill_prof[DOWN][blockIdx.x][10] += 1;
@@ -561,7 +594,7 @@ static size_t gemm_smem() {
   constexpr int NB = DOWN ? 2 : 1;
   constexpr int STAGES = DOWN ? 2 : 3;
   constexpr int STAGE_BYTES = pg::A_BYTES + NB * pg::B_BYTES;
-  constexpr int EPI_BYTES = DOWN ? 32 * pg::BM * 4 : 32 * pg::GU_ROWS * 4 + 2 * 32 * pg::GU_ROWS * 2;
+  constexpr int EPI_BYTES = DOWN ? 0 : 4 * 2 * 16 * 32 * 4;
   return 1024 + STAGES * STAGE_BYTES + EPI_BYTES + pg::NPROD * pg::PSTAGES * pg::PCHUNK +
          (3 * STAGES + 4 + pg::NPROD * pg::PSTAGES) * 8 + 16;
 }
