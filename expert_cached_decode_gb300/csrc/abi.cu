@@ -606,6 +606,8 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
     return fail(MOE_ERR_UNIMPLEMENTED, "prefill (T > %d) needs every expert resident in this build", kMaxDecodeT);
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
     return fail(MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
+  if (c->f % 128 != 0)
+    return fail(MOE_ERR_UNIMPLEMENTED, "prefill (T > %d) needs f %% 128 == 0 (f = %d)", kMaxDecodeT, c->f);
   moe_status st = ensure_prefill_scratch(c);
   if (st == MOE_OK) st = ensure_prefill_ffn_scratch(c);
   if (st != MOE_OK) return st;
@@ -645,9 +647,10 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   CUDA_TRY(launch_prefill_gather(static_cast<const uint16_t*>(x), c->p_perm, c->p_xg, rows, c->d, s));
   CUDA_TRY(cudaMemsetAsync(y, 0, (size_t)T * c->d * sizeof(float), s));
   CUtensorMap tx, th, thl;
-  st = make_tmap_2d(&tx, c->p_xg, rows, c->d, kPrefillBN, false);
-  if (st == MOE_OK) st = make_tmap_2d(&th, c->p_hg, rows, c->f, kPrefillBN, false);
-  if (st == MOE_OK) st = make_tmap_2d(&thl, c->p_hg_lo, rows, c->f, kPrefillBN, false);
+  // token tiles are loaded in two halves, one by each CTA of a cluster pair
+  st = make_tmap_2d(&tx, c->p_xg, rows, c->d, kPrefillBN / 2, false);
+  if (st == MOE_OK) st = make_tmap_2d(&th, c->p_hg, rows, c->f, kPrefillBN / 2, false);
+  if (st == MOE_OK) st = make_tmap_2d(&thl, c->p_hg_lo, rows, c->f, kPrefillBN / 2, false);
   if (st != MOE_OK) return st;
   PrefillGemmArgs ga{};
   ga.slots = c->slots;

@@ -185,6 +185,9 @@ constexpr int EPI0 = 2 + NPROD;        // first epilogue warp
 constexpr int NEPI = 8;                // epilogue warps: 4 TMEM quarters x 2 column halves
 constexpr int THREADS = (EPI0 + NEPI) * 32;   // 0 TMA, 1 MMA, 2-9 producers, 10-17 epilogue
 constexpr int GU_ROWS = BM / 2;        // f rows per gate/up tile (Wg rows, then the same Wu rows)
+constexpr int MAX_CTA_TILES = 128;     // tile descriptors of a CTA kept in shared memory
+constexpr int CLUSTER = 2;             // CTAs sharing each token tile (TMA multicast)
+constexpr int B_HALF = B_BYTES / CLUSTER;   // token rows a CTA loads for both
 }  // namespace pg
 
 // Expand one 32x32 block (448 B at `bp`, shared memory) into 32 rows and 32
@@ -258,12 +261,23 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   const int K = DOWN ? a.f : a.d;
   const int n_kb = K / BK;   // even (K is a multiple of 128)
   const PrefillTile* tiles = DOWN ? a.tiles_dn : a.tiles_gu;
+  // this CTA's tiles are blockIdx.x + lt * gridDim.x; their descriptors are
+  // read once into shared memory (beyond MAX_CTA_TILES from global memory)
+  __shared__ PrefillTile s_tiles[MAX_CTA_TILES];
+  for (int l = threadIdx.x; l < MAX_CTA_TILES; l += blockDim.x) {
+    const int ti = blockIdx.x + l * gridDim.x;
+    if (ti < n_tiles) s_tiles[l] = tiles[ti];
+  }
+  auto tile_at = [&](int ti) -> PrefillTile {
+    const int l = (ti - (int)blockIdx.x) / (int)gridDim.x;
+    return l < MAX_CTA_TILES ? s_tiles[l] : tiles[ti];
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_a[i], NPROD / 2);
       mbar_init(&full_b[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], CLUSTER);   // the MMAs of both CTAs of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -282,6 +296,10 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the peer CTA multicasts into this CTA's stages and arrives on its
+  // barriers: both must have initialised them first
+  cluster_sync();
+  const uint32_t crank = blockIdx.x % CLUSTER;
 
   auto weights = [&](int group) -> const uint8_t* {
     return group < a.E ? a.slots + (int64_t)a.group_slot[group] * a.expert_bytes : a.shared_expert;
@@ -298,10 +316,26 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     // ---- token tiles by TMA -------------------------------------------------
     if (lane == 0) {
       PF_VAR(pf_t9);
+      // the token tiles of the item kPrefetch ahead are prefetched into L2, so
+      // a stage's load waits for L2 rather than DRAM
+      constexpr int kPrefetch = 4;
+      int pf_ti = blockIdx.x, pf_kb = 0;
+      auto prefetch_next = [&]() {
+        if (pf_ti >= n_tiles) return;
+        const int row0 = tile_at(pf_ti).row0 + (int)crank * (BN / CLUSTER);
+        tma_prefetch_l2_2d(&tmB, pf_kb * BK, row0);
+        if (DOWN) tma_prefetch_l2_2d(&tmB2, pf_kb * BK, row0);
+        if (++pf_kb == n_kb) {
+          pf_kb = 0;
+          pf_ti += gridDim.x;
+        }
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch_next();
       uint32_t it = 0;
       for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
-        const PrefillTile tl = tiles[ti];
+        const PrefillTile tl = tile_at(ti);
         for (int kb = 0; kb < n_kb; ++kb, ++it) {
+          prefetch_next();
           const int s = it % STAGES;
           const uint32_t use = it / STAGES;
           {
@@ -313,9 +347,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
             PF_ACC(pf_t9);
           }
           uint8_t* st = stages + s * STAGE_BYTES;
+          // this CTA loads token rows [crank * BN/2, +BN/2) of the tile for
+          // both CTAs of the cluster (the other half comes from the peer)
           mbar_arrive_expect_tx(&full_b[s], NB * B_BYTES);
-          tma_load_2d(st + A_BYTES, &tmB, kb * BK, tl.row0, &full_b[s]);
-          if (DOWN) tma_load_2d(st + A_BYTES + B_BYTES, &tmB2, kb * BK, tl.row0, &full_b[s]);
+          const int yrow = tl.row0 + (int)crank * (BN / CLUSTER);
+          tma_load_2d_multicast(st + A_BYTES + crank * B_HALF, &tmB, kb * BK, yrow, &full_b[s], 0x3);
+          if (DOWN)
+            tma_load_2d_multicast(st + A_BYTES + B_BYTES + crank * B_HALF, &tmB2, kb * BK, yrow, &full_b[s], 0x3);
         }
       }
       PF_PUT(DOWN, 9, pf_t9);
@@ -329,7 +367,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       PF_VAR(pf_is);
       uint32_t it = 0, lt = 0;
       for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
-        const PrefillTile tl = tiles[ti];
+        const PrefillTile tl = tile_at(ti);
         const int nmma = (tl.nlen + 15) & ~15;
         const uint32_t idesc = idesc_f16(BM, nmma, 0);
         const int ab = lt & 1;
@@ -376,7 +414,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               umma_f16(d_tmem, da + 2 * kk, db_lo + 2 * kk, idesc, 1u);
             }
           }
-          umma_commit(&empty[s]);
+          umma_commit_multicast(&empty[s], 0x3);   // frees the stage in both CTAs
           PF_ACC(pf_is);
         }
         umma_commit(&tfull[ab]);
@@ -406,7 +444,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     uint32_t n_issued = 0;
     auto issue_next = [&]() {
       if (ti_issue >= n_tiles) return;
-      const PrefillTile tl = tiles[ti_issue];
+      const PrefillTile tl = tile_at(ti_issue);
       const int ps = n_issued % PSTAGES;
       if (lane == 0) {
         mbar_arrive_expect_tx(&my_bar[ps], PCHUNK);
@@ -481,8 +519,11 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     const int hf = (warp - EPI0) >> 2;
     const int ew = warp - EPI0;                     // 0..7
     uint32_t lt = 0, chunk = 0;                     // chunk: running count across tiles
+    PF_VAR(pf_e12);
+    PF_VAR(pf_e13);
+    PF_VAR(pf_e14);
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
-      const PrefillTile tl = tiles[ti];
+      const PrefillTile tl = tile_at(ti);
       const int ab = lt & 1;
       // down: the token and routing weight of every column this warp reads,
       // loaded before the accumulator is ready (lane j of chunk cc holds
@@ -512,36 +553,51 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       for (int cc = 0; cc * 32 < tl.nlen; ++cc, ++chunk) {
         const int col0 = cc * 32 + hf * 16;          // first column (token) of this warp
         uint32_t r[16];
-        tmem_ld16(taddr + cc * 32, r);
-        tmem_ld_wait();
+        {
+          PF_T0();
+          tmem_ld16(taddr + cc * 32, r);
+          tmem_ld_wait();
+          PF_ACC(pf_e12);
+        }
         if (!DOWN) {
-          // g rows sit in quarters 0-1, the same f rows of u in quarters 2-3:
-          // the u warp hands its values to its g warp through a two-slot
-          // exchange buffer and a 64-thread barrier (ids 1-4, one per pair);
-          // slots alternate by the running chunk count, so a slot is written
-          // again only after the g warp has passed the barrier of the chunk
-          // after the one that read it
+          // g rows sit in quarters 0-1, the same f rows of u in quarters 2-3.
+          // The two warps of a pair swap halves through a two-slot buffer and
+          // a 64-thread barrier (ids 1-4, one per pair): the g warp gets u of
+          // columns 0-7 and finishes them, the u warp gets g of columns 8-15
+          // and finishes those.  Slots alternate by the running chunk count,
+          // so a slot is written again only after both warps have passed the
+          // barrier of the chunk after the one that read it.
           const int pair = (quarter & 1) + 2 * hf;
+          const bool is_g = quarter < 2;
           float* slot = reinterpret_cast<float*>(epi) + ((size_t)pair * 2 + (chunk & 1)) * 16 * 32;
-          if (quarter >= 2) {
+          float* give = slot + (is_g ? 8 * 32 : 0);        // g 8-15 or u 0-7
+          const float* take = slot + (is_g ? 0 : 8 * 32);  // u 0-7 or g 8-15
+          const int own0 = is_g ? 0 : 8;                    // columns this warp finishes
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) slot[jj * 32 + lane] = __uint_as_float(r[jj]);
+          for (int jj = 0; jj < 8; ++jj) give[jj * 32 + lane] = __uint_as_float(is_g ? r[8 + jj] : r[jj]);
+          {
+            PF_T0();
             named_bar(1 + pair, 64);
-          } else {
-            named_bar(1 + pair, 64);
-            const int frow = tl.m * GU_ROWS + quarter * 32 + lane;
+            PF_ACC(pf_e13);
+          }
+          PF_T0();
+          const int frow = tl.m * GU_ROWS + (quarter & 1) * 32 + lane;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              if (col0 + jj < tl.nlen) {
-                const float gv = __uint_as_float(r[jj]), uv = slot[jj * 32 + lane];
-                const float hv = gv / (1.f + expf(-gv)) * uv;
-                const __half hi = __float2half_rn(hv);
-                const size_t o = (size_t)(tl.row0 + col0 + jj) * a.f + frow;
-                a.hg[o] = __half_as_ushort(hi);
-                a.hg_lo[o] = __half_as_ushort(__float2half_rn(hv - __half2float(hi)));
-              }
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = col0 + own0 + jj;
+            if (col < tl.nlen) {
+              const float mine = __uint_as_float(is_g ? r[jj] : r[8 + jj]), other = take[jj * 32 + lane];
+              const float gv = is_g ? mine : other, uv = is_g ? other : mine;
+              // silu(g) * u with the fast exponential and division (relative
+              // error ~2^-21, below what the fp16 pair carries)
+              const float hv = __fdividef(gv, 1.f + __expf(-gv)) * uv;
+              const __half hi = __float2half_rn(hv);
+              const size_t o = (size_t)(tl.row0 + col) * a.f + frow;
+              a.hg[o] = __half_as_ushort(hi);
+              a.hg_lo[o] = __half_as_ushort(__float2half_rn(hv - __half2float(hi)));
             }
           }
+          PF_ACC(pf_e14);
         } else {
           int tokc = 0;
           float wc = 0.f;
@@ -569,10 +625,17 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
 #endif
       }
     }
+    if (ew == 2 && lane == 0) {
+      PF_PUT(DOWN, 12, pf_e12);
+      PF_PUT(DOWN, 13, pf_e13);
+      PF_PUT(DOWN, 14, pf_e14);
+    }
   }
 done:
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its peer may still write into it
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -601,17 +664,37 @@ static size_t gemm_smem() {
 
 template <bool DOWN>
 static cudaError_t launch_gemm(const CUtensorMap& tmB, const CUtensorMap& tmB2, const PrefillGemmArgs& a,
-                               cudaStream_t s, int grid) {
+                               cudaStream_t s, int num_sms) {
   static bool configured = false;
+  static int grid = 0;
   const size_t smem = gemm_smem<DOWN>();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pg::CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(pg::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    // persistent grid: as many whole clusters as can be resident at once
+    cfg.gridDim = dim3(num_sms - num_sms % pg::CLUSTER);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, prefill_gemm_kernel<DOWN>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    grid = clusters * pg::CLUSTER;
+    if (grid > num_sms) grid = num_sms - num_sms % pg::CLUSTER;
     configured = true;
   }
-  prefill_gemm_kernel<DOWN><<<grid, pg::THREADS, smem, s>>>(tmB, tmB2, a);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(grid);
+  return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<DOWN>, tmB, tmB2, a);
 }
 
 cudaError_t launch_prefill_plan(const PrefillPlanArgs& a, cudaStream_t s) {

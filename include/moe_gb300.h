@@ -136,7 +136,8 @@ moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32
 
 /* One layer-call: route, look up / fill the cache, run the experts and write
  * y[T][d] (fp32, device).  x[T][d] bf16 (device); x and y 16-byte aligned.  1 <= T <= 16 uses the
- * decode path; larger T (up to 16,384) the prefill path.  Asynchronous on
+ * decode path; larger T (up to 16,384) the prefill path, which needs every
+ * key resident and f % 128 == 0 (MOE_ERR_UNIMPLEMENTED otherwise).  Asynchronous on
  * `stream` when every key is resident (see moe_cache_configure); otherwise the
  * host waits for the routing kernel, issues the miss copies on a side stream
  * and joins it with an event before the experts run.  On error the cache
