@@ -39,7 +39,7 @@
 namespace moe {
 
 #ifdef MOE_TIMELINE
-__device__ unsigned long long g_ffn_timeline[512][16];
+__device__ unsigned long long g_ffn_timeline[512][24];
 #endif
 
 constexpr int kCW = 8;                        // consumer warps
@@ -347,7 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       MOE_TL(g_ffn_timeline, cta, 7);
     }
     __syncthreads();
+#ifdef MOE_TIMELINE
+    select_call(a.logits, T, E, K, sel, &g_ffn_timeline[cta][16]);
+#else
     select_call(a.logits, T, E, K, sel);
+#endif
     const int n_act = sel->n_act;
     for (int i = tid; i < T * K; i += kThreads) {
       const int id = sel->sel_id[i / K][i % K];

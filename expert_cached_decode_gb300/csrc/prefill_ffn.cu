@@ -74,39 +74,55 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillPlanArgs a) {
   }
   const int n_ntiles = s_nt[n_groups];
   const int MG = a.f / 64, MD = a.d / 128;   // gate/up tiles cover 64 f rows (Wg and Wu)
+  int act = 0;
   for (int g = tid; g < n_groups; g += 1024) {
     const int off = s_off[g];
     const int n = s_off[g + 1] - off;
     if (g < E) a.cursor[g] = off;
     int slot = -1;
     if (g < E && n > 0) {
+      ++act;
       slot = a.table[(size_t)a.layer * E + g];
       if (slot < 0) set_error(a.err, DEV_NOT_RESIDENT);
       else a.stamp[slot] = *a.clock;
     }
     a.group_slot[g] = slot;
-    for (int j = 0; j * kPrefillBN < n; ++j) {
-      const int nt = s_nt[g] + j;
-      PrefillTile tl;
-      tl.group = g;
-      tl.row0 = off + j * kPrefillBN;
-      tl.nlen = min(kPrefillBN, n - j * kPrefillBN);
-      for (int m = 0; m < MG; ++m) {
-        tl.m = m;
-        a.tiles_gu[nt * MG + m] = tl;
-      }
-      for (int m = 0; m < MD; ++m) {
-        tl.m = m;
-        a.tiles_dn[nt * MD + m] = tl;
-      }
+  }
+  // tile lists: thread i writes the tiles of token tiles i, i + 1024, ...;
+  // the group of token tile nt is the last g with s_nt[g] <= nt (an empty
+  // group shares its s_nt with the next group, so the last match is the
+  // non-empty one)
+  for (int nt = tid; nt < n_ntiles; nt += 1024) {
+    int lo = 0, hi = n_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_nt[mid] <= nt) lo = mid; else hi = mid - 1;
+    }
+    const int g = lo, j = nt - s_nt[g];
+    const int off = s_off[g], n = s_off[g + 1] - off;
+    PrefillTile tl;
+    tl.group = g;
+    tl.row0 = off + j * kPrefillBN;
+    tl.nlen = min(kPrefillBN, n - j * kPrefillBN);
+    for (int m = 0; m < MG; ++m) {
+      tl.m = m;
+      a.tiles_gu[nt * MG + m] = tl;
+    }
+    for (int m = 0; m < MD; ++m) {
+      tl.m = m;
+      a.tiles_dn[nt * MD + m] = tl;
     }
   }
+  // distinct routed experts of the chunk
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) act += __shfl_xor_sync(0xffffffffu, act, o);
+  if (lane == 0) s_warp[warp] = act;
   __syncthreads();
   if (tid == 0) {
+    int n_act = 0;
+    for (int w = 0; w < 32; ++w) n_act += s_warp[w];
     a.n_tiles[0] = n_ntiles * MG;
     a.n_tiles[1] = n_ntiles * MD;
-    int n_act = 0;
-    for (int g = 0; g < E; ++g) n_act += (s_off[g + 1] > s_off[g]);
     a.stats[ST_CALLS] += 1;
     a.stats[ST_TOK_HIT] += (int64_t)a.T * a.k;
     a.stats[ST_DIST_HIT] += n_act;
@@ -129,28 +145,36 @@ __global__ void prefill_scatter_kernel(PrefillScatterArgs a) {
   }
 }
 
-// Xg[r] = fp16(x[perm[r]]), one CTA of 256 threads per row (d % 2048 handled by a loop)
+// Xg[r] = fp16(x[perm[r]]): one warp per row at a time, 256 16-byte chunks
+// of the row (8 per lane) loaded before they are converted and stored
 __global__ void __launch_bounds__(256) prefill_gather_kernel(const uint16_t* x, const int32_t* perm, uint16_t* xg,
-                                                             int d) {
-  const int r = blockIdx.x;
-  const int t = perm[r];
-  const uint16_t* src = x + (size_t)t * d;
-  uint16_t* dst = xg + (size_t)r * d;
-  for (int j = threadIdx.x * 8; j < d; j += 256 * 8) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + j));
-    uint4 o;
-    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[4];
+                                                             int rows, int d) {
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int cpr = d / 8;   // 16-byte chunks per row
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)perm[r] * d);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)r * d);
+    for (int c0 = 0; c0 < cpr; c0 += 256) {
+      uint4 v[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const __half2 h = __floats2half2_rn(bf16_bits_to_float(in[q] & 0xffffu), bf16_bits_to_float(in[q] >> 16));
-      out[q] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int u = 0; u < 8; ++u)
+        if (c0 + lane + 32 * u < cpr) v[u] = __ldg(src + c0 + lane + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + lane + 32 * u < cpr) {
+          const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          uint32_t out[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __half2 h =
+                __floats2half2_rn(bf16_bits_to_float(in[q] & 0xffffu), bf16_bits_to_float(in[q] >> 16));
+            out[q] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          dst[c0 + lane + 32 * u] = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+      }
     }
-    o.x = out[0];
-    o.y = out[1];
-    o.z = out[2];
-    o.w = out[3];
-    *reinterpret_cast<uint4*>(dst + j) = o;
   }
 }
 
@@ -710,7 +734,9 @@ cudaError_t launch_prefill_scatter(const PrefillScatterArgs& a, cudaStream_t s) 
 
 cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16_t* xg, int rows, int d,
                                   cudaStream_t s) {
-  prefill_gather_kernel<<<rows, 256, 0, s>>>(x, perm, xg, d);
+  int blocks = (rows + 7) / 8;
+  if (blocks > 152 * 6) blocks = 152 * 6;
+  prefill_gather_kernel<<<blocks, 256, 0, s>>>(x, perm, xg, rows, d);
   return cudaGetLastError();
 }
 

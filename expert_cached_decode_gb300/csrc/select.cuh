@@ -100,8 +100,16 @@ __device__ __forceinline__ int sel_act_index(const SelSmem* s, int id) {
 // written by other CTAs of this kernel or of the same launch); warps take
 // tokens in turn: top-k (ties to the lower id), weights, ids ascending; then
 // warp 0 forms U.
-__device__ __forceinline__ void select_call(const float* logits, int T, int E, int K, SelSmem* s) {
+// `tl` (timeline builds only) receives %globaltimer stamps of the steps.
+__device__ __forceinline__ void select_call(const float* logits, int T, int E, int K, SelSmem* s,
+                                            unsigned long long* tl = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef MOE_TIMELINE
+#define SEL_TL(i) \
+  if (tl && threadIdx.x == 0) tl[i] = globaltimer()
+#else
+#define SEL_TL(i) ((void)0)
+#endif
   for (int i = threadIdx.x; i < kMaxE / 32; i += blockDim.x) s->mask[i] = 0;
   __syncthreads();
   for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
@@ -109,9 +117,11 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
 #pragma unroll 16
     for (int id = lane; id < E; id += 32) row[id] = ld_cg_f32(logits + (size_t)t * E + id);
     __syncwarp();
+    if (t == 0) SEL_TL(0);
     float my_v;
     int my_id;
     warp_topk(row, E, K, lane, s->topk[warp], my_v, my_id);
+    if (t == 0) SEL_TL(1);
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = lane < K ? expf(my_v - top) : 0.f;
     float sum = ex;
@@ -127,8 +137,10 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
       s->sel_w[t][rank] = ex / sum;
       atomicOr(&s->mask[my_id >> 5], 1u << (my_id & 31));
     }
+    if (t == 0) SEL_TL(2);
   }
   __syncthreads();
+  SEL_TL(3);
   const int n_words = (E + 31) / 32;
   if (warp == 0) {
     const uint32_t m = lane < n_words ? s->mask[lane] : 0u;
@@ -151,6 +163,8 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
     }
   }
   __syncthreads();
+  SEL_TL(4);
+#undef SEL_TL
 }
 
 }  // namespace moe
