@@ -77,11 +77,15 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# the sources the decode kernel is compiled from
+DECODE_SOURCES = ("decode_ffn.cu", "select.cuh", "common.cuh", "internal.h")
+
+
 def source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "expert_cached_decode_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -310,9 +314,11 @@ def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
     return float(np.median(out))
 
 
-def run_stack(cfg_id, pool_entries=0, calls=0):
+def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1):
     """48-layer stack with the 8,445-slot cache that starts empty (miss path):
-    the warm-up passes over the call stream, then the measured pass."""
+    the warm-up passes over the call stream, then the measured pass.
+    miss_mode 1: the GPU reads missing experts from the host pool itself;
+    0: the host issues the copies after reading the routing plan."""
     import time
     import torch
     from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA, expert_nbytes
@@ -329,6 +335,7 @@ def run_stack(cfg_id, pool_entries=0, calls=0):
     shared = np.stack([s.shared_packed(l) for l in range(wl.n_layers)])
     layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
                      host_pool_entries=0 if P == wl.keys else P)
+    layer.moe_set_miss_mode(miss_mode)
     layer.moe_cache_configure(wl.capacity)
     setup_s = time.time() - t0
     xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
@@ -365,6 +372,7 @@ def run_stack(cfg_id, pool_entries=0, calls=0):
     return {"workload": f"{wl.name}: 48 layers, T={wl.tokens} per call, Zipf s={wl.zipf_s} (lambda "
                         f"{BIAS_LAMBDA}), {wl.capacity} slots starting empty, {wl.warm_passes} warm-up passes "
                         f"then the measured pass of {calls} calls",
+            "miss_copies": "GPU reads the host pool" if miss_mode == 1 else "host-issued cudaMemcpyAsync",
             "host_pool_entries": P, "tokens_per_s": tokens / (ms / 1e3), "ms_measured_pass": ms,
             "token_hit_rate": dlt["token_hits"] / max(1, dlt["token_hits"] + dlt["token_misses"]),
             "distinct_expert_bytes": distinct_bytes, "miss_bytes": dlt["miss_bytes"],
@@ -556,7 +564,7 @@ def run_gpu(args):
                 line["prefill"] = {"error": str(ex)[:300]}
         if args.stack:
             try:
-                line["stack"] = [run_stack(c, args.stack_pool) for c in (3, 4)]
+                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m) for c in (3, 4) for m in (1, 0)]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:

@@ -72,6 +72,8 @@ struct moe_ctx {
   float* router_b = nullptr;     // [L][E]
   uint8_t* shared = nullptr;     // [L] device layout
   const uint8_t* host_pool = nullptr;
+  const uint8_t* host_pool_dev = nullptr;   // device address of the registered pool (NULL: none)
+  bool pull = false;                        // misses pulled by the GPU
   int64_t P = 0;
   bool registered = false;
   // cache
@@ -274,6 +276,14 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
     } else if (at.type == cudaMemoryTypeDevice) {
       moe_layer_destroy(c);
       return fail(MOE_ERR_INVALID_ARG, "host_pool must be host memory");
+    }
+    // the GPU's address of the pool, for misses pulled by the GPU itself
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, const_cast<void*>(D.host_pool), 0) == cudaSuccess && dp) {
+      c->host_pool_dev = static_cast<const uint8_t*>(dp);
+      c->pull = true;
+    } else {
+      cudaGetLastError();
     }
   }
   // scratch
@@ -711,6 +721,46 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   // miss-capable path
   RouteArgs ra = route_args(c, layer, x, T, ROUTE_PLAN);
   CUDA_TRY(launch_route(ra, s));
+  if (c->pull) {
+    // every step on the caller's stream, the miss list read on the device
+    MissPullArgs mp{};
+    mp.plan = c->plan;
+    mp.host_pool = c->host_pool_dev;
+    mp.pool_entries = c->P;
+    mp.expert_bytes = c->B;
+    mp.staging = c->staging;
+    mp.staging_n = c->staging_n;
+    mp.layer = layer;
+    mp.E = c->E;
+    mp.err = c->err;
+    CUDA_TRY(launch_miss_pull(mp, s, c->num_sms));
+    RepackArgs rp{};
+    rp.src = c->staging;
+    rp.src_stride = c->B;
+    rp.dst_base = c->slots;
+    rp.dst_stride = c->B;
+    rp.d = c->d;
+    rp.f = c->f;
+    rp.plan = c->plan;
+    CUDA_TRY(launch_repack_misses(rp, s, c->num_sms));
+    CommitArgs ca{};
+    ca.plan = c->plan;
+    ca.counters = c->counters;
+    ca.set_words = c->set_words;
+    ca.table = c->table;
+    ca.owner = c->owner;
+    ca.stamp = c->stamp;
+    ca.clock = c->clock;
+    ca.stats = c->stats + (size_t)layer * ST_N;
+    ca.layer = layer;
+    ca.E = c->E;
+    ca.expert_bytes = c->B;
+    CUDA_TRY(launch_commit(ca, s));
+    c->qcur ^= 1;
+    CUDA_TRY(launch_decode_ffn(fa, s, false));
+    if (trace) return fill_trace(c, s, T, trace);
+    return MOE_OK;
+  }
   CUDA_TRY(cudaMemcpyAsync(c->plan_host, c->plan, sizeof(Plan), cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaEventRecord(c->ev_route, s));
   CUDA_TRY(cudaEventSynchronize(c->ev_route));
@@ -758,6 +808,20 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
     // plan_host was refreshed after the call; the miss list is that of this call
   }
   return MOE_OK;
+}
+
+extern "C" moe_status moe_set_miss_mode(moe_ctx* c, int32_t mode) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "NULL context");
+  if (mode == MOE_MISS_HOST_COPY) {
+    c->pull = false;
+    return MOE_OK;
+  }
+  if (mode == MOE_MISS_DEVICE_PULL) {
+    if (!c->host_pool_dev) return fail(MOE_ERR_UNIMPLEMENTED, "the host pool has no device address");
+    c->pull = true;
+    return MOE_OK;
+  }
+  return fail(MOE_ERR_INVALID_ARG, "unknown miss mode %d", mode);
 }
 
 static moe_status check_device_error(moe_ctx* c) {

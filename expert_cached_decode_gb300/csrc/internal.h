@@ -85,6 +85,19 @@ struct RepackArgs {
   int64_t dst_stride;
   int n_experts;
   int d, f;
+  const Plan* plan;         // if set: n_experts = plan->n_miss, dst_slot = plan->miss_slot
+};
+
+// Miss copies pulled by the GPU from the device-mapped host pool.
+struct MissPullArgs {
+  const Plan* plan;          // miss list of the layer-call
+  const uint8_t* host_pool;  // device address of the registered host pool
+  int64_t pool_entries;      // identity (layer, e) reads entry (layer*E + e) mod pool_entries
+  int64_t expert_bytes;
+  uint8_t* staging;          // [staging_n][expert_bytes]
+  int staging_n;
+  int layer, E;
+  uint32_t* err;
 };
 
 struct FfnArgs {
@@ -191,6 +204,8 @@ moe_status set_last_error(moe_status st, const char* fmt, ...);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 cudaError_t launch_repack(const RepackArgs& a, cudaStream_t s);
+cudaError_t launch_miss_pull(const MissPullArgs& a, cudaStream_t s, int num_sms);
+cudaError_t launch_repack_misses(const RepackArgs& a, cudaStream_t s, int num_sms);
 }  // namespace moe
 
 #include <cuda.h>

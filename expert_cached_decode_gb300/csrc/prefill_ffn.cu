@@ -202,12 +202,13 @@ namespace pg {
 constexpr int BM = 128, BN = kPrefillBN, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB weight tile
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB token tile
-constexpr int NPROD = 8;               // dequant warps
+constexpr int NGROUP = 2;              // producer groups: group q takes the k blocks kb % NGROUP == q
+constexpr int NPROD = 4 * NGROUP;      // dequant warps (4 per group, 2 blocks of each k block each)
 constexpr int PSTAGES = 4;             // packed-weight staging depth per producer
 constexpr int PCHUNK = 2 * kBlockBytes;   // packed bytes per producer and k block
 constexpr int EPI0 = 2 + NPROD;        // first epilogue warp
 constexpr int NEPI = 8;                // epilogue warps: 4 TMEM quarters x 2 column halves
-constexpr int THREADS = (EPI0 + NEPI) * 32;   // 0 TMA, 1 MMA, 2-9 producers, 10-17 epilogue
+constexpr int THREADS = (EPI0 + NEPI) * 32;   // 0 TMA, 1 MMA, then producers, then epilogue
 constexpr int GU_ROWS = BM / 2;        // f rows per gate/up tile (Wg rows, then the same Wu rows)
 constexpr int MAX_CTA_TILES = 128;     // tile descriptors of a CTA kept in shared memory
 constexpr int CLUSTER = 2;             // CTAs sharing each token tile (TMA multicast)
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_a[i], NPROD / 2);
+      mbar_init(&full_a[i], 4);   // the 4 producers of the k block's group
       mbar_init(&full_b[i], 1);
       mbar_init(&empty[i], CLUSTER);   // the MMAs of both CTAs of the cluster
     }
@@ -450,9 +451,9 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     }
   } else if (warp < EPI0) {
     // ---- weight producers: 3-bit blocks -> fp16 swizzled tiles -------------
-    // producer p takes the k blocks of parity p/4; per k block the 4
-    // producers of that parity expand 2 blocks each (the 8 blocks of the
-    // 128 x 64 tile)
+    // producer p takes the k blocks kb with kb % NGROUP == p/4; per k block
+    // the 4 producers of that group expand 2 blocks each (the 8 blocks of
+    // the 128 x 64 tile)
     const int p = warp - 2, par = p >> 2;
     uint8_t* my_stage = pstage + p * PSTAGES * PCHUNK;
     uint64_t* my_bar = pbar + p * PSTAGES;
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         bulk_g2s(my_stage + ps * PCHUNK, psrc(tl, p, kb_issue), PCHUNK, &my_bar[ps]);
       }
       ++n_issued;
-      kb_issue += 2;
+      kb_issue += NGROUP;
       if (kb_issue >= n_kb) {
         kb_issue = par;
         ti_issue += gridDim.x;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     PF_VAR(pf_p8);
     uint32_t j = 0, lt = 0;
     for (int ti = blockIdx.x; ti < n_tiles; ti += gridDim.x, ++lt) {
-      for (int kb = par; kb < n_kb; kb += 2, ++j) {
+      for (int kb = par; kb < n_kb; kb += NGROUP, ++j) {
         __syncwarp();
         issue_next();   // refills the slot consumed PSTAGES-1 items ago
         const int ps = j % PSTAGES;

@@ -96,6 +96,11 @@ class MoELayer:
                 "n_distinct": int(tr.n_distinct), "token_hits": int(tr.token_hits),
                 "token_misses": int(tr.token_misses)}
 
+    def moe_set_miss_mode(self, mode):
+        """mode: _abi.MOE_MISS_DEVICE_PULL (GPU reads the host pool itself) or
+        _abi.MOE_MISS_HOST_COPY (host issues the miss copies)."""
+        check(self._lib.moe_set_miss_mode(self.ctx, int(mode)), "moe_set_miss_mode")
+
     def moe_sync(self):
         check(self._lib.moe_sync(self.ctx), "moe_sync")
 

@@ -145,6 +145,21 @@ moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32
 moe_status moe_forward(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T,
                        float* y, void* stream, moe_trace* trace);
 
+/* How a layer-call with misses fetches the missing experts (the cache of
+ * page "单卡5090跑125B 大模型", §2.1 and §7.2: misses come from pinned host RAM).
+ *   MOE_MISS_DEVICE_PULL (default when the host pool is device-accessible):
+ *     the GPU reads the registered host pool itself (NVLink-C2C or PCIe),
+ *     kernels take the miss list from the routing plan in device memory, and
+ *     moe_forward does not wait for the GPU (nothing between routing and the
+ *     copies goes through the host);
+ *   MOE_MISS_HOST_COPY: the host waits for the routing plan and issues one
+ *     cudaMemcpyAsync per miss on a side stream.
+ * Both give the same slots, counters and outputs.  Returns
+ * MOE_ERR_UNIMPLEMENTED for device pull when the pool has no device address,
+ * MOE_ERR_INVALID_ARG for an unknown mode. */
+typedef enum { MOE_MISS_HOST_COPY = 0, MOE_MISS_DEVICE_PULL = 1 } moe_miss_mode;
+moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
+
 /* Wait for all work of the context and report a deferred device error
  * (MOE_ERR_TIMEOUT if a bounded device wait gave up). */
 moe_status moe_sync(moe_ctx* ctx);

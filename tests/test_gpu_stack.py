@@ -1,5 +1,7 @@
 """GPU parity of the miss path: 48-layer stacks with an 8,445-slot cache
-that starts empty, misses copied from pinned host memory on a side stream.
+that starts empty, misses fetched from pinned host memory (by default read by
+the GPU itself from the registered pool; the small stack also runs the
+host-issued copies on a side stream).
 
 Every layer-call of every pass is compared with the oracle bit-exactly:
 routing indices, the slot of every pick, the miss list with its victim
@@ -17,6 +19,7 @@ import torch
 from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA
 from oracle.stack import StackOracle
 
+from expert_cached_decode_gb300._abi import MOE_MISS_DEVICE_PULL, MOE_MISS_HOST_COPY
 from gpu_helpers import make_layer, to_device_bf16, ExpertMemo, oracle_y, assert_close_rms, W_TOL
 from stack_prep import prepare_stack
 
@@ -27,7 +30,7 @@ pytestmark = pytest.mark.gpu
 POOL_ENTRIES = 2048
 
 
-def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None):
+def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None, miss_mode=None):
     wl = WORKLOADS[cfg_id]
     if overrides:
         wl = dataclasses.replace(wl, **overrides)
@@ -41,6 +44,8 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
             so.routes[(b, l)] = (idx[l, b].astype(np.int64), w[l, b])
             so.x_bits[(b, l)] = xs[l, b]
     layer = make_layer(s, pool_entries=pool_entries)
+    if miss_mode is not None:
+        layer.moe_set_miss_mode(miss_mode)
     layer.moe_cache_configure(wl.capacity)            # empty cache
     xdev = to_device_bf16(xs)
     y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
@@ -78,10 +83,12 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
     return meas["hits"] / meas["picks"], tot, st
 
 
-def test_small_stack_with_evictions():
+@pytest.mark.parametrize("miss_mode", [MOE_MISS_DEVICE_PULL, MOE_MISS_HOST_COPY])
+def test_small_stack_with_evictions(miss_mode):
+    # both ways of fetching misses: the GPU reading the host pool, or host-issued copies
     over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=5, capacity=40, calls=60)
     rate, tot, _ = run_stack(3, passes=2, pool_entries=96, overrides=over,
-                             ffn_sample={(0, 0), (17, 3), (59, 5)})
+                             ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode)
     assert tot["evictions"] > 0 and tot["token_misses"] > 0
     assert 0.0 < rate < 1.0
 
