@@ -293,7 +293,7 @@ __device__ __forceinline__ uint64_t topk_key(const float* row, int id) {
 // reductions: largest key, then smallest id).  Lane r < K receives the r-th
 // largest value and its id.  Loops stay short: this runs once per call, so
 // code size matters more than instruction count.
-__device__ __forceinline__ void warp_topk(const float* row, int E, int K, int lane, uint64_t* scratch, float& out_v,
+static __device__ __noinline__ void warp_topk(const float* row, int E, int K, int lane, uint64_t* scratch, float& out_v,
                                           int& out_id) {
   uint64_t m = 0;
 #pragma unroll 4
@@ -370,6 +370,70 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int K, int la
     }
     if (hk == mx && hid == win) taken |= 1u << li;
   }
+}
+
+// The same selection for E <= 32 * VPL with each lane's entries held in
+// registers: one shared-memory read per entry, then every pass runs on
+// registers (for the E <= 512 rows of the decode path, where the loop form
+// above is latency-bound).
+template <int VPL>
+__device__ __forceinline__ void warp_topk_reg(const float* row, int E, int K, int lane, uint64_t* scratch,
+                                              float& out_v, int& out_id) {
+  uint64_t s[VPL];
+  uint64_t m = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int id = lane + 32 * i;
+    s[i] = id < E ? topk_key(row, id) : 0ull;
+    m = s[i] > m ? s[i] : m;
+  }
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) above += shfl_u64(m, j) > m ? 1 : 0;
+  const uint32_t holder = __ballot_sync(0xffffffffu, above == K - 1 && m != 0);
+  const uint64_t tau = shfl_u64(m, __ffs(holder) - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) cnt += s[i] >= tau ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const int n_c = __shfl_sync(0xffffffffu, incl, 31);
+  if (n_c > kTopkMaxCand) {   // values crowded into few lanes: the general route
+    warp_topk(row, E, K, lane, scratch, out_v, out_id);
+    return;
+  }
+  out_v = -INFINITY;
+  out_id = 0x7fffffff;
+  int pos = incl - cnt;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (s[i] >= tau) scratch[pos++] = s[i];
+  __syncwarp();
+  if (lane < n_c) {
+    const uint64_t me = scratch[lane];
+    int r = 0;
+#pragma unroll 8
+    for (int j2 = 0; j2 < n_c; ++j2) r += scratch[j2] > me ? 1 : 0;
+    if (r < K) scratch[kTopkMaxCand + r] = me;
+  }
+  if (lane + 32 < n_c) {
+    const uint64_t me = scratch[lane + 32];
+    int r = 0;
+#pragma unroll 8
+    for (int j2 = 0; j2 < n_c; ++j2) r += scratch[j2] > me ? 1 : 0;
+    if (r < K) scratch[kTopkMaxCand + r] = me;
+  }
+  __syncwarp();
+  if (lane < K) {
+    const uint64_t w = scratch[kTopkMaxCand + lane];
+    out_v = key_float((uint32_t)(w >> 32));
+    out_id = (int)~(uint32_t)w;
+  }
+  __syncwarp();   // scratch is reused by the warp's next selection
 }
 
 }  // namespace moe

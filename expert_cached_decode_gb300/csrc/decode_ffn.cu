@@ -53,7 +53,7 @@ constexpr int kXPerThread = 4;                // 16-byte x chunks per thread loa
 
 template <int NT>
 struct FfnCfg {
-  static constexpr int kStages = NT == 1 ? 20 : 11;
+  static constexpr int kStages = NT == 1 ? 20 : 10;
 };
 
 // row blocks per down tile: the smallest R with R * (f/32) a multiple of 16
@@ -71,10 +71,11 @@ __host__ __device__ __forceinline__ int h_row_bytes(int f) { return (f + 8) * 2;
 __host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
 
 // floats per lane of one warp's partials: gate/up 16 per token tile, down 8
-// per row block and token tile; +1 keeps the lanes on distinct banks
+// per row block and token tile; +4 keeps 16-byte vectors aligned and the 8
+// lanes of each 128-byte access on distinct banks
 __host__ __device__ __forceinline__ int red_per_lane(int f, int nt) {
   const int rt8 = down_rows_per_tile(f) * 8;
-  return (rt8 > 16 ? rt8 : 16) * nt + 1;
+  return (rt8 > 16 ? rt8 : 16) * nt + 4;
 }
 
 template <int NT>
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       xv[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
     }
   }
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 21);
   // now the stores
   if (FUSED) {
 #pragma unroll
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
   }
   __syncthreads();
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 22);
   // x fragments (B operand of the gate/up products), fp16, zero past T.
   // Word (nt, kstep, lane, reg), in that order, holds token nt*8 + lane/4,
   // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one.
@@ -519,18 +522,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       }
       if (ti < n_gt) {
         const int tg = g0 + ti, ai = tg / RG, rb = tg % RG;
-        // lane l adds fragment element e of lane l over the 8 warps
+        // lane l adds its fragment elements over the 8 warps in order
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+          float gs[8], us[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) gs[e] = us[e] = 0.f;
+#pragma unroll
+          for (int w = 0; w < kCW; ++w) {
+            const float4* pw = reinterpret_cast<const float4*>(red + ((size_t)w * 32 + lane) * RPL + nt * 16);
+            const float4 g0 = pw[0], g1 = pw[1], u0 = pw[2], u1 = pw[3];
+            gs[0] += g0.x; gs[1] += g0.y; gs[2] += g0.z; gs[3] += g0.w;
+            gs[4] += g1.x; gs[5] += g1.y; gs[6] += g1.z; gs[7] += g1.w;
+            us[0] += u0.x; us[1] += u0.y; us[2] += u0.z; us[3] += u0.w;
+            us[4] += u1.x; us[5] += u1.y; us[6] += u1.z; us[7] += u1.w;
+          }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            float g = 0.f, u = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) {
-              const float* pw = red + ((size_t)w * 32 + lane) * RPL + nt * 16;
-              g += pw[e];
-              u += pw[8 + e];
-            }
+            const float g = gs[e], u = us[e];
             const int mt = e >> 2, i = e & 3;
             const int tok = nt * 8 + 2 * cq + (i & 1);
             if (tok < T) {
@@ -551,11 +560,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         for (int r = 0; r < RT; ++r) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
+            float os[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) os[e] = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) {
+              const float4* pw =
+                  reinterpret_cast<const float4*>(red + ((size_t)w * 32 + lane) * RPL + (r * NT + nt) * 8);
+              const float4 o0 = pw[0], o1 = pw[1];
+              os[0] += o0.x; os[1] += o0.y; os[2] += o0.z; os[3] += o0.w;
+              os[4] += o1.x; os[5] += o1.y; os[6] += o1.z; os[7] += o1.w;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              float o = 0.f;
-#pragma unroll
-              for (int w = 0; w < kCW; ++w) o += red[((size_t)w * 32 + lane) * RPL + (r * NT + nt) * 8 + e];
+              const float o = os[e];
               const int mt = e >> 2, i = e & 3;
               const int tok = nt * 8 + 2 * cq + (i & 1);
               if (tok < T) {
@@ -622,38 +640,71 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         float ag[NT][2][4], au[NT][2][4];
         zero_acc<NT>(ag);
         zero_acc<NT>(au);
-        for (int st = 0; st < SGU; ++st, ++it) {
-          const int s = it % NS;
-          if (ok && !mbar_wait(&full[s], (it / NS) & 1)) {
+        // two stages at a time where the tile has them: four independent
+        // block products per warp are in flight together; the sums are
+        // still added in stage order
+        for (int st = 0; st < SGU;) {
+          const int ns = st + 1 < SGU ? 2 : 1;
+          const int s0 = it % NS, s1 = (it + 1) % NS;
+          if (ok && !mbar_wait(&full[s0], (it / NS) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            ok = false;
+          }
+          if (ok && ns == 2 && !mbar_wait(&full[s1], ((it + 1) / NS) & 1)) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             ok = false;
           }
           if (ok) {
-            const uint8_t* sp = ring + (size_t)s * kStageBytes;
-            const int gi = st * (kStageBlocks / 2) + warp;     // input group of this warp
-            uint2 bx[NT][2];
+            const uint8_t* sp0 = ring + (size_t)s0 * kStageBytes + 2 * warp * kBlockBytes;
+            const int gi0 = st * (kStageBlocks / 2) + warp;     // input group of this warp
+            uint2 bx0[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              bx[nt][0] = xfrag[((size_t)nt * nks + gi * 2 + 0) * 32 + lane];
-              bx[nt][1] = xfrag[((size_t)nt * nks + gi * 2 + 1) * 32 + lane];
+              bx0[nt][0] = xfrag[((size_t)nt * nks + gi0 * 2 + 0) * 32 + lane];
+              bx0[nt][1] = xfrag[((size_t)nt * nks + gi0 * 2 + 1) * 32 + lane];
             }
-            block_mma<NT>(sp + (2 * warp + 0) * kBlockBytes, lane, bx, ag);
-            block_mma<NT>(sp + (2 * warp + 1) * kBlockBytes, lane, bx, au);
+            if (ns == 2) {
+              const uint8_t* sp1 = ring + (size_t)s1 * kStageBytes + 2 * warp * kBlockBytes;
+              const int gi1 = gi0 + kStageBlocks / 2;
+              uint2 bx1[NT][2];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                bx1[nt][0] = xfrag[((size_t)nt * nks + gi1 * 2 + 0) * 32 + lane];
+                bx1[nt][1] = xfrag[((size_t)nt * nks + gi1 * 2 + 1) * 32 + lane];
+              }
+              float Dg0[NT][2][4], Du0[NT][2][4], Dg1[NT][2][4], Du1[NT][2][4];
+              float sg0[4], su0[4], sg1[4], su1[4];
+              block_products<NT>(sp0, lane, bx0, Dg0, sg0);
+              block_products<NT>(sp0 + kBlockBytes, lane, bx0, Du0, su0);
+              block_products<NT>(sp1, lane, bx1, Dg1, sg1);
+              block_products<NT>(sp1 + kBlockBytes, lane, bx1, Du1, su1);
+              block_accum<NT>(Dg0, sg0, ag);
+              block_accum<NT>(Du0, su0, au);
+              block_accum<NT>(Dg1, sg1, ag);
+              block_accum<NT>(Du1, su1, au);
+            } else {
+              block_mma<NT>(sp0, lane, bx0, ag);
+              block_mma<NT>(sp0 + kBlockBytes, lane, bx0, au);
+            }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
+          if (lane == 0) {
+            mbar_arrive(&empty[s0]);
+            if (ns == 2) mbar_arrive(&empty[s1]);
+          }
+          st += ns;
+          it += ns;
         }
         wait_buf_free(ti);
         if (ok) {
+          float4* m4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                mine[nt * 16 + mt * 4 + i] = ag[nt][mt][i];
-                mine[nt * 16 + 8 + mt * 4 + i] = au[nt][mt][i];
-              }
+            for (int mt = 0; mt < 2; ++mt) {
+              m4[nt * 4 + mt] = make_float4(ag[nt][mt][0], ag[nt][mt][1], ag[nt][mt][2], ag[nt][mt][3]);
+              m4[nt * 4 + 2 + mt] = make_float4(au[nt][mt][0], au[nt][mt][1], au[nt][mt][2], au[nt][mt][3]);
+            }
         }
         signal_buf_full();
       } else {
@@ -679,47 +730,80 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         float acc[kMaxRT][NT][2][4];
 #pragma unroll
         for (int r = 0; r < kMaxRT; ++r) zero_acc<NT>(acc[r]);
-        for (int st = 0; st < SDN; ++st, ++it) {
-          const int s = it % NS;
-          if (ok && !mbar_wait(&full[s], (it / NS) & 1)) {
+        // two stages at a time, as for gate/up: this warp's blocks b, b + 8
+        // of each stage; products first (independent, so they overlap), then
+        // each is added to its row block's sums in block order
+        for (int st = 0; st < SDN;) {
+          const int ns = st + 1 < SDN ? 2 : 1;
+          const int s0 = it % NS, s1 = (it + 1) % NS;
+          if (ok && !mbar_wait(&full[s0], (it / NS) & 1)) {
+            set_error(a.err, DEV_TIMEOUT_BARRIER);
+            ok = false;
+          }
+          if (ok && ns == 2 && !mbar_wait(&full[s1], ((it + 1) / NS) & 1)) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             ok = false;
           }
           if (ok) {
-            // this warp's two blocks of the stage: products first (independent,
-            // so they overlap), then each is added to its row block's sums
-            const uint8_t* sp = ring + (size_t)s * kStageBytes;
+            const uint8_t* sp0 = ring + (size_t)s0 * kStageBytes;
             const int b0 = st * kStageBlocks + warp, b1 = b0 + kCW;   // blocks of the tile
             const int rl0 = b0 / DG, rl1 = b1 / DG;
             uint2 bx0[NT][2], bx1[NT][2];
             h_frags<NT>(hb, hrow, T, b0 - rl0 * DG, lane, bx0);
             h_frags<NT>(hb, hrow, T, b1 - rl1 * DG, lane, bx1);
-            float D0[NT][2][4], D1[NT][2][4], s0[4], s1[4];
-            block_products<NT>(sp + warp * kBlockBytes, lane, bx0, D0, s0);
-            block_products<NT>(sp + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1);
+            float D0[NT][2][4], D1[NT][2][4], s0v[4], s1v[4];
+            if (ns == 2) {
+              const uint8_t* sp1 = ring + (size_t)s1 * kStageBytes;
+              const int b2 = b0 + kStageBlocks, b3 = b1 + kStageBlocks;
+              const int rl2 = b2 / DG, rl3 = b3 / DG;
+              uint2 bx2[NT][2], bx3[NT][2];
+              h_frags<NT>(hb, hrow, T, b2 - rl2 * DG, lane, bx2);
+              h_frags<NT>(hb, hrow, T, b3 - rl3 * DG, lane, bx3);
+              float D2[NT][2][4], D3[NT][2][4], s2v[4], s3v[4];
+              block_products<NT>(sp0 + warp * kBlockBytes, lane, bx0, D0, s0v);
+              block_products<NT>(sp0 + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1v);
+              block_products<NT>(sp1 + warp * kBlockBytes, lane, bx2, D2, s2v);
+              block_products<NT>(sp1 + (warp + kCW) * kBlockBytes, lane, bx3, D3, s3v);
 #pragma unroll
-            for (int r = 0; r < kMaxRT; ++r) {
-              if (r == rl0) block_accum<NT>(D0, s0, acc[r]);
-              if (r == rl1) block_accum<NT>(D1, s1, acc[r]);
+              for (int r = 0; r < kMaxRT; ++r) {
+                if (r == rl0) block_accum<NT>(D0, s0v, acc[r]);
+                if (r == rl1) block_accum<NT>(D1, s1v, acc[r]);
+                if (r == rl2) block_accum<NT>(D2, s2v, acc[r]);
+                if (r == rl3) block_accum<NT>(D3, s3v, acc[r]);
+              }
+            } else {
+              block_products<NT>(sp0 + warp * kBlockBytes, lane, bx0, D0, s0v);
+              block_products<NT>(sp0 + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1v);
+#pragma unroll
+              for (int r = 0; r < kMaxRT; ++r) {
+                if (r == rl0) block_accum<NT>(D0, s0v, acc[r]);
+                if (r == rl1) block_accum<NT>(D1, s1v, acc[r]);
+              }
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
+          if (lane == 0) {
+            mbar_arrive(&empty[s0]);
+            if (ns == 2) mbar_arrive(&empty[s1]);
+          }
+          st += ns;
+          it += ns;
         }
         // this warp is done reading expert ai's h slot after its last tile of ai
         const bool last_of_expert = (ti + 1 == n_gt + n_dt) || ((d0 + ti + 1 - n_gt) / DPE != ai);
         if (last_of_expert && lane == 0) mbar_arrive(&hempty[hs]);
         wait_buf_free(ti);
         if (ok) {
+          float4* m4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
           for (int r = 0; r < kMaxRT; ++r)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (r < RT) mine[(r * NT + nt) * 8 + mt * 4 + i] = acc[r][nt][mt][i];
+                if (r < RT)
+                  m4[(r * NT + nt) * 2 + mt] =
+                      make_float4(acc[r][nt][mt][0], acc[r][nt][mt][1], acc[r][nt][mt][2], acc[r][nt][mt][3]);
         }
         signal_buf_full();
       }

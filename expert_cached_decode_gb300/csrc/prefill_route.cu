@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(PrefillTopkArgs a) {
   __syncwarp();
   float my_v;
   int my_id;
-  warp_topk(row, E, K, lane, scratch[threadIdx.x >> 5], my_v, my_id);
+  if (E <= 512) warp_topk_reg<16>(row, E, K, lane, scratch[threadIdx.x >> 5], my_v, my_id);
+  else warp_topk(row, E, K, lane, scratch[threadIdx.x >> 5], my_v, my_id);
   const float top = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = lane < K ? expf(my_v - top) : 0.f;
   float sum = ex;

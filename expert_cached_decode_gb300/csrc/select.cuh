@@ -120,7 +120,8 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
     if (t == 0) SEL_TL(0);
     float my_v;
     int my_id;
-    warp_topk(row, E, K, lane, s->topk[warp], my_v, my_id);
+    if (E <= 512) warp_topk_reg<16>(row, E, K, lane, s->topk[warp], my_v, my_id);
+    else warp_topk(row, E, K, lane, s->topk[warp], my_v, my_id);
     if (t == 0) SEL_TL(1);
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     const float ex = lane < K ? expf(my_v - top) : 0.f;
