@@ -293,7 +293,7 @@ __device__ __forceinline__ uint64_t topk_key(const float* row, int id) {
 // reductions: largest key, then smallest id).  Lane r < K receives the r-th
 // largest value and its id.  Loops stay short: this runs once per call, so
 // code size matters more than instruction count.
-static __device__ __noinline__ void warp_topk(const float* row, int E, int K, int lane, uint64_t* scratch, float& out_v,
+__device__ __forceinline__ void warp_topk(const float* row, int E, int K, int lane, uint64_t* scratch, float& out_v,
                                           int& out_id) {
   uint64_t m = 0;
 #pragma unroll 4

@@ -39,7 +39,7 @@
 namespace moe {
 
 #ifdef MOE_TIMELINE
-__device__ unsigned long long g_ffn_timeline[512][24];
+__device__ unsigned long long g_ffn_timeline[512][32];
 #endif
 
 constexpr int kCW = 8;                        // consumer warps
@@ -304,17 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 22);
   // x fragments (B operand of the gate/up products), fp16, zero past T.
   // Word (nt, kstep, lane, reg), in that order, holds token nt*8 + lane/4,
-  // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one.
+  // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one; each warp writes
+  // whole k-steps (one 8-byte store per lane).
   {
-    uint32_t* xf = reinterpret_cast<uint32_t*>(xfrag);
     const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw);
-    for (int o = tid; o < NT * nks * 64; o += kThreads) {
-      const int reg = o & 1, lq = (o >> 1) & 31, ks_nt = o >> 6;
-      const int nt = ks_nt / nks, kstep = ks_nt - nt * nks;
-      const int n = nt * 8 + (lq >> 2), k = kstep * 16 + 2 * (lq & 3) + 8 * reg;
-      xf[o] = n < T ? pack_half2_from_bf16(xr[((size_t)n * xs + k) >> 1]) : 0u;
+#pragma unroll 1
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = nt * 8 + (lane >> 2);
+      const uint32_t* xrow = xr + (((size_t)(n < T ? n : 0) * xs + 2 * (lane & 3)) >> 1);
+#pragma unroll 4
+      for (int kstep = warp; kstep < nks; kstep += kThreads / 32) {
+        uint2 v = make_uint2(0u, 0u);
+        if (n < T) v = make_uint2(pack_half2_from_bf16(xrow[kstep * 8]), pack_half2_from_bf16(xrow[kstep * 8 + 4]));
+        xfrag[((size_t)nt * nks + kstep) * 32 + lane] = v;
+      }
     }
   }
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 26);
   __syncthreads();
   // this call's counter set; the fused kernel's CTA 0 zeroes the other one
   // (the previous call's, complete by now) for the next call
@@ -370,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       s_act_slot[i] = slot;
     }
     if (tid == 0) s_nexp = n_act + 1;
+    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 27);
     __syncthreads();
     if (cta == 0) {
       // the plan of the call (read back for traces), LRU stamps, counters
@@ -439,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     if (lane == 0) {
       // the ring held generic-proxy scratch; order it before the bulk copies
       fence_proxy_async_smem();
+      MOE_TL(g_ffn_timeline, cta, 25);
       uint32_t it = 0;
       bool ok = true;
       for (int ti = 0; ti < n_gt + n_dt && ok; ++ti) {
@@ -601,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         good = 0;
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      if (lane == 0 && rb == cta) MOE_TL(g_ffn_timeline, cta, 23);
       __syncwarp();   // the other lanes read after lane 0's acquire
       const int row = rb * 32 + lane;
 #pragma unroll 1
@@ -613,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
 #pragma unroll
         for (int k2 = 0; k2 < kMaxTopK; ++k2)
           if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
+        if (lane == 0 && rb == cta && t == 0) MOE_TL(g_ffn_timeline, cta, 24);
         a.y[(size_t)t * d + row] = yv;
       }
     }
@@ -640,60 +650,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         float ag[NT][2][4], au[NT][2][4];
         zero_acc<NT>(ag);
         zero_acc<NT>(au);
-        // two stages at a time where the tile has them: four independent
-        // block products per warp are in flight together; the sums are
-        // still added in stage order
-        for (int st = 0; st < SGU;) {
-          const int ns = st + 1 < SGU ? 2 : 1;
-          const int s0 = it % NS, s1 = (it + 1) % NS;
-          if (ok && !mbar_wait(&full[s0], (it / NS) & 1)) {
-            set_error(a.err, DEV_TIMEOUT_BARRIER);
-            ok = false;
-          }
-          if (ok && ns == 2 && !mbar_wait(&full[s1], ((it + 1) / NS) & 1)) {
+        for (int st = 0; st < SGU; ++st, ++it) {
+          const int s = it % NS;
+          if (ok && !mbar_wait(&full[s], (it / NS) & 1)) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             ok = false;
           }
           if (ok) {
-            const uint8_t* sp0 = ring + (size_t)s0 * kStageBytes + 2 * warp * kBlockBytes;
-            const int gi0 = st * (kStageBlocks / 2) + warp;     // input group of this warp
-            uint2 bx0[NT][2];
+            const uint8_t* sp = ring + (size_t)s * kStageBytes;
+            const int gi = st * (kStageBlocks / 2) + warp;     // input group of this warp
+            uint2 bx[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              bx0[nt][0] = xfrag[((size_t)nt * nks + gi0 * 2 + 0) * 32 + lane];
-              bx0[nt][1] = xfrag[((size_t)nt * nks + gi0 * 2 + 1) * 32 + lane];
+              bx[nt][0] = xfrag[((size_t)nt * nks + gi * 2 + 0) * 32 + lane];
+              bx[nt][1] = xfrag[((size_t)nt * nks + gi * 2 + 1) * 32 + lane];
             }
-            if (ns == 2) {
-              const uint8_t* sp1 = ring + (size_t)s1 * kStageBytes + 2 * warp * kBlockBytes;
-              const int gi1 = gi0 + kStageBlocks / 2;
-              uint2 bx1[NT][2];
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                bx1[nt][0] = xfrag[((size_t)nt * nks + gi1 * 2 + 0) * 32 + lane];
-                bx1[nt][1] = xfrag[((size_t)nt * nks + gi1 * 2 + 1) * 32 + lane];
-              }
-              float Dg0[NT][2][4], Du0[NT][2][4], Dg1[NT][2][4], Du1[NT][2][4];
-              float sg0[4], su0[4], sg1[4], su1[4];
-              block_products<NT>(sp0, lane, bx0, Dg0, sg0);
-              block_products<NT>(sp0 + kBlockBytes, lane, bx0, Du0, su0);
-              block_products<NT>(sp1, lane, bx1, Dg1, sg1);
-              block_products<NT>(sp1 + kBlockBytes, lane, bx1, Du1, su1);
-              block_accum<NT>(Dg0, sg0, ag);
-              block_accum<NT>(Du0, su0, au);
-              block_accum<NT>(Dg1, sg1, ag);
-              block_accum<NT>(Du1, su1, au);
-            } else {
-              block_mma<NT>(sp0, lane, bx0, ag);
-              block_mma<NT>(sp0 + kBlockBytes, lane, bx0, au);
-            }
+            block_mma<NT>(sp + (2 * warp + 0) * kBlockBytes, lane, bx, ag);
+            block_mma<NT>(sp + (2 * warp + 1) * kBlockBytes, lane, bx, au);
           }
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&empty[s0]);
-            if (ns == 2) mbar_arrive(&empty[s1]);
-          }
-          st += ns;
-          it += ns;
+          if (lane == 0) mbar_arrive(&empty[s]);
         }
         wait_buf_free(ti);
         if (ok) {
@@ -730,64 +706,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         float acc[kMaxRT][NT][2][4];
 #pragma unroll
         for (int r = 0; r < kMaxRT; ++r) zero_acc<NT>(acc[r]);
-        // two stages at a time, as for gate/up: this warp's blocks b, b + 8
-        // of each stage; products first (independent, so they overlap), then
-        // each is added to its row block's sums in block order
-        for (int st = 0; st < SDN;) {
-          const int ns = st + 1 < SDN ? 2 : 1;
-          const int s0 = it % NS, s1 = (it + 1) % NS;
-          if (ok && !mbar_wait(&full[s0], (it / NS) & 1)) {
-            set_error(a.err, DEV_TIMEOUT_BARRIER);
-            ok = false;
-          }
-          if (ok && ns == 2 && !mbar_wait(&full[s1], ((it + 1) / NS) & 1)) {
+        for (int st = 0; st < SDN; ++st, ++it) {
+          const int s = it % NS;
+          if (ok && !mbar_wait(&full[s], (it / NS) & 1)) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             ok = false;
           }
           if (ok) {
-            const uint8_t* sp0 = ring + (size_t)s0 * kStageBytes;
+            // this warp's two blocks of the stage: products first (independent,
+            // so they overlap), then each is added to its row block's sums
+            const uint8_t* sp = ring + (size_t)s * kStageBytes;
             const int b0 = st * kStageBlocks + warp, b1 = b0 + kCW;   // blocks of the tile
             const int rl0 = b0 / DG, rl1 = b1 / DG;
             uint2 bx0[NT][2], bx1[NT][2];
             h_frags<NT>(hb, hrow, T, b0 - rl0 * DG, lane, bx0);
             h_frags<NT>(hb, hrow, T, b1 - rl1 * DG, lane, bx1);
-            float D0[NT][2][4], D1[NT][2][4], s0v[4], s1v[4];
-            if (ns == 2) {
-              const uint8_t* sp1 = ring + (size_t)s1 * kStageBytes;
-              const int b2 = b0 + kStageBlocks, b3 = b1 + kStageBlocks;
-              const int rl2 = b2 / DG, rl3 = b3 / DG;
-              uint2 bx2[NT][2], bx3[NT][2];
-              h_frags<NT>(hb, hrow, T, b2 - rl2 * DG, lane, bx2);
-              h_frags<NT>(hb, hrow, T, b3 - rl3 * DG, lane, bx3);
-              float D2[NT][2][4], D3[NT][2][4], s2v[4], s3v[4];
-              block_products<NT>(sp0 + warp * kBlockBytes, lane, bx0, D0, s0v);
-              block_products<NT>(sp0 + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1v);
-              block_products<NT>(sp1 + warp * kBlockBytes, lane, bx2, D2, s2v);
-              block_products<NT>(sp1 + (warp + kCW) * kBlockBytes, lane, bx3, D3, s3v);
+            float D0[NT][2][4], D1[NT][2][4], s0[4], s1[4];
+            block_products<NT>(sp + warp * kBlockBytes, lane, bx0, D0, s0);
+            block_products<NT>(sp + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1);
 #pragma unroll
-              for (int r = 0; r < kMaxRT; ++r) {
-                if (r == rl0) block_accum<NT>(D0, s0v, acc[r]);
-                if (r == rl1) block_accum<NT>(D1, s1v, acc[r]);
-                if (r == rl2) block_accum<NT>(D2, s2v, acc[r]);
-                if (r == rl3) block_accum<NT>(D3, s3v, acc[r]);
-              }
-            } else {
-              block_products<NT>(sp0 + warp * kBlockBytes, lane, bx0, D0, s0v);
-              block_products<NT>(sp0 + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1v);
-#pragma unroll
-              for (int r = 0; r < kMaxRT; ++r) {
-                if (r == rl0) block_accum<NT>(D0, s0v, acc[r]);
-                if (r == rl1) block_accum<NT>(D1, s1v, acc[r]);
-              }
+            for (int r = 0; r < kMaxRT; ++r) {
+              if (r == rl0) block_accum<NT>(D0, s0, acc[r]);
+              if (r == rl1) block_accum<NT>(D1, s1, acc[r]);
             }
           }
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&empty[s0]);
-            if (ns == 2) mbar_arrive(&empty[s1]);
-          }
-          st += ns;
-          it += ns;
+          if (lane == 0) mbar_arrive(&empty[s]);
         }
         // this warp is done reading expert ai's h slot after its last tile of ai
         const bool last_of_expert = (ti + 1 == n_gt + n_dt) || ((d0 + ti + 1 - n_gt) / DPE != ai);
