@@ -614,11 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
       const int row = rb * 32 + lane;
 #pragma unroll 1
       for (int t = 0; t < T; ++t) {
-        float ov[kMaxTopK];
+        // every load is issued before the first use; picks past K read the
+        // shared expert's row and carry weight 0
+        const float* prow[kMaxTopK];
 #pragma unroll
         for (int k2 = 0; k2 < kMaxTopK; ++k2)
-          ov[k2] = k2 < K ? ld_cg_f32(a.obuf + ((size_t)(1 + s_pick_act[t * K + k2]) * T + t) * d + row) : 0.f;
-        float yv = a.shared_weight * ld_cg_f32(a.obuf + (size_t)t * d + row);
+          prow[k2] = a.obuf + ((size_t)(k2 < K ? 1 + s_pick_act[t * K + k2] : 0) * T + t) * d + row;
+        const float sh = __ldcg(a.obuf + (size_t)t * d + row);
+        float ov[kMaxTopK];
+#pragma unroll
+        for (int k2 = 0; k2 < kMaxTopK; ++k2) ov[k2] = __ldcg(prow[k2]);
+        float yv = a.shared_weight * sh;
 #pragma unroll
         for (int k2 = 0; k2 < kMaxTopK; ++k2)
           if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
