@@ -262,11 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     if (FUSED && cta == 0) clk = (long long)*a.clock;
   }
   // x (bf16) staged once in shared memory, rows xs apart, in the h / partial
-  // area that is free until the first tile ends; the router and the gate/up
-  // fragments read it there
+  // area that is free until the first tile ends (the router reads it there),
+  // and as fp16 B fragments of the gate/up products, zero past T.  Fragment
+  // word (nt, kstep, lane, reg), in that order, holds token nt*8 + lane/4,
+  // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one, so the 16-byte
+  // chunk c of token n fills reg c%2 of k-step c/2 for lanes 4(n%8) + j.
   uint16_t* xraw = reinterpret_cast<uint16_t*>(hbuf);
   const int xs = x_row_elems(d);
   const int cpr = d / 8;
+  uint32_t* const xfw = reinterpret_cast<uint32_t*>(xfrag);
+  auto put_x = [&](int n, int c, uint4 v) {
+    *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) = v;
+    uint32_t* w = xfw + ((((size_t)(n >> 3) * nks + (c >> 1)) * 32 + (n & 7) * 4) << 1) + (c & 1);
+    w[0] = pack_half2_from_bf16(v.x);
+    w[2] = pack_half2_from_bf16(v.y);
+    w[4] = pack_half2_from_bf16(v.z);
+    w[6] = pack_half2_from_bf16(v.w);
+  };
   uint4 xv[kXPerThread];
 #pragma unroll
   for (int q = 0; q < kXPerThread; ++q) {
@@ -292,36 +304,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     const int i = tid + q * kThreads;
     if (i < T * cpr) {
       const int n = i / cpr, c = i - n * cpr;
-      *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) = xv[q];
+      put_x(n, c, xv[q]);
     }
   }
   for (int i = tid + kXPerThread * kThreads; i < T * cpr; i += kThreads) {   // large T*d only
     const int n = i / cpr, c = i - n * cpr;
-    *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) =
-        __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
+    put_x(n, c, __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8)));
   }
-  __syncthreads();
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 22);
-  // x fragments (B operand of the gate/up products), fp16, zero past T.
-  // Word (nt, kstep, lane, reg), in that order, holds token nt*8 + lane/4,
-  // inputs kstep*16 + 2*(lane%4) + 8*reg and the next one; each warp writes
-  // whole k-steps (one 8-byte store per lane).
+  // zero fragments of the token slots T .. NT*8-1: 32 contiguous bytes per
+  // (n-tile, k-step, token)
   {
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw);
-#pragma unroll 1
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = nt * 8 + (lane >> 2);
-      const uint32_t* xrow = xr + (((size_t)(n < T ? n : 0) * xs + 2 * (lane & 3)) >> 1);
-#pragma unroll 4
-      for (int kstep = warp; kstep < nks; kstep += kThreads / 32) {
-        uint2 v = make_uint2(0u, 0u);
-        if (n < T) v = make_uint2(pack_half2_from_bf16(xrow[kstep * 8]), pack_half2_from_bf16(xrow[kstep * 8 + 4]));
-        xfrag[((size_t)nt * nks + kstep) * 32 + lane] = v;
-      }
+    const int nz = NT * 8 - T;
+    for (int i = tid; i < nz * nks * 2; i += kThreads) {
+      const int h = i & 1, q = i >> 1, kstep = q % nks, n = T + q / nks;
+      reinterpret_cast<uint4*>(xfw + ((((size_t)(n >> 3) * nks + kstep) * 32 + (n & 7) * 4) << 1))[h] =
+          make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 26);
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 22);
   __syncthreads();
+  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 26);
   // this call's counter set; the fused kernel's CTA 0 zeroes the other one
   // (the previous call's, complete by now) for the next call
   const uint32_t call_set = FUSED ? (s_calls & 1u) : ((s_calls - 1u) & 1u);
