@@ -217,11 +217,15 @@ constexpr int B_HALF = B_BYTES / CLUSTER;   // token rows a CTA loads for both
 
 // Expand one 32x32 block (448 B at `bp`, shared memory) into 32 rows and 32
 // k columns of a 128-byte-swizzled K-major fp16 tile, as RN(q * scale).
-// `lane_base` is this lane's byte address in the tile for row offset 0 of
-// the block and chunk 0 before the swizzle (tile + row0*128 + g*128 + 4c);
-// gx = g << 4; KC = the first 16-byte chunk of the block's k columns (0 or 4).
+// The expanded registers are in mma A-fragment order, which is the order
+// stmatrix takes: register (mt, ks, rh, rl) holds, for lane (g, c), rows
+// mt*16 + 8rl + g and k pair 16ks + 8rh + 2c, so one m8n8.x4 store per
+// (mt, ks) writes four 8x8 sub-tiles; lane L gives the address of row L%8 of
+// sub-tile L/8 (rl = (L/8)%2, rh = L/16).  `lane_base` = tile + (row offset
+// of the block + 8*((L/8)%2) + L%8) * 128; sw = (L%8) << 4 (the swizzle of
+// that row); KC = the first 16-byte chunk of the block's k columns (0 or 4).
 template <int KC>
-__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint32_t lane_base, uint32_t gx) {
+__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint32_t lane_base, uint32_t sw) {
   const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
   const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
   const uint2 sc = *reinterpret_cast<const uint2*>(bp + kBlockCodeBytes + (lane >> 2) * 8);
@@ -230,21 +234,19 @@ __device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lan
                           __byte_perm(sc.y, 0, 0x3232)};
   uint32_t A[16];
   dequant_block(w0, w1, w2, A);
-  // register p = mt*8 + ks*4 + r holds rows mt*16 + g + 8*(r&1), k pair
-  // ks*16 + 2c + 8*(r>>1): 16-byte chunk KC + 2ks + (r>>1), bytes 4c
+  const uint32_t rh = (uint32_t)(lane >> 4);
 #pragma unroll
-  for (int ch = 0; ch < 4; ++ch) {
-    const uint32_t addr = lane_base + ((uint32_t)((KC + ch) << 4) ^ gx);
-    const int ks = ch >> 1, rh = ch & 1;
+  for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t v[4];
 #pragma unroll
-      for (int rl = 0; rl < 2; ++rl) {
-        const int pidx = mt * 8 + ks * 4 + rh * 2 + rl;
-        uint32_t v;
-        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(A[pidx]), "r"(s2[2 * mt + rl]));
-        asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr + (uint32_t)((mt * 2 + rl) * 1024)), "r"(v) : "memory");
-      }
+      for (int r = 0; r < 4; ++r)
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v[r]) : "r"(A[mt * 8 + ks * 4 + r]), "r"(s2[2 * mt + (r & 1)]));
+      const uint32_t addr = lane_base + (uint32_t)(mt * 2048) + ((((uint32_t)(KC + 2 * ks) + rh) << 4) ^ sw);
+      asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]),
+                   "r"(v[1]), "r"(v[2]), "r"(v[3])
+                   : "memory");
     }
   }
 }
@@ -457,13 +459,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     const int p = warp - 2, par = p >> 2;
     uint8_t* my_stage = pstage + p * PSTAGES * PCHUNK;
     uint64_t* my_bar = pbar + p * PSTAGES;
-    const int g = lane >> 2, c = lane & 3;
-    const uint32_t gx = (uint32_t)g << 4;
+    // stmatrix row addresses: lane L writes row L%8 of sub-tile L/8
+    const uint32_t gx = (uint32_t)(lane & 7) << 4;
     // tile rows of this producer's first block, and the k chunk of each block
     //   down:    rows (p%4)*32, k chunks 0 and 4 (input groups 2kb, 2kb+1);
     //   gate/up: Wg rows (p%2)*32, Wu rows 64 + (p%2)*32, k chunk 4*((p/2)%2).
     const int row0 = DOWN ? (p & 3) * 32 : (p & 1) * 32;
-    const uint32_t lane_off = (uint32_t)(row0 * 128 + g * 128 + 4 * c);
+    const uint32_t lane_off = (uint32_t)((row0 + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
     const bool hi_group = !DOWN && ((p >> 1) & 1);
     int ti_issue = blockIdx.x, kb_issue = par;
     uint32_t n_issued = 0;
