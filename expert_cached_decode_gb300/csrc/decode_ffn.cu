@@ -47,7 +47,6 @@ constexpr int kThreads = (kCW + 3) * 32;      // + producer, h-loader and finali
 constexpr int kStageBlocks = 16;
 constexpr int kStageBytes = kStageBlocks * kBlockBytes;   // 7,168
 constexpr int kHSlots = 2;
-constexpr int kMaxRT = 4;                     // row blocks per down tile, at most
 constexpr int kTabPerThread = (kMaxE + kThreads - 1) / kThreads;   // slot-table entries per thread
 constexpr int kXPerThread = 4;                // 16-byte x chunks per thread loaded up front
 
@@ -71,17 +70,14 @@ __host__ __device__ __forceinline__ int h_row_bytes(int f) { return (f + 8) * 2;
 __host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
 
 // floats per lane of one warp's partials: gate/up 16 per token tile, down 8
-// per row block and token tile; +4 keeps 16-byte vectors aligned and the 8
-// lanes of each 128-byte access on distinct banks
-__host__ __device__ __forceinline__ int red_per_lane(int f, int nt) {
-  const int rt8 = down_rows_per_tile(f) * 8;
-  return (rt8 > 16 ? rt8 : 16) * nt + 4;
-}
+// per token tile (each warp sums one row block); +4 keeps 16-byte vectors
+// aligned and the 8 lanes of each 128-byte access on distinct banks
+__host__ __device__ __forceinline__ int red_per_lane(int nt) { return 16 * nt + 4; }
 
 template <int NT>
 __host__ __device__ __forceinline__ size_t ffn_smem_bytes(int d, int f) {
   return (size_t)NT * d * 16 + (size_t)FfnCfg<NT>::kStages * kStageBytes +
-         (size_t)kHSlots * NT * 8 * h_row_bytes(f) + (size_t)kCW * 32 * red_per_lane(f, NT) * 4 +
+         (size_t)kHSlots * NT * 8 * h_row_bytes(f) + (size_t)kCW * 32 * red_per_lane(NT) * 4 +
          (2 * FfnCfg<NT>::kStages + 2 * kHSlots + 2) * 8 + 64;
 }
 
@@ -196,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   uint2* xfrag = reinterpret_cast<uint2*>(smem);
   uint8_t* ring = smem + (size_t)NT * d * 16;
   uint8_t* hbuf = ring + (size_t)NS * kStageBytes;
-  const int RPL = red_per_lane(f, NT);
+  const int RPL = red_per_lane(NT);
+  const int WPR = kCW / RT;            // consumer warps per row block of a down tile
   float* red = reinterpret_cast<float*>(hbuf + (size_t)kHSlots * NT * 8 * hrow);
   uint64_t* full = reinterpret_cast<uint64_t*>(red + (size_t)kCW * 32 * RPL);
   uint64_t* empty = full + NS;
@@ -210,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   __shared__ int s_act_slot[kMaxPicks];   // slot of each distinct routed expert
   __shared__ int s_pick_act[kMaxPicks];   // [T][k] index of each pick in the distinct list
   __shared__ float s_w[kMaxPicks];        // [T][k] routing weights
-  __shared__ int s_g0, s_g1, s_d0, s_d1, s_nexp;
+  __shared__ int s_act_expert[kMaxPicks]; // expert id of each distinct routed expert (fused routing)
+  __shared__ int s_nexp;
   __shared__ uint32_t s_calls;
   __shared__ long long s_clock;
   __shared__ volatile int s_hexp[kHSlots];
@@ -376,39 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         slot = 0;
       }
       s_act_slot[i] = slot;
+      s_act_expert[i] = sel->act[i];
     }
     if (tid == 0) s_nexp = n_act + 1;
     if (tid == 0) MOE_TL(g_ffn_timeline, cta, 27);
-    __syncthreads();
-    if (cta == 0) {
-      // the plan of the call (read back for traces), LRU stamps, counters
-      Plan* P = a.plan;
-      const long long clk = s_clock;
-      for (int i = tid; i < T * K; i += kThreads) {
-        P->idx[i] = sel->sel_id[i / K][i % K];
-        P->w[i] = s_w[i];
-        P->pick_act[i] = s_pick_act[i];
-      }
-      for (int i = tid; i < n_act; i += kThreads) {
-        P->act_expert[i] = sel->act[i];
-        P->act_slot[i] = s_act_slot[i];
-        P->act_hit[i] = 1;
-        a.stamp[s_act_slot[i]] = clk;
-      }
-      if (tid == 0) {
-        P->n_act = n_act;
-        P->n_miss = 0;
-        P->T = T;
-        P->clock = clk;
-        P->token_hits = (int64_t)T * K;
-        P->token_misses = 0;
-        a.stats[ST_CALLS] += 1;
-        a.stats[ST_TOK_HIT] += (int64_t)T * K;
-        a.stats[ST_DIST_HIT] += n_act;
-        *a.clock = clk + 1;
-        *a.counters = s_calls + 1;   // every CTA read the count before the grid barrier
-      }
-    }
+    // CTA 0 publishes the plan from its h-loader warp, after the split
   } else {
     const Plan* P = a.plan;   // the routing plan is complete and visible
     for (int i = tid; i < kMaxPicks; i += kThreads) s_act_slot[i] = P->act_slot[i];
@@ -423,18 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   // ---- this CTA's share: gate/up tiles [g0, g1), down tiles [d0, d1) ------
   // Each phase is split evenly by tile count: every down tile waits for the
   // gate/up phase, so balancing the phases separately ends both sooner than
-  // balancing a CTA's total bytes.
-  if (tid == 0) {
-    const int n = s_nexp;
-    const int NG = n * RG, ND = n * (RD / RT);
-    s_g0 = cta * NG / G;
-    s_g1 = (cta + 1) * NG / G;
-    s_d0 = cta * ND / G;
-    s_d1 = (cta + 1) * ND / G;
-  }
-  __syncthreads();
+  // balancing a CTA's total bytes.  Every thread computes it.
+  const int n_exp_all = s_nexp;
+  const int NG = n_exp_all * RG, ND = n_exp_all * (RD / RT);
+  const int g0 = cta * NG / G, g1 = (cta + 1) * NG / G;
+  const int d0 = cta * ND / G, d1 = (cta + 1) * ND / G;
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 3);
-  const int g0 = s_g0, g1 = s_g1, d0 = s_d0, d1 = s_d1;
   const int n_gt = g1 - g0, n_dt = d1 - d0;
   const int DPE = RD / RT;               // down tiles per expert
   auto expert_base = [&](int ai) -> const uint8_t* {
@@ -484,6 +448,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         if (!mbar_wait(&full[k % NS], (k / NS) & 1)) set_error(a.err, DEV_TIMEOUT_BARRIER);
     }
   } else if (warp == kCW + 1) {
+    if (FUSED && cta == 0) {
+      // the plan of the call (read back for traces), LRU stamps, counters;
+      // this warp is idle until the first h is ready
+      Plan* P = a.plan;
+      const long long clk = s_clock;
+      const int n_act = n_exp_all - 1;
+      for (int i = lane; i < T * K; i += 32) {
+        P->idx[i] = s_act_expert[s_pick_act[i]];
+        P->w[i] = s_w[i];
+        P->pick_act[i] = s_pick_act[i];
+      }
+      for (int i = lane; i < n_act; i += 32) {
+        P->act_expert[i] = s_act_expert[i];
+        P->act_slot[i] = s_act_slot[i];
+        P->act_hit[i] = 1;
+        a.stamp[s_act_slot[i]] = clk;
+      }
+      if (lane == 0) {
+        P->n_act = n_act;
+        P->n_miss = 0;
+        P->T = T;
+        P->clock = clk;
+        P->token_hits = (int64_t)T * K;
+        P->token_misses = 0;
+        a.stats[ST_CALLS] += 1;
+        a.stats[ST_TOK_HIT] += (int64_t)T * K;
+        a.stats[ST_DIST_HIT] += n_act;
+        *a.clock = clk + 1;
+        *a.counters = s_calls + 1;   // every CTA read the count before the grid barrier
+      }
+      __syncwarp();
+    }
     // ---------------- h loader: one bulk copy of h_a per expert ------------
     if (lane == 0) {
       fence_proxy_async_smem();   // the h area held x through the generic proxy
@@ -567,16 +563,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         if (ti + 1 == n_gt && lane == 0) MOE_TL(g_ffn_timeline, cta, 9);
       } else {
         const int td = d0 + ti - n_gt, ai = td / DPE, rp = td % DPE;
+        // row block r is the sum, in warp order, of the WPR warps that took it
+#pragma unroll 1
         for (int r = 0; r < RT; ++r) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             float os[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) os[e] = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) {
-              const float4* pw =
-                  reinterpret_cast<const float4*>(red + ((size_t)w * 32 + lane) * RPL + (r * NT + nt) * 8);
+#pragma unroll 4
+            for (int w = r * WPR; w < (r + 1) * WPR; ++w) {
+              const float4* pw = reinterpret_cast<const float4*>(red + ((size_t)w * 32 + lane) * RPL + nt * 8);
               const float4 o0 = pw[0], o1 = pw[1];
               os[0] += o0.x; os[1] += o0.y; os[2] += o0.z; os[3] += o0.w;
               os[4] += o1.x; os[5] += o1.y; os[6] += o1.z; os[7] += o1.w;
@@ -711,9 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         }
         if (tid == 0 && ti == n_gt) MOE_TL(g_ffn_timeline, cta, 10);
         const uint8_t* hb = hbuf + (size_t)hs * NT * 8 * hrow;
-        float acc[kMaxRT][NT][2][4];
-#pragma unroll
-        for (int r = 0; r < kMaxRT; ++r) zero_acc<NT>(acc[r]);
+        // this warp sums row block r_w of the tile: its input groups j_w,
+        // j_w + WPR, ..., met in stage order, two blocks at a time
+        const int r_w = warp / WPR, j_w = warp - r_w * WPR;
+        const int rbase = r_w * DG;   // first block of the row block in the tile
+        float acc[NT][2][4];
+        zero_acc<NT>(acc);
         for (int st = 0; st < SDN; ++st, ++it) {
           const int s = it % NS;
           if (ok && !mbar_wait(&full[s], (it / NS) & 1)) {
@@ -721,21 +721,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
             ok = false;
           }
           if (ok) {
-            // this warp's two blocks of the stage: products first (independent,
-            // so they overlap), then each is added to its row block's sums
             const uint8_t* sp = ring + (size_t)s * kStageBytes;
-            const int b0 = st * kStageBlocks + warp, b1 = b0 + kCW;   // blocks of the tile
-            const int rl0 = b0 / DG, rl1 = b1 / DG;
-            uint2 bx0[NT][2], bx1[NT][2];
-            h_frags<NT>(hb, hrow, T, b0 - rl0 * DG, lane, bx0);
-            h_frags<NT>(hb, hrow, T, b1 - rl1 * DG, lane, bx1);
-            float D0[NT][2][4], D1[NT][2][4], s0[4], s1[4];
-            block_products<NT>(sp + warp * kBlockBytes, lane, bx0, D0, s0);
-            block_products<NT>(sp + (warp + kCW) * kBlockBytes, lane, bx1, D1, s1);
-#pragma unroll
-            for (int r = 0; r < kMaxRT; ++r) {
-              if (r == rl0) block_accum<NT>(D0, s0, acc[r]);
-              if (r == rl1) block_accum<NT>(D1, s1, acc[r]);
+            const int b_lo = max(rbase, st * kStageBlocks), b_hi = min(rbase + DG, (st + 1) * kStageBlocks);
+            for (int b = rbase + j_w + ((b_lo - rbase - j_w + WPR - 1) / WPR) * WPR; b < b_hi; b += 2 * WPR) {
+              const int b1 = b + WPR;
+              uint2 bx0[NT][2];
+              h_frags<NT>(hb, hrow, T, b - rbase, lane, bx0);
+              float D0[NT][2][4], s0[4];
+              block_products<NT>(sp + (b - st * kStageBlocks) * kBlockBytes, lane, bx0, D0, s0);
+              if (b1 < b_hi) {
+                uint2 bx1[NT][2];
+                h_frags<NT>(hb, hrow, T, b1 - rbase, lane, bx1);
+                float D1[NT][2][4], s1[4];
+                block_products<NT>(sp + (b1 - st * kStageBlocks) * kBlockBytes, lane, bx1, D1, s1);
+                block_accum<NT>(D0, s0, acc);
+                block_accum<NT>(D1, s1, acc);
+              } else {
+                block_accum<NT>(D0, s0, acc);
+              }
             }
           }
           __syncwarp();
@@ -748,14 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
         if (ok) {
           float4* m4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
-          for (int r = 0; r < kMaxRT; ++r)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int mt = 0; mt < 2; ++mt)
-                if (r < RT)
-                  m4[(r * NT + nt) * 2 + mt] =
-                      make_float4(acc[r][nt][mt][0], acc[r][nt][mt][1], acc[r][nt][mt][2], acc[r][nt][mt][3]);
+            for (int mt = 0; mt < 2; ++mt)
+              m4[nt * 2 + mt] = make_float4(acc[nt][mt][0], acc[nt][mt][1], acc[nt][mt][2], acc[nt][mt][3]);
         }
         signal_buf_full();
       }
@@ -774,11 +773,11 @@ template <int NT, bool FUSED>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   const size_t smem = ffn_smem_bytes<NT>(a.d, a.f);
   if (route_scratch_bytes(FUSED ? a.E : 0) > (size_t)FfnCfg<NT>::kStages * kStageBytes ||
-      (FUSED && a.E > kTabPerThread * kThreads))
+      (FUSED && a.E > kTabPerThread * kThreads) || kCW % down_rows_per_tile(a.f) != 0)
     return cudaErrorInvalidValue;
   // x is staged in the h + partial area
   if ((size_t)a.T * x_row_elems(a.d) * 2 >
-      (size_t)kHSlots * NT * 8 * h_row_bytes(a.f) + (size_t)kCW * 32 * red_per_lane(a.f, NT) * 4)
+      (size_t)kHSlots * NT * 8 * h_row_bytes(a.f) + (size_t)kCW * 32 * red_per_lane(NT) * 4)
     return cudaErrorInvalidValue;
   // raise the dynamic shared-memory limit once per size (not during stream capture)
   static size_t configured = 0;

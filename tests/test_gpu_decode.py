@@ -134,3 +134,22 @@ def test_decode_many_calls_sampled(decode):
     assert st["layer_calls"] - before["layer_calls"] == 64
     assert st["token_hits"] - before["token_hits"] == 64 * wl.top_k
     assert st["distinct_hits"] - before["distinct_hits"] == 64 * wl.top_k
+
+
+@pytest.mark.parametrize("f", [64, 192, 320, 256])
+def test_ffn_widths_row_blocks_per_down_tile(f):
+    # f = 64, 192, 320 put 8 row blocks in a down tile (one consumer warp
+    # each), f = 256 two; the tiny shape otherwise
+    import dataclasses
+    from moe_inputs import WORKLOADS, BIAS_LAMBDA
+    wl = dataclasses.replace(WORKLOADS[1], f=f)
+    s = Synth(wl, bias_lambda=BIAS_LAMBDA)
+    layer = make_layer(s)
+    try:
+        layer.moe_cache_configure(wl.capacity, np.arange(wl.keys))
+        memo = ExpertMemo(s, wl.keys)
+        for T in (1, 5):
+            xb = s.tokens_many(0, [900 + T], T=T)[0]
+            _check_call(s, layer, memo, xb)
+    finally:
+        layer.close()
