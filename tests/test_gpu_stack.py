@@ -83,10 +83,12 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
     return meas["hits"] / meas["picks"], tot, st
 
 
-@pytest.mark.parametrize("miss_mode", [MOE_MISS_DEVICE_PULL, MOE_MISS_HOST_COPY])
-def test_small_stack_with_evictions(miss_mode):
-    # both ways of fetching misses: the GPU reading the host pool, or host-issued copies
-    over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=5, capacity=40, calls=60)
+@pytest.mark.parametrize("miss_mode,tokens", [(MOE_MISS_DEVICE_PULL, 5), (MOE_MISS_HOST_COPY, 5),
+                                             (MOE_MISS_DEVICE_PULL, 1)])
+def test_small_stack_with_evictions(miss_mode, tokens):
+    # both ways of fetching misses: the GPU reading the host pool, or host-issued copies;
+    # one-token calls take the selection's single-token path
+    over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=tokens, capacity=40, calls=60)
     rate, tot, _ = run_stack(3, passes=2, pool_entries=96, overrides=over,
                              ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode)
     assert tot["evictions"] > 0 and tot["token_misses"] > 0
