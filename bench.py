@@ -240,22 +240,22 @@ def run_prefill(steps, warmup, sweep=(4096, 6144, 8192, 12288, 16384)):
 
 # ------------------------------------------------------------ 48-layer stack --
 def _draw_layer_tokens(args):
-    cfg_id, lam, layer, calls = args
+    cfg_id, lam, layer, calls, T = args
     sys.path.insert(0, ROOT)
     from moe_inputs import Synth, WORKLOADS
     s = Synth(WORKLOADS[cfg_id], bias_lambda=lam)
-    return layer, s.tokens_many(layer, list(range(calls)))
+    return layer, s.tokens_many(layer, list(range(calls)), T=T)
 
 
-def draw_stack_tokens(cfg_id, calls, n_layers, workers=16):
+def draw_stack_tokens(cfg_id, calls, n_layers, workers=16, T=None):
     """Seeded activations [L, calls, T, d] (bf16 bits) of a stack workload,
-    one spawn-pool job per layer."""
+    one spawn-pool job per layer (T defaults to the workload's)."""
     import concurrent.futures as cf
     import multiprocessing as mp
     from moe_inputs import BIAS_LAMBDA
     out = [None] * n_layers
     with cf.ProcessPoolExecutor(max_workers=min(workers, n_layers), mp_context=mp.get_context("spawn")) as ex:
-        for layer, xs in ex.map(_draw_layer_tokens, [(cfg_id, BIAS_LAMBDA, l, calls) for l in range(n_layers)]):
+        for layer, xs in ex.map(_draw_layer_tokens, [(cfg_id, BIAS_LAMBDA, l, calls, T) for l in range(n_layers)]):
             out[layer] = xs
     return np.stack(out)
 
@@ -383,6 +383,69 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1):
             "roofline": {"bound_ms": 1e3 * t_bound, "frac": 1e3 * t_bound / ms,
                          "note": "max(distinct-expert bytes / HBM, miss bytes / measured H2D)"},
             "setup_s": setup_s}
+
+
+def run_stack_sweep(pool_entries=2048, calls=500, tokens=(1, 4, 7), capacities=(9057, 8445, 6144)):
+    """Draft width x cache capacity sweep on the verify stack (48 layers,
+    Zipf s=1.1): for each verify width T (1 + draft tokens) and capacity C
+    the cache starts empty, 3 warm-up passes over `calls` calls, then the
+    timed pass; misses pulled by the GPU.  Tokens of width T are the first T
+    rows of the widest draw (the generator is prefix-consistent)."""
+    import time
+    import torch
+    from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA
+    from expert_cached_decode_gb300.layer import MoELayer
+    cfg_id = 3
+    wl = WORKLOADS[cfg_id]
+    t0 = time.time()
+    xs = draw_stack_tokens(cfg_id, calls, wl.n_layers, T=max(tokens))
+    shm, pool = make_host_pool(cfg_id, pool_entries)
+    s = Synth(wl, bias_lambda=BIAS_LAMBDA)
+    wr = np.stack([s.router(l)[0] for l in range(wl.n_layers)])
+    b = np.stack([s.router(l)[2] for l in range(wl.n_layers)])
+    shared = np.stack([s.shared_packed(l) for l in range(wl.n_layers)])
+    layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
+                     host_pool_entries=pool_entries)
+    layer.moe_set_miss_mode(1)
+    setup_s = time.time() - t0
+    xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
+    stream = torch.cuda.Stream()
+    rows = []
+    for T in tokens:
+        y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
+        for C in capacities:
+            layer.moe_cache_configure(C)
+            with torch.cuda.stream(stream):
+                for _ in range(wl.warm_passes):
+                    for c in range(calls):
+                        for l in range(wl.n_layers):
+                            layer.moe_forward(l, xdev[l, c, :T], y)
+            stream.synchronize()
+            before = layer.moe_cache_stats()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for c in range(calls):
+                    for l in range(wl.n_layers):
+                        layer.moe_forward(l, xdev[l, c, :T], y)
+            e1.record(stream)
+            stream.synchronize()
+            ms = e0.elapsed_time(e1)
+            after = layer.moe_cache_stats()
+            dl = {k: after[k] - before[k] for k in after}
+            lc = max(1, dl["layer_calls"])
+            rows.append({"T": T, "capacity": C, "tokens_per_s": calls * T / (ms / 1e3),
+                         "token_hit_rate": dl["token_hits"] / max(1, dl["token_hits"] + dl["token_misses"]),
+                         "distinct_experts_per_layer_call": (dl["distinct_hits"] + dl["distinct_misses"]) / lc,
+                         "misses_per_layer_call": dl["distinct_misses"] / lc,
+                         "us_per_layer_call": 1e3 * ms / lc})
+    layer.close()
+    del pool
+    shm.close()
+    shm.unlink()
+    return {"workload": f"verify stack (48 layers, Zipf s={wl.zipf_s}, lambda {BIAS_LAMBDA}), cache starting empty, "
+                        f"{wl.warm_passes} warm-up passes then the timed pass over {calls} calls; GPU pulls misses; "
+                        f"host pool {pool_entries} entries", "setup_s": setup_s, "rows": rows}
 
 
 def cpu_oracle_sample(n_calls, threads=1):
@@ -565,6 +628,11 @@ def run_gpu(args):
                 line["prefill"] = run_prefill(args.prefill_steps, 3)
             except Exception as ex:   # reported, not hidden
                 line["prefill"] = {"error": str(ex)[:300]}
+        if args.stack_sweep:
+            try:
+                line["stack_sweep"] = run_stack_sweep(calls=args.stack_sweep)
+            except Exception as ex:   # reported, not hidden
+                line["stack_sweep"] = {"error": str(ex)[:300]}
         if args.stack:
             try:
                 line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m) for c in (3, 4) for m in (1, 0)]
@@ -598,6 +666,9 @@ def main():
     ap.add_argument("--stack-pool", type=int, default=2048,
                     help="host-pool entries for --stack: expert (l, e) reads entry (512 l + e) mod P; "
                          "0 = one per (layer, expert), 50.7 GB, slow to fill (default 2048, 4.2 GB)")
+    ap.add_argument("--stack-sweep", type=int, default=0, metavar="CALLS",
+                    help="verify width (T = 1, 4, 7) x cache capacity (9,057 / 8,445 / 6,144) sweep on the "
+                         "verify stack, CALLS calls per pass")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="time only the prefill path at T tokens (profiling runs)")
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="T",
