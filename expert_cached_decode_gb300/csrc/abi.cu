@@ -296,7 +296,9 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
   CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
   CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
-  c->set_words = c->max_exp + 1 + c->d / 32;
+  // h_ready[max_exp] | router barrier | d_cnt[d/32] | cache-mode flags:
+  // victims published, misses pulled, misses placed
+  c->set_words = c->max_exp + 1 + c->d / 32 + 3;
   c->counters_n = 1 + 2 * (size_t)c->set_words;
   CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
@@ -583,6 +585,14 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.stamp = c->stamp;
   fa.stats = c->stats + (size_t)layer * ST_N;
   fa.clock = c->clock;
+  // fused routing with misses pulled by the GPU (cache not all resident)
+  fa.owner = c->owner;
+  fa.q_in = c->lruq[c->qcur];
+  fa.q_out = c->lruq[c->qcur ^ 1];
+  fa.C = (int)c->C;
+  fa.host_pool = c->host_pool_dev;
+  fa.pool_entries = c->P;
+  fa.staging = c->staging;
   return fa;
 }
 
@@ -715,6 +725,16 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   if (c->all_resident) {
     fa.fused = 1;
     CUDA_TRY(launch_decode_ffn(fa, s, true));
+    if (trace) return fill_trace(c, s, T, trace);
+    return MOE_OK;
+  }
+  if (c->pull && c->num_sms >= 2) {
+    // one launch: routing, the cache (CTA 0) and the GPU's own pull of the
+    // misses, then the experts; the LRU order alternates between two arrays
+    fa.fused = 1;
+    fa.cached = 1;
+    CUDA_TRY(launch_decode_ffn(fa, s, true));
+    c->qcur ^= 1;
     if (trace) return fill_trace(c, s, T, trace);
     return MOE_OK;
   }

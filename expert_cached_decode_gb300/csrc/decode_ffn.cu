@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
+#include "repack.cuh"
 
 namespace moe {
 
@@ -176,8 +177,275 @@ __host__ __device__ __forceinline__ size_t route_scratch_bytes(int E) {
   return ((sizeof(SelSmem) + 15) & ~size_t(15)) + (size_t)E * 4;
 }
 
-template <int NT, bool FUSED>
+// MODE kPlanRead: the routing plan comes from memory (routing kernel and
+// host-issued miss copies before this launch).  kFusedResident: routing in
+// this kernel, every key resident.  kFusedCached: routing in this kernel with
+// a cache that may miss; CTA 0 manages the cache (LRU victims, the next LRU
+// order, commit, plan) while CTAs 1..G-1 pull the misses from the host pool,
+// re-lay them out into their victim slots and run the experts.
+// exclusive prefix sum over the kThreads threads of the CTA (every thread
+// calls it); s_warp holds kThreads/32 + 1 ints
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* s_warp, int* total) {
+  constexpr int NW = kThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int wv = lane < NW ? s_warp[lane] : 0;
+    int wi = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < NW) s_warp[lane] = wi - wv;
+    if (lane == NW - 1) s_warp[NW] = wi;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + inc - v;
+  *total = s_warp[NW];
+  __syncthreads();   // s_warp may be reused
+  return r;
+}
+
+// Cache of a layer-call with fused routing, run by every thread of CTA 0
+// (which takes no tiles).  LRU by (layer, expert), ties to the lower slot id
+// (page "单卡5090跑125B 大模型", §2.1 and §7.2): U = the call's distinct
+// experts (ascending); resident ones are hits; the misses, in ascending
+// expert id, take the least recently used slots in (stamp, slot id) order,
+// which is the order of q (least recent first) with the hits skipped.  The
+// call's touched slots (hits and victims) move, in slot-id order, to the
+// recent end of q.  The victims are published first (xbar[0]), because CTAs
+// 1..G-1 wait for them before pulling the misses; then the commit (table,
+// owners, stamps), the next order, the plan and the statistics.
+// `scratch` is shared memory this CTA does not otherwise use.
+__device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m, const int* s_act_expert,
+                                              int* s_act_slot, const int* s_pick_act, const float* s_w,
+                                              long long clk, uint32_t calls, uint8_t* scratch,
+                                              size_t scratch_bytes, uint32_t* xbar) {
+  __shared__ int s_warp[kThreads / 32 + 1];
+  __shared__ int s_evict;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, K = a.k, C = a.C;
+  const int c_words = (C + 31) / 32;
+  Plan* P = a.plan;
+  int32_t* table = const_cast<int32_t*>(a.table);
+  // scratch: four per-pick arrays, the touched-slot bitmap, then (if it
+  // fits) the staged LRU order
+  int* s_miss_ai = reinterpret_cast<int*>(scratch);
+  int* s_victim = s_miss_ai + kMaxPicks;
+  int* s_old = s_victim + kMaxPicks;
+  int* s_hitf = s_old + kMaxPicks;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(s_hitf + kMaxPicks);
+  const size_t head = (size_t)4 * kMaxPicks * 4;
+  const size_t bits_bytes = ((size_t)c_words * 4 + 15) & ~size_t(15);
+  int32_t* sq = head + bits_bytes + (size_t)C * 4 <= scratch_bytes
+                    ? reinterpret_cast<int32_t*>(scratch + head + bits_bytes)
+                    : nullptr;
+  for (int i = tid; i < c_words; i += kThreads) bits[i] = 0;
+  if (sq) {   // the LRU order staged with 16-byte loads, all in flight
+    const int n4 = C >> 2;
+    const int4* src4 = reinterpret_cast<const int4*>(a.q_in);
+#pragma unroll 4
+    for (int i = tid; i < n4; i += kThreads) reinterpret_cast<int4*>(sq)[i] = __ldcg(src4 + i);
+    for (int i = 4 * n4 + tid; i < C; i += kThreads) sq[i] = a.q_in[i];
+  }
+  for (int i = tid; i < n_act; i += kThreads) s_hitf[i] = s_act_slot[i] >= 0;
+  if (warp == 0) {   // the misses in ascending expert id
+    int base = 0;
+    for (int i0 = 0; i0 < n_act; i0 += 32) {
+      const int i = i0 + lane;
+      const bool miss = i < n_act && s_act_slot[i] < 0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, miss);
+      if (miss) s_miss_ai[base + __popc(bal & ((1u << lane) - 1u))] = i;
+      base += __popc(bal);
+    }
+  }
+  if (tid == 0) s_evict = 0;
+  __syncthreads();
+  for (int i = tid; i < n_act; i += kThreads) {
+    const int sl = s_act_slot[i];
+    if (sl >= 0) atomicOr(&bits[sl >> 5], 1u << (sl & 31));
+  }
+  __syncthreads();
+  const int32_t* q_in = sq ? sq : a.q_in;
+  // walk q skipping the hits: the first m slots are the victims, the rest
+  // keep their order at the front of the next q
+  const int chunk = (C + kThreads - 1) / kThreads;
+  const int lo = min(C, tid * chunk), hi = min(C, lo + chunk);
+  int cnt = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int sl = q_in[i];
+    cnt += !((bits[sl >> 5] >> (sl & 31)) & 1u);
+  }
+  int total;
+  int r = cta_exclusive_scan(cnt, s_warp, &total);
+  for (int i = lo; i < hi; ++i) {
+    const int sl = q_in[i];
+    if (!((bits[sl >> 5] >> (sl & 31)) & 1u)) {
+      if (r < m) s_victim[r] = sl;
+      else a.q_out[r - m] = sl;
+      ++r;
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j < m; j += kThreads) {
+    const int v = s_victim[j];
+    const int ai = s_miss_ai[j];
+    const int old = a.owner[v];
+    atomicOr(&bits[v >> 5], 1u << (v & 31));
+    s_old[j] = old;
+    s_act_slot[ai] = v;
+    P->miss_expert[j] = s_act_expert[ai];
+    P->miss_slot[j] = v;
+    P->evicted_key[j] = old;
+  }
+  __syncthreads();
+  for (int i = tid; i < n_act; i += kThreads) {
+    P->act_slot[i] = s_act_slot[i];
+    P->act_hit[i] = s_hitf[i];
+    P->act_expert[i] = s_act_expert[i];
+  }
+  __syncthreads();
+  if (m > 0 && tid == 0) red_release_add(&xbar[0], 1u);   // covers the plan's victim entries (after the barrier)
+  // commit: evicted keys leave the table before the misses enter it
+  for (int j = tid; j < m; j += kThreads) {
+    const int old = s_old[j];
+    if (old >= 0) {
+      table[old] = -1;
+      atomicAdd(&s_evict, 1);
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j < m; j += kThreads) {
+    const int v = s_victim[j];
+    const int key = a.layer * a.E + s_act_expert[s_miss_ai[j]];
+    a.owner[v] = key;
+    table[key] = v;
+    a.stamp[v] = clk;
+  }
+  for (int i = tid; i < n_act; i += kThreads)
+    if (s_hitf[i]) a.stamp[s_act_slot[i]] = clk;
+  // touched slots (hits and victims) in ascending slot id to the recent end
+  const int wchunk = (c_words + kThreads - 1) / kThreads;
+  const int wlo = min(c_words, tid * wchunk), whi = min(c_words, wlo + wchunk);
+  int tc = 0;
+  for (int i = wlo; i < whi; ++i) tc += __popc(bits[i]);
+  int tr = cta_exclusive_scan(tc, s_warp, &total);
+  for (int i = wlo; i < whi; ++i) {
+    uint32_t b = bits[i];
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      b &= b - 1;
+      a.q_out[C - n_act + tr] = i * 32 + bit;
+      ++tr;
+    }
+  }
+  // the plan's routing part and the counts
+  for (int i = tid; i < T * K; i += kThreads) {
+    P->idx[i] = s_act_expert[s_pick_act[i]];
+    P->w[i] = s_w[i];
+    P->pick_act[i] = s_pick_act[i];
+  }
+  const int th = __syncthreads_count(tid < T * K && s_hitf[s_pick_act[tid]]);
+  if (tid == 0) {
+    P->n_act = n_act;
+    P->n_miss = m;
+    P->T = T;
+    P->clock = clk;
+    P->token_hits = th;
+    P->token_misses = (int64_t)T * K - th;
+    a.stats[ST_CALLS] += 1;
+    a.stats[ST_TOK_HIT] += th;
+    a.stats[ST_TOK_MISS] += (int64_t)T * K - th;
+    a.stats[ST_DIST_HIT] += n_act - m;
+    a.stats[ST_DIST_MISS] += m;
+    a.stats[ST_EVICT] += s_evict;
+    a.stats[ST_MISS_BYTES] += (int64_t)m * a.expert_bytes;
+    *a.clock = clk + 1;
+    *a.counters = calls + 1;   // every CTA read the count before the router barrier
+  }
+}
+
+// One arrival of this CTA on a grid counter, then the wait for all GT CTAs
+// (bounded); false if the wait gave up.  Every thread calls it.
+__device__ __forceinline__ bool cta_grid_barrier(uint32_t* bar, uint32_t GT, uint32_t* err, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    red_release_add(bar, 1u);   // covers this CTA's writes (after the block barrier)
+    const bool ok = wait_flag_geq(bar, GT);
+    if (!ok) set_error(err, DEV_TIMEOUT_FLAG);
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+// CTAs 1..G-1 (index ct of GT) of a call with m > 0 misses: wait for CTA 0's
+// victims, pull the misses' canonical bytes from the host pool into
+// staging, a grid barrier, re-lay them out into their victim slots, a grid
+// barrier.  False if a wait gave up (the error word is set).
+__device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, int n_act, int* s_act_slot,
+                                                      uint32_t* xbar, int GT, int ct, uint8_t* scratch) {
+  int* s_mslot = reinterpret_cast<int*>(scratch);   // shared memory not yet in use by the tiles
+  int* s_mexp = s_mslot + kMaxPicks;
+  __shared__ int s_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Plan* P = a.plan;
+  if (tid == 0) {
+    const bool ok = wait_flag_geq(&xbar[0], 1u);
+    if (!ok) set_error(a.err, DEV_TIMEOUT_FLAG);
+    s_flag = ok;
+  }
+  __syncthreads();
+  if (!s_flag) return false;
+  for (int j = tid; j < m; j += kThreads) {
+    s_mslot[j] = __ldcg(&P->miss_slot[j]);
+    s_mexp[j] = __ldcg(&P->miss_expert[j]);
+  }
+  for (int i = tid; i < n_act; i += kThreads)
+    if (s_act_slot[i] < 0) s_act_slot[i] = __ldcg(&P->act_slot[i]);
+  __syncthreads();
+  // host pool -> staging, 16 bytes per thread and step, four loads in flight
+  const int64_t per = a.expert_bytes / 16;
+  const int64_t nthr = (int64_t)GT * kThreads;
+  for (int j = 0; j < m; ++j) {
+    const int64_t entry = ((int64_t)a.layer * a.E + s_mexp[j]) % a.pool_entries;
+    const uint4* src = reinterpret_cast<const uint4*>(a.host_pool + entry * a.expert_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(a.staging + (int64_t)j * a.expert_bytes);
+    int64_t c = (int64_t)ct * kThreads + tid;
+    for (; c + 3 * nthr < per; c += 4 * nthr) {
+      const uint4 v0 = src[c], v1 = src[c + nthr], v2 = src[c + 2 * nthr], v3 = src[c + 3 * nthr];
+      dst[c] = v0;
+      dst[c + nthr] = v1;
+      dst[c + 2 * nthr] = v2;
+      dst[c + 3 * nthr] = v3;
+    }
+    for (; c < per; c += nthr) dst[c] = src[c];
+  }
+  if (!cta_grid_barrier(&xbar[1], (uint32_t)GT, a.err, &s_flag)) return false;
+  // staging -> victim slots in the device block layout, one block per warp
+  const int nb = (a.f / 32) * (a.d / 32) * 2 + (a.d / 32) * (a.f / 32);
+  const int64_t nwarps = (int64_t)GT * (kThreads / 32);
+  uint8_t* slots = const_cast<uint8_t*>(a.slots);
+  for (int64_t gw = (int64_t)ct * (kThreads / 32) + warp; gw < (int64_t)nb * m; gw += nwarps) {
+    const int ex = (int)(gw / nb), bi = (int)(gw % nb);
+    repack_block(a.staging + (int64_t)ex * a.expert_bytes, slots + (int64_t)s_mslot[ex] * a.expert_bytes, bi, a.d,
+                 a.f, lane);
+  }
+  return cta_grid_barrier(&xbar[2], (uint32_t)GT, a.err, &s_flag);
+}
+
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
+  constexpr bool FUSED = MODE != kPlanRead;
+  constexpr bool CACHED = MODE == kFusedCached;
   constexpr int NS = FfnCfg<NT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const int d = a.d, f = a.f, T = a.T, K = a.k;
@@ -238,10 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   uint4 wfirst[8];
   float wbias = 0.f;
   if (FUSED) {
+    if (!CACHED) {
 #pragma unroll
-    for (int q = 0; q < kTabPerThread; ++q) {
-      const int i = tid + q * kThreads;
-      tv[q] = i < a.E ? a.table[(size_t)a.layer * a.E + i] : -1;
+      for (int q = 0; q < kTabPerThread; ++q) {
+        const int i = tid + q * kThreads;
+        tv[q] = i < a.E ? a.table[(size_t)a.layer * a.E + i] : -1;
+      }
     }
     const int e = cta + G * warp;
     if (e < a.E) {
@@ -253,6 +523,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   // x, the clock and the counters may be written by earlier work in the
   // stream
   pdl_wait();
+  if (CACHED) {   // the slot table changes with every commit: read it after the previous call
+#pragma unroll
+    for (int q = 0; q < kTabPerThread; ++q) {
+      const int i = tid + q * kThreads;
+      tv[q] = i < a.E ? a.table[(size_t)a.layer * a.E + i] : -1;
+    }
+  }
   uint32_t calls = 0;
   long long clk = 0;
   if (tid == 0) {
@@ -369,11 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     }
     for (int i = tid; i < n_act; i += kThreads) {
       int slot = s_tab[sel->act[i]];
-      if (slot < 0) {
+      if (slot < 0 && !CACHED) {
         set_error(a.err, DEV_NOT_RESIDENT);
         slot = 0;
       }
-      s_act_slot[i] = slot;
+      s_act_slot[i] = slot;   // cached: -1 marks a miss until CTA 0 assigns its victim
       s_act_expert[i] = sel->act[i];
     }
     if (tid == 0) s_nexp = n_act + 1;
@@ -395,10 +672,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
   // gate/up phase, so balancing the phases separately ends both sooner than
   // balancing a CTA's total bytes.  Every thread computes it.
   const int n_exp_all = s_nexp;
+  // cached mode: CTA 0 manages the cache, CTAs 1..G-1 take the tiles
+  const int GT = CACHED ? G - 1 : G;
+  const int ct = CACHED ? cta - 1 : cta;
   const int NG = n_exp_all * RG, ND = n_exp_all * (RD / RT);
-  const int g0 = cta * NG / G, g1 = (cta + 1) * NG / G;
-  const int d0 = cta * ND / G, d1 = (cta + 1) * ND / G;
+  const int g0 = ct * NG / GT, g1 = (ct + 1) * NG / GT;
+  const int d0 = ct * ND / GT, d1 = (ct + 1) * ND / GT;
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 3);
+  if (CACHED) {
+    const int n_act_c = n_exp_all - 1;
+    const int n_miss = __syncthreads_count(tid < n_act_c && s_act_slot[tid] < 0);
+    uint32_t* const xbar = a.counters + 1 + (size_t)call_set * a.set_words + a.max_exp + 1 + RD;
+    if (cta == 0) {
+      cache_manager(a, n_act_c, n_miss, s_act_expert, s_act_slot, s_pick_act, s_w, s_clock, s_calls, ring,
+                    (size_t)NS * kStageBytes, xbar);
+      return;
+    }
+    if (n_miss > 0 && !pull_and_place_misses(a, n_miss, n_act_c, s_act_slot, xbar, G - 1, cta - 1, ring))
+      return;   // the error word is set; no copy was issued
+  }
   const int n_gt = g1 - g0, n_dt = d1 - d0;
   const int DPE = RD / RT;               // down tiles per expert
   auto expert_base = [&](int ai) -> const uint8_t* {
@@ -412,6 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     if (lane == 0) {
       // the ring held generic-proxy scratch; order it before the bulk copies
       fence_proxy_async_smem();
+      // slots of this call's misses were written by other CTAs' generic stores
+      if (CACHED) asm volatile("fence.proxy.async.global;" ::: "memory");
       MOE_TL(g_ffn_timeline, cta, 25);
       uint32_t it = 0;
       bool ok = true;
@@ -601,14 +895,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
     // order (shared expert, then the picks in ascending id), all loads of
     // one output issued before the sum.
     const int n_exp = s_nexp;
-    for (int rb = cta; ok && rb < RD; rb += G) {
+    for (int rb = ct; ok && rb < RD; rb += GT) {
       uint32_t good = 1;
       if (lane == 0 && !wait_flag_geq(&d_cnt[rb], (uint32_t)n_exp)) {
         set_error(a.err, DEV_TIMEOUT_FLAG);
         good = 0;
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
-      if (lane == 0 && rb == cta) MOE_TL(g_ffn_timeline, cta, 23);
+      if (lane == 0 && rb == ct) MOE_TL(g_ffn_timeline, cta, 23);
       __syncwarp();   // the other lanes read after lane 0's acquire
       const int row = rb * 32 + lane;
 #pragma unroll 1
@@ -627,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_ffn_kernel(FfnArgs a) {
 #pragma unroll
         for (int k2 = 0; k2 < kMaxTopK; ++k2)
           if (k2 < K) yv = fmaf(s_w[t * K + k2], ov[k2], yv);
-        if (lane == 0 && rb == cta && t == 0) MOE_TL(g_ffn_timeline, cta, 24);
+        if (lane == 0 && rb == ct && t == 0) MOE_TL(g_ffn_timeline, cta, 24);
         a.y[(size_t)t * d + row] = yv;
       }
     }
@@ -769,8 +1063,9 @@ extern "C" int moe_debug_timeline_ffn(unsigned long long* out) {
 }
 #endif
 
-template <int NT, bool FUSED>
+template <int NT, int MODE>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
+  constexpr bool FUSED = MODE != kPlanRead;
   const size_t smem = ffn_smem_bytes<NT>(a.d, a.f);
   if (route_scratch_bytes(FUSED ? a.E : 0) > (size_t)FfnCfg<NT>::kStages * kStageBytes ||
       (FUSED && a.E > kTabPerThread * kThreads) || kCW % down_rows_per_tile(a.f) != 0)
@@ -782,7 +1077,7 @@ static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int gri
   // raise the dynamic shared-memory limit once per size (not during stream capture)
   static size_t configured = 0;
   if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
@@ -797,13 +1092,17 @@ static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int gri
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel<NT, FUSED>, a);
+  return cudaLaunchKernelEx(&cfg, decode_ffn_kernel<NT, MODE>, a);
 }
 
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl) {
-  if (a.grid <= 0) return cudaErrorInvalidValue;
-  if (a.T <= 8) return a.fused ? launch_nt<1, true>(a, s, pdl, a.grid) : launch_nt<1, false>(a, s, pdl, a.grid);
-  return a.fused ? launch_nt<2, true>(a, s, pdl, a.grid) : launch_nt<2, false>(a, s, pdl, a.grid);
+  if (a.grid <= 0 || (a.cached && (!a.fused || a.grid < 2))) return cudaErrorInvalidValue;
+  if (a.T <= 8) {
+    if (!a.fused) return launch_nt<1, kPlanRead>(a, s, pdl, a.grid);
+    return a.cached ? launch_nt<1, kFusedCached>(a, s, pdl, a.grid) : launch_nt<1, kFusedResident>(a, s, pdl, a.grid);
+  }
+  if (!a.fused) return launch_nt<2, kPlanRead>(a, s, pdl, a.grid);
+  return a.cached ? launch_nt<2, kFusedCached>(a, s, pdl, a.grid) : launch_nt<2, kFusedResident>(a, s, pdl, a.grid);
 }
 
 }  // namespace moe

@@ -130,7 +130,19 @@ struct FfnArgs {
   int64_t* stamp;               // [C]
   int64_t* stats;               // this layer's counters
   int64_t* clock;
+  // fused routing with a cache that may miss (misses pulled by the GPU)
+  int cached;
+  int32_t* owner;               // [C] key held by each slot, -1 if none
+  const int32_t* q_in;          // [C] slots, least recently used first
+  int32_t* q_out;               // [C] the order after this call
+  int C;
+  const uint8_t* host_pool;     // device address of the registered host pool (canonical experts)
+  int64_t pool_entries;         // key (layer, e) reads entry (layer*E + e) mod pool_entries
+  uint8_t* staging;             // [>= T*k][expert_bytes] canonical copies of this call's misses
 };
+
+// decode kernel modes
+enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2 };
 
 struct RouterGemmArgs {
   const float* bias;   // [E]

@@ -32,6 +32,10 @@ __device__ unsigned long long g_route_timeline[256][16];
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
+// the LRU order q is staged in shared memory (one 16-byte load per 4 slots,
+// all in flight) when the cache has at most this many slots
+constexpr int kRouteQSmem = 32768;
+constexpr size_t kSelBytes = (sizeof(SelSmem) + 15) & ~size_t(15);
 
 // exclusive prefix sum over the 256 threads of the CTA; returns the total
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
@@ -137,6 +141,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   const int C = a.C;
   const int c_words = (C + 31) / 32;
   for (int i = threadIdx.x; i < c_words; i += kRouteThreads) s_bits[i] = 0;
+  int32_t* s_q = C <= kRouteQSmem ? reinterpret_cast<int32_t*>(route_dyn_smem + kSelBytes) : nullptr;
+  if (s_q) {
+    const int n4 = C >> 2;
+    const int4* src4 = reinterpret_cast<const int4*>(a.q_in);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n4; i += kRouteThreads) reinterpret_cast<int4*>(s_q)[i] = __ldg(src4 + i);
+    for (int i = 4 * n4 + threadIdx.x; i < C; i += kRouteThreads) s_q[i] = a.q_in[i];
+  }
+  const int32_t* q_in = s_q ? s_q : a.q_in;
   if (threadIdx.x == 0) {
     int m = 0;
     for (int i = 0; i < n_act; ++i)
@@ -155,13 +168,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   const int lo = min(C, (int)threadIdx.x * chunk), hi = min(C, lo + chunk);
   int cnt = 0;
   for (int i = lo; i < hi; ++i) {
-    const int s = a.q_in[i];
+    const int s = q_in[i];
     cnt += !((s_bits[s >> 5] >> (s & 31)) & 1u);
   }
   int total;
   int r = block_exclusive_scan(cnt, s_scan, &total);
   for (int i = lo; i < hi; ++i) {
-    const int s = a.q_in[i];
+    const int s = q_in[i];
     if (!((s_bits[s >> 5] >> (s & 31)) & 1u)) {
       if (r < m) s_victim[r] = s;
       else a.q_out[r - m] = s;
@@ -263,16 +276,18 @@ extern "C" int moe_debug_timeline_route(unsigned long long* out) {
 #endif
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-  // the selection scratch is dynamic shared memory (static + dynamic > 48 KB)
+  // the selection scratch (and the staged LRU order) is dynamic shared
+  // memory (static + dynamic > 48 KB)
   static bool configured = false;
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SelSmem));
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kSelBytes + (size_t)kRouteQSmem * 4));
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  const size_t dyn = kSelBytes + (a.mode == ROUTE_PLAN && a.C <= kRouteQSmem ? (size_t)a.C * 4 : 0);
   const int grid = (a.E + kRouteWarps - 1) / kRouteWarps;
-  route_kernel<<<grid, kRouteThreads, sizeof(SelSmem), s>>>(a);
+  route_kernel<<<grid, kRouteThreads, dyn, s>>>(a);
   return cudaGetLastError();
 }
 
