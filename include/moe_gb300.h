@@ -138,20 +138,23 @@ moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32
  * y[T][d] (fp32, device).  x[T][d] bf16 (device); x and y 16-byte aligned.  1 <= T <= 16 uses the
  * decode path; larger T (up to 16,384) the prefill path, which needs every
  * key resident and f % 128 == 0 (MOE_ERR_UNIMPLEMENTED otherwise).  Asynchronous on
- * `stream` when every key is resident (see moe_cache_configure); otherwise the
- * host waits for the routing kernel, issues the miss copies on a side stream
- * and joins it with an event before the experts run.  On error the cache
- * state is unchanged.  `trace` may be NULL. */
+ * `stream` when every key is resident (see moe_cache_configure) and, with the
+ * default MOE_MISS_DEVICE_PULL, also when misses can occur (one kernel launch
+ * routes, plans and commits the cache, pulls the misses and runs the
+ * experts); with MOE_MISS_HOST_COPY the host waits for the routing kernel,
+ * issues the miss copies on a side stream and joins it with an event before
+ * the experts run.  On error the cache state is unchanged.  `trace` may be
+ * NULL (with a trace the call synchronises to read the plan back). */
 moe_status moe_forward(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T,
                        float* y, void* stream, moe_trace* trace);
 
 /* How a layer-call with misses fetches the missing experts (the cache of
  * page "单卡5090跑125B 大模型", §2.1 and §7.2: misses come from pinned host RAM).
  *   MOE_MISS_DEVICE_PULL (default when the host pool is device-accessible):
- *     the GPU reads the registered host pool itself (NVLink-C2C or PCIe),
- *     kernels take the miss list from the routing plan in device memory, and
- *     moe_forward does not wait for the GPU (nothing between routing and the
- *     copies goes through the host);
+ *     the GPU reads the registered host pool itself (NVLink-C2C or PCIe)
+ *     inside the decode kernel, which takes the miss list from its own plan,
+ *     and moe_forward does not wait for the GPU (nothing between routing and
+ *     the copies goes through the host);
  *   MOE_MISS_HOST_COPY: the host waits for the routing plan and issues one
  *     cudaMemcpyAsync per miss on a side stream.
  * Both give the same slots, counters and outputs.  Returns
