@@ -635,7 +635,9 @@ def run_gpu(args):
                 line["stack_sweep"] = {"error": str(ex)[:300]}
         if args.stack:
             try:
-                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m) for c in (3, 4) for m in (1, 0)]
+                cfgs = (3, 4) if args.stack_config == 0 else (args.stack_config,)
+                modes = (1, 0) if args.stack_mode < 0 else (args.stack_mode,)
+                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m) for c in cfgs for m in modes]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:
@@ -666,6 +668,10 @@ def main():
     ap.add_argument("--stack-pool", type=int, default=2048,
                     help="host-pool entries for --stack: expert (l, e) reads entry (512 l + e) mod P; "
                          "0 = one per (layer, expert), 50.7 GB, slow to fill (default 2048, 4.2 GB)")
+    ap.add_argument("--stack-config", type=int, default=0, choices=(0, 3, 4),
+                    help="--stack: 3 = verify stack only, 4 = concurrent stack only (default both)")
+    ap.add_argument("--stack-mode", type=int, default=-1, choices=(-1, 0, 1),
+                    help="--stack: 1 = GPU pulls misses, 0 = host-issued copies (default both)")
     ap.add_argument("--stack-sweep", type=int, default=0, metavar="CALLS",
                     help="verify width (T = 1, 4, 7) x cache capacity (9,057 / 8,445 / 6,144) sweep on the "
                          "verify stack, CALLS calls per pass")

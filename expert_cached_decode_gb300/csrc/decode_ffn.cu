@@ -313,7 +313,10 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
     P->act_expert[i] = s_act_expert[i];
   }
   __syncthreads();
-  if (m > 0 && tid == 0) red_release_add(&xbar[0], 1u);   // covers the plan's victim entries (after the barrier)
+  if (m > 0 && tid == 0) {
+    MOE_TL(g_ffn_timeline, 0, 28);
+    red_release_add(&xbar[0], 1u);   // covers the plan's victim entries (after the barrier)
+  }
   // commit: evicted keys leave the table before the misses enter it
   for (int j = tid; j < m; j += kThreads) {
     const int old = s_old[j];
@@ -405,6 +408,7 @@ __device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, i
   }
   __syncthreads();
   if (!s_flag) return false;
+  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 29);
   for (int j = tid; j < m; j += kThreads) {
     s_mslot[j] = __ldcg(&P->miss_slot[j]);
     s_mexp[j] = __ldcg(&P->miss_expert[j]);
@@ -430,6 +434,7 @@ __device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, i
     for (; c < per; c += nthr) dst[c] = src[c];
   }
   if (!cta_grid_barrier(&xbar[1], (uint32_t)GT, a.err, &s_flag)) return false;
+  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 30);
   // staging -> victim slots in the device block layout, one block per warp
   const int nb = (a.f / 32) * (a.d / 32) * 2 + (a.d / 32) * (a.f / 32);
   const int64_t nwarps = (int64_t)GT * (kThreads / 32);
@@ -439,7 +444,9 @@ __device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, i
     repack_block(a.staging + (int64_t)ex * a.expert_bytes, slots + (int64_t)s_mslot[ex] * a.expert_bytes, bi, a.d,
                  a.f, lane);
   }
-  return cta_grid_barrier(&xbar[2], (uint32_t)GT, a.err, &s_flag);
+  const bool ok = cta_grid_barrier(&xbar[2], (uint32_t)GT, a.err, &s_flag);
+  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 31);
+  return ok;
 }
 
 template <int NT, int MODE>
