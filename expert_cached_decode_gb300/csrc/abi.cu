@@ -593,6 +593,7 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.host_pool = c->host_pool_dev;
   fa.pool_entries = c->P;
   fa.staging = c->staging;
+  fa.staging_n = c->staging_n;
   return fa;
 }
 

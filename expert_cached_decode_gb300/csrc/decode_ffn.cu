@@ -401,6 +401,10 @@ __device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, i
   __shared__ int s_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Plan* P = a.plan;
+  if (m > a.staging_n) {   // cannot happen (m <= T*k and m <= E); never write past the staging slots
+    if (tid == 0) set_error(a.err, DEV_BAD_PLAN);
+    return false;
+  }
   if (tid == 0) {
     const bool ok = wait_flag_geq(&xbar[0], 1u);
     if (!ok) set_error(a.err, DEV_TIMEOUT_FLAG);

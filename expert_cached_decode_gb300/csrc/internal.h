@@ -138,7 +138,8 @@ struct FfnArgs {
   int C;
   const uint8_t* host_pool;     // device address of the registered host pool (canonical experts)
   int64_t pool_entries;         // key (layer, e) reads entry (layer*E + e) mod pool_entries
-  uint8_t* staging;             // [>= T*k][expert_bytes] canonical copies of this call's misses
+  uint8_t* staging;             // [staging_n][expert_bytes] canonical copies of this call's misses
+  int staging_n;
 };
 
 // decode kernel modes
