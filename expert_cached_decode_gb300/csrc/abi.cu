@@ -575,7 +575,7 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.max_exp = c->max_exp;
   fa.err = c->err;
   fa.grid = c->num_sms;
-  // fused routing (used when every key is resident)
+  // fused routing (every key resident, or misses pulled by the GPU)
   fa.wr = c->router_w + (size_t)layer * c->E * c->d;
   fa.bias = c->router_b + (size_t)layer * c->E;
   fa.logits = c->logits;

@@ -4,13 +4,17 @@
 //   g = Wg.x, u = Wu.x, h = silu(g) * u, o = Wd.h,
 //   y[t] = shared_weight * o_shared[t] + sum_i w[t,i] * o_idx[t,i][t].
 //
-// Fused routing (every key resident): the same launch first computes the
-// router logits (CTA c takes rows c, c + G, ...), passes a grid-wide arrival
-// counter, and then every CTA selects the experts of the call from the full
-// logits itself (the same selection as the routing kernel), so no second
-// kernel and no plan round trip separate routing from the expert work.  CTA 0
-// publishes the plan, stamps the hit slots and bumps the layer counters.
-// Otherwise the kernel follows the routing kernel and reads its plan.
+// Fused routing: the same launch first computes the router logits (CTA c
+// takes rows c, c + G, ...), passes a grid-wide arrival counter, and then
+// every CTA selects the experts of the call from the full logits itself (the
+// same selection as the routing kernel), so no second kernel and no plan
+// round trip separate routing from the expert work.  With every key resident
+// CTA 0 also takes tiles and publishes the plan, stamps and counters from
+// its h-loader warp.  With a cache that can miss, CTA 0 takes no tiles and
+// runs the cache (LRU victims, commit, next LRU order, plan), and CTAs
+// 1..G-1 pull the call's misses from the host pool into their victim slots
+// before the experts.  Otherwise (host-issued miss copies) the kernel
+// follows the routing kernel and reads its plan.
 //
 // Work is cut into tiles of contiguous bytes of the device block layout:
 //   gate/up tile (expert a, 32-row block rb of f): the Wg and Wu blocks of
@@ -19,16 +23,18 @@
 //     bumps h_ready[a];
 //   down tile (expert a, R consecutive 32-row blocks of d): R * f/32 Wd blocks
 //     (R = 2 at f = 768); it multiplies by h_a and writes o_a for its rows.
-// One persistent CTA per SM takes an even share of each phase: a contiguous
-// range of gate/up tiles, then a contiguous range of down tiles.  A producer
+// One persistent CTA per SM (but CTA 0 with a cache that can miss) takes an
+// even share of each phase: a contiguous range of gate/up tiles, then a
+// contiguous range of down tiles.  A producer
 // thread streams every tile through a ring of 16-block stages with bulk TMA
 // copies (mbarrier completion); an h-loader thread bulk-copies each expert's
 // h into shared memory once per CTA when it is ready.  All 8 consumer warps
-// work on every stage (2 blocks each): they expand the 3-bit codes to fp16 in
+// work on every gate/up stage (2 blocks each): they expand the 3-bit codes to fp16 in
 // registers and multiply on the tensor cores (mma.sync m16n8k16, fp32
-// accumulate, per-group scale in fp32), then hand each tile's partial sums
-// to a finalizer warp that adds them in a fixed order, writes h or o and
-// publishes it.  CTA c then combines the row blocks c, c + G, ... of y once
+// accumulate, per-group scale in fp32); in a down tile each warp sums one
+// row block.  They hand each tile's partial sums to a finalizer warp that
+// adds them in a fixed order, writes h or o and publishes it.  The tile CTA
+// of index c then combines the row blocks c, c + G, ... of y once
 // every expert's output there is written, in a fixed order (shared expert,
 // then routed experts in ascending id), so y is deterministic.  All waits are
 // bounded.

@@ -120,7 +120,7 @@ struct FfnArgs {
   int set_words, max_exp;
   uint32_t* err;
   int grid;
-  // fused routing (every key resident): router, slot table, LRU stamps, counters
+  // fused routing (kFusedResident, kFusedCached): router, slot table, LRU stamps, counters
   int fused;
   const uint16_t* wr;           // [E][d] bf16 (this layer)
   const float* bias;            // [E] (this layer)
