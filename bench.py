@@ -548,8 +548,7 @@ def run_gpu(args):
     st0 = layer.moe_cache_stats()
     cur = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clk = ClockSampler(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
-                                    f"clocks_rank{rank}.csv"))
+    clk = ClockSampler(os.path.join(os.environ.get("BENCH_LOG_DIR", "."), f"clocks_rank{rank}.csv"))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
