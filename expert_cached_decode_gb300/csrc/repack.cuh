@@ -25,8 +25,9 @@ __device__ __forceinline__ uint32_t field3(uint32_t w0, uint32_t w1, uint32_t w2
 // Block bi of the expert at `src` (canonical) into the expert at `dst`
 // (device layout); blocks 0 .. 2(f/32)(d/32)-1 are gate/up (row block, group,
 // Wg then Wu), the rest down (row block, group).  One whole warp calls it.
-__device__ __forceinline__ void repack_block(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int bi, int d,
-                                             int f, int lane) {
+// The source is read through L2 (it may have been written by other CTAs of
+// the same kernel).
+__device__ __forceinline__ void repack_block(const uint8_t* src, uint8_t* dst, int bi, int d, int f, int lane) {
   const int gu_blocks = (f / 32) * (d / 32) * 2;
   // canonical sections
   const int64_t gq = (int64_t)f * (d / 32) * 12, dq = (int64_t)d * (f / 32) * 12;
@@ -53,8 +54,8 @@ __device__ __forceinline__ void repack_block(const uint8_t* __restrict__ src, ui
   const int row = rb * 32 + lane;
   const int64_t g_index = (int64_t)row * (cols / 32) + gi;
   const uint32_t* gp = reinterpret_cast<const uint32_t*>(src + sec_q[mat] + g_index * 12);
-  const uint32_t r0 = gp[0], r1 = gp[1], r2 = gp[2];
-  const uint16_t my_scale = *reinterpret_cast<const uint16_t*>(src + sec_s[mat] + g_index * 2);
+  const uint32_t r0 = __ldcg(gp), r1 = __ldcg(gp + 1), r2 = __ldcg(gp + 2);
+  const uint16_t my_scale = __ldcg(reinterpret_cast<const unsigned short*>(src + sec_s[mat] + g_index * 2));
 
   const int g = lane >> 2, c = lane & 3;
   uint32_t W[3] = {0u, 0u, 0u};
