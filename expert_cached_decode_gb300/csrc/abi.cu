@@ -6,7 +6,12 @@
 //                        work); programmatic dependent launch lets it be
 //                        scheduled while the previous call drains.  No host
 //                        wait.
-//   otherwise          : route kernel (ROUTE_PLAN) -> the host reads the
+//   misses, GPU pull   : one launch of the decode kernel in its cached mode
+//   (default)            (CTA 0 plans and commits the cache, the other CTAs
+//                        pull the misses from the registered host pool into
+//                        their victim slots, then run the experts).  No host
+//                        wait.
+//   misses, host copies: route kernel (ROUTE_PLAN) -> the host reads the
 //                        miss list -> one cudaMemcpyAsync per miss (host pool
 //                        -> staging) on a side stream and a re-layout kernel
 //                        into the victim slots -> the main stream waits on
@@ -853,8 +858,11 @@ static moe_status check_device_error(moe_ctx* c) {
     CUDA_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
     CUDA_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
     CUDA_TRY(cudaDeviceSynchronize());
+    // with a cache that can miss, a call that gave up may have committed
+    // slots whose contents never arrived: the cache must be configured again
+    if (!c->all_resident) c->configured = false;
     return fail(e == DEV_NOT_RESIDENT ? MOE_ERR_STATE : MOE_ERR_TIMEOUT,
-                "device error %u (1: barrier wait, 2: flag wait, 3: key not resident)", e);
+                "device error %u (1: barrier wait, 2: flag wait, 3: key not resident, 4: bad plan)", e);
   }
   return MOE_OK;
 }

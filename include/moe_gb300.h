@@ -164,7 +164,10 @@ typedef enum { MOE_MISS_HOST_COPY = 0, MOE_MISS_DEVICE_PULL = 1 } moe_miss_mode;
 moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
 
 /* Wait for all work of the context and report a deferred device error
- * (MOE_ERR_TIMEOUT if a bounded device wait gave up). */
+ * (MOE_ERR_TIMEOUT if a bounded device wait gave up).  After a device error
+ * on a cache that can miss, the cache must be configured again
+ * (moe_forward returns MOE_ERR_STATE until then): a call that gave up may
+ * have committed slots whose contents never arrived. */
 moe_status moe_sync(moe_ctx* ctx);
 
 /* Counters (synchronises).  per_layer may be NULL or point to n_layers
