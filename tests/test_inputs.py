@@ -113,3 +113,13 @@ def test_margin_screen_agrees_with_fp64_on_large_batches():
     fast = s._small_gap(xs, wr64, b)
     exact = s._small_gap(xs, wr64, b, exact=True)
     assert np.array_equal(fast, exact)
+
+
+def test_token_draws_are_prefix_consistent():
+    # the verify-width sweep slices the widest draw: the first T rows of a
+    # T=7 draw equal the T-token draw (margin redraws are per token)
+    from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA
+    s = Synth(WORKLOADS[3], bias_lambda=BIAS_LAMBDA)
+    wide = s.tokens_many(2, [0, 5, 17], T=7)
+    for T in (1, 4):
+        assert np.array_equal(wide[:, :T], s.tokens_many(2, [0, 5, 17], T=T))
