@@ -98,3 +98,16 @@ def test_noalloc_router_rejects_null_pointers(lib):
     for args in ((None, a, a, a), (a, None, a, a), (a, a, None, a), (a, a, a, None)):
         x, wr, idx, w = args
         assert lib.moe_route_topk_noalloc(x, wr, None, 1, 2048, 512, 10, idx, w, None) == INVALID
+
+
+def test_create_without_a_device_fails_cleanly(lib):
+    # on a machine without a usable GPU the first CUDA call fails: the status
+    # is MOE_ERR_CUDA, the partial context is released, *out stays NULL
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    out = ctypes.c_void_p(12345)
+    st = lib.moe_layer_create(ctypes.byref(_desc()), ctypes.byref(out))
+    assert st == -3
+    assert out.value is None
+    assert "cuda" in lib.moe_last_error().decode().lower()
