@@ -18,10 +18,11 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "
 
 ENTRY_POINTS = ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                 "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_layer_destroy",
-                "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_last_error")
+                "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure", "moe_last_error")
 
 MOE_MISS_HOST_COPY = 0
 MOE_MISS_DEVICE_PULL = 1
+MOE_INJECT_MISS_COPY = 1
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -74,11 +75,12 @@ def load():
     L.moe_layer_destroy.restype = None
     L.moe_route_topk_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.moe_set_miss_mode.argtypes = [vp, i32]
+    L.moe_debug_inject_failure.argtypes = [i32, i64]
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     for name in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                  "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_route_topk_noalloc",
-                 "moe_set_miss_mode"):
+                 "moe_set_miss_mode", "moe_debug_inject_failure"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

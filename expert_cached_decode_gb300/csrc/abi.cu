@@ -129,6 +129,31 @@ struct moe_ctx {
 
 extern "C" const char* moe_last_error(void) { return g_last_error.c_str(); }
 
+// ---- host-side failure injection (test hook; disarmed by default) ---------
+static int g_inject_kind = 0;
+static int64_t g_inject_left = 0;
+
+// true (and disarmed) when this is the armed kind's nth event
+static bool injected(int kind) {
+  if (g_inject_kind != kind) return false;
+  if (--g_inject_left > 0) return false;
+  g_inject_kind = 0;
+  return true;
+}
+
+extern "C" moe_status moe_debug_inject_failure(int32_t kind, int64_t nth) {
+  if (kind == 0) {
+    g_inject_kind = 0;
+    return MOE_OK;
+  }
+  if (kind != MOE_INJECT_MISS_COPY || nth < 1)
+    return fail(MOE_ERR_INVALID_ARG, "moe_debug_inject_failure: unknown kind %d or nth %lld < 1", kind,
+                (long long)nth);
+  g_inject_kind = kind;
+  g_inject_left = nth;
+  return MOE_OK;
+}
+
 constexpr int kMaxPrefillT = 16384;
 
 // ---- TMA tensor maps (driver entry point fetched through the runtime) -----
@@ -796,6 +821,8 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   for (int j = 0; j < m; ++j) {
     const int64_t key = (int64_t)layer * c->E + p.miss_expert[j];
     const int64_t entry = key % c->P;
+    if (injected(MOE_INJECT_MISS_COPY))
+      return fail(MOE_ERR_CUDA, "injected failure: issue of miss copy %d of the layer-call", j);
     CUDA_TRY(cudaMemcpyAsync(c->staging + (size_t)j * c->B, c->host_pool + (size_t)entry * c->B, c->B,
                              cudaMemcpyHostToDevice, c->side));
   }

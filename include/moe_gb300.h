@@ -163,6 +163,14 @@ moe_status moe_forward(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t 
 typedef enum { MOE_MISS_HOST_COPY = 0, MOE_MISS_DEVICE_PULL = 1 } moe_miss_mode;
 moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
 
+/* Test hook: make the nth (>= 1) future event of `kind` fail once, then
+ * disarm; kind 0 disarms.  MOE_INJECT_MISS_COPY: the issue of a miss copy in
+ * the host-copy miss mode fails, so moe_forward returns MOE_ERR_CUDA before
+ * any cache state changes.  Process-wide, not thread-safe.  Errors:
+ * INVALID_ARG for an unknown kind or nth < 1. */
+enum { MOE_INJECT_MISS_COPY = 1 };
+moe_status moe_debug_inject_failure(int32_t kind, int64_t nth);
+
 /* Wait for all work of the context and report a deferred device error
  * (MOE_ERR_TIMEOUT if a bounded device wait gave up).  After a device error
  * on a cache that can miss, the cache must be configured again

@@ -111,3 +111,11 @@ def test_create_without_a_device_fails_cleanly(lib):
     assert st == -3
     assert out.value is None
     assert "cuda" in lib.moe_last_error().decode().lower()
+
+
+def test_failure_injection_hook_arguments(lib):
+    assert lib.moe_debug_inject_failure(7, 1) == INVALID
+    assert lib.moe_debug_inject_failure(_abi.MOE_INJECT_MISS_COPY, 0) == INVALID
+    assert "unknown kind" in lib.moe_last_error().decode()
+    assert lib.moe_debug_inject_failure(_abi.MOE_INJECT_MISS_COPY, 3) == 0
+    assert lib.moe_debug_inject_failure(0, 0) == 0        # disarm
