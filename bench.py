@@ -18,12 +18,16 @@ experts it runs (11 at T=1, counted from the cache statistics) x 2,064,384 B
 average per-call duration (one kernel launch per call), against the
 measured HBM copy bandwidth.  --tokens T runs verify batches of T tokens
 per call instead (value then counts all T tokens).
-cpu_baseline: the fp64 CPU oracle on a bounded sample of calls.
+cpu_baseline: the fp64 CPU oracle on a bounded sample of calls, on every
+host core (one process per core) and on one thread.
+prefill (by default at T=1 with the default call count; --no-prefill drops
+it): the 12,288-token chunk and the chunk-size sweep, expert FLOP rate
+against the measured bf16 tensor peak.
 
 --impl reference times the CPU oracle itself (the pages publish no code and
 no number for this step; the oracle is the only reference implementation).
---stack additionally runs the 48-layer verify stack (T=5) and --prefill the
-12,288-token chunk when the library supports it.
+--stack additionally runs the 48-layer verify and concurrent stacks,
+--stack-sweep the verify-width x cache-capacity sweep.
 """
 
 import argparse
@@ -39,6 +43,7 @@ sys.path.insert(0, ROOT)
 import numpy as np
 
 CALLS = 10_000
+DEFAULT_CALLS = CALLS
 EXPERT_BYTES = 2_064_384
 ROUTER_BYTES = 512 * 2048 * 2
 L2_BYTES = 129 * 1024 * 1024
@@ -657,7 +662,7 @@ def run_gpu(args):
             "clocks": clk.summary(local),
             "cache": {"token_hits": stats["token_hits"], "token_misses": stats["token_misses"]},
         }
-        if args.prefill:
+        if args.prefill and T == 1 and CALLS == DEFAULT_CALLS:
             try:
                 line["prefill"] = run_prefill(args.prefill_steps, 3)
             except Exception as ex:   # reported, not hidden
@@ -699,7 +704,9 @@ def main():
     ap.add_argument("--cpu-calls", type=int, default=12)
     ap.add_argument("--ref-calls", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--prefill", action="store_true", help="also time the 12,288-token prefill chunk and sweep")
+    ap.add_argument("--prefill", action="store_true", default=True,
+                    help="also time the 12,288-token prefill chunk and sweep (the default at T=1)")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--stack", action="store_true",
                     help="also run the 48-layer stacks (T=5 Zipf 1.1, T=16 Zipf 0.8) with the 8,445-slot cache")
