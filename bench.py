@@ -1,4 +1,4 @@
-"""Benchmark of the routed-expert FFN step on GB300 (one JSON line on rank 0).
+"""Benchmark of the routed-expert FFN step on one GB300 (one JSON line).
 
 Workload (N=1): one MoE layer at the pages' scale, single-stream decode:
 d=2048, f=768, 512 routed experts + 1 shared, top-10, 3-bit g32 experts
@@ -57,21 +57,6 @@ def _dist():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
-
-
-def reduce_max(value, dist, device):
-    """Max of a per-rank float over all ranks (identity without a process group)."""
-    if dist is None:
-        return float(value)
-    import torch
-    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_rate(units_per_rank, world_size, max_ms):
-    """Units of all ranks over the slowest rank's time (weak scaling)."""
-    return units_per_rank * world_size / (max_ms / 1e3)
 
 
 def peaks():
@@ -552,10 +537,6 @@ def run_gpu(args):
     import torch
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
-    dist = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
     CALLS = args.calls
     T = args.tokens
     s, layer, xs = build_decode_layer(CALLS, T=T)
@@ -589,8 +570,6 @@ def run_gpu(args):
     cur = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk = ClockSampler(os.path.join(os.environ.get("BENCH_LOG_DIR", "."), f"clocks_rank{rank}.csv"))
-    if dist:
-        dist.barrier()
     torch.cuda.synchronize()
     with clk:
         time.sleep(0.3)
@@ -599,16 +578,13 @@ def run_gpu(args):
             step()
         e1.record(cur)
         torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     ms = e0.elapsed_time(e1)
     layer.moe_sync()
     st1 = layer.moe_cache_stats()
     # distinct routed experts per call in the timed steps (+ the shared one)
     exp_per_call = 1.0 + (st1["distinct_hits"] - st0["distinct_hits"]) / max(1, st1["layer_calls"] - st0["layer_calls"])
     alg_bytes = exp_per_call * EXPERT_BYTES
-    ms = reduce_max(ms, dist, "cuda")
-    value = whole_job_rate(CALLS * T * args.steps, ws, ms)
+    value = CALLS * T * args.steps / (ms / 1e3)
     per_call_s = (ms / 1e3) / (CALLS * args.steps)
 
     # end to end: H2D of the step's inputs, the calls, D2H of the outputs
@@ -619,8 +595,6 @@ def run_gpu(args):
         graph.replay()
         y_host.copy_(y_dev, non_blocking=True)
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     e2.record(cur)
     for _ in range(args.steps):
         x_dev.copy_(x_host, non_blocking=True)
@@ -628,17 +602,15 @@ def run_gpu(args):
         y_host.copy_(y_dev, non_blocking=True)
     e3.record(cur)
     torch.cuda.synchronize()
-    ms_e2e = reduce_max(e2.elapsed_time(e3), dist, "cuda")
-    e2e_value = whole_job_rate(CALLS * T * args.steps, ws, ms_e2e)
-    if dist:
-        dist.barrier()
+    ms_e2e = e2.elapsed_time(e3)
+    e2e_value = CALLS * T * args.steps / (ms_e2e / 1e3)
     stats = layer.moe_cache_stats()
 
     if rank == 0:
         hbm, peak_kind = peaks()
         achieved = alg_bytes / per_call_s / 1e9
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma operands, f32 accumulate (3-bit weights)",
             "data": "synthetic",
@@ -648,7 +620,7 @@ def run_gpu(args):
                        "l2": "inputs larger than L2: 512 resident experts = 1.06 GB > 129 MB L2 "
                              "(the shared expert and the router stay L2-resident across calls)",
                        "graph": "10,000 moe_forward calls captured once, replayed per step",
-                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "parallelism": "single GPU",
                        "stack_tokens_per_s_derived": value / 48.0},
             "gpu_launches": CALLS * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -691,8 +663,6 @@ def run_gpu(args):
                                                    "sample": f"first {n} calls, 1 BLAS thread"}}
         print(json.dumps(line), flush=True)
     layer.close()
-    if dist:
-        dist.destroy_process_group()
 
 
 def main():
@@ -731,6 +701,10 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.gpus != 1 or _dist()[0] != 1:
+        # the step runs on one GPU by scope; there is no multi-GPU arm
+        print(f"bench.py: single GPU only (got --gpus {args.gpus}, WORLD_SIZE {_dist()[0]})", file=sys.stderr)
+        sys.exit(2)
     elif args.prefill_only:
         import torch
         torch.cuda.set_device(_dist()[2])

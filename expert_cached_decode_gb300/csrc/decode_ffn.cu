@@ -1091,14 +1091,9 @@ static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int gri
   if ((size_t)a.T * x_row_elems(a.d) * 2 >
       (size_t)kHSlots * NT * 8 * h_row_bytes(a.f) + (size_t)kCW * 32 * red_per_lane(NT) * 4)
     return cudaErrorInvalidValue;
-  // raise the dynamic shared-memory limit once per size (not during stream capture)
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  // the dynamic shared-memory limit, raised once per device
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_ffn_kernel<NT, MODE>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -14,6 +14,7 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kMaxPicks = kMaxDecodeT * kMaxTopK;   // 256
 constexpr int kMaxSlots = 1 << 17;                  // LRU scan bitmap bound
+constexpr int kMaxDevices = 64;                     // per-device launch state
 
 // Routing plan of one layer-call, written by the route kernel.
 struct Plan {
@@ -210,6 +211,10 @@ struct PrefillGemmArgs {
   int E, d, f;
   uint32_t* err;
 };
+
+// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
+// current device (once per device and kernel; thread-safe).
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
 
 // Records the thread-local message returned by moe_last_error().
 moe_status set_last_error(moe_status st, const char* fmt, ...);

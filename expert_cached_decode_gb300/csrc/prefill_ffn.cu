@@ -17,6 +17,8 @@
 // 128-byte-swizzled K-major operand tile; the token tile comes by TMA; one
 // thread issues tcgen05.mma into a double-buffered tensor-memory accumulator;
 // four epilogue warps read it back while the next tile accumulates.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -692,8 +694,14 @@ static size_t gemm_smem() {
 template <bool DOWN>
 static cudaError_t launch_gemm(const CUtensorMap& tmB, const CUtensorMap& tmB2, const PrefillGemmArgs& a,
                                cudaStream_t s, int num_sms) {
-  static bool configured = false;
-  static int grid = 0;
+  // the persistent grid (as many whole clusters as can be resident at once)
+  // is found once per device, after the shared-memory limit is raised there
+  static std::mutex mu;
+  static int grid_of[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   const size_t smem = gemm_smem<DOWN>();
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -706,19 +714,22 @@ static cudaError_t launch_gemm(const CUtensorMap& tmB, const CUtensorMap& tmB2, 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    // persistent grid: as many whole clusters as can be resident at once
-    cfg.gridDim = dim3(num_sms - num_sms % pg::CLUSTER);
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, prefill_gemm_kernel<DOWN>, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    grid = clusters * pg::CLUSTER;
-    if (grid > num_sms) grid = num_sms - num_sms % pg::CLUSTER;
-    configured = true;
+  int grid;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (grid_of[dev] == 0) {
+      e = ensure_dyn_smem(reinterpret_cast<const void*>(prefill_gemm_kernel<DOWN>), smem);
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3(num_sms - num_sms % pg::CLUSTER);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, prefill_gemm_kernel<DOWN>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (clusters < 1) return cudaErrorInvalidConfiguration;
+      int g = clusters * pg::CLUSTER;
+      if (g > num_sms) g = num_sms - num_sms % pg::CLUSTER;
+      grid_of[dev] = g;
+    }
+    grid = grid_of[dev];
   }
   cfg.gridDim = dim3(grid);
   return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<DOWN>, tmB, tmB2, a);

@@ -186,12 +186,8 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(PrefillTopkArgs a) {
 
 cudaError_t launch_router_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const RouterGemmArgs& a,
                                cudaStream_t s, int num_sms) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rg::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(router_gemm_kernel), rg::SMEM);
+  if (e != cudaSuccess) return e;
   const int n_tiles = ((a.E + rg::BM - 1) / rg::BM) * ((a.T + rg::BN - 1) / rg::BN);
   const int grid = n_tiles < num_sms ? n_tiles : num_sms;
   router_gemm_kernel<<<grid, rg::THREADS, rg::SMEM, s>>>(tmA, tmB, a);

@@ -278,13 +278,8 @@ extern "C" int moe_debug_timeline_route(unsigned long long* out) {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   // the selection scratch (and the staged LRU order) is dynamic shared
   // memory (static + dynamic > 48 KB)
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kSelBytes + (size_t)kRouteQSmem * 4));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(route_kernel), kSelBytes + (size_t)kRouteQSmem * 4);
+  if (e != cudaSuccess) return e;
   const size_t dyn = kSelBytes + (a.mode == ROUTE_PLAN && a.C <= kRouteQSmem ? (size_t)a.C * 4 : 0);
   const int grid = (a.E + kRouteWarps - 1) / kRouteWarps;
   route_kernel<<<grid, kRouteThreads, dyn, s>>>(a);

@@ -118,7 +118,10 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x
 
 // 2-D tiled load multicast to the CTAs of `cta_mask` in this cluster: the
 // box lands at the same shared-memory offset in each and completes bytes on
-// the mbarrier at the same offset in each.
+// the mbarrier at the same offset in each.  Two rules for its callers: the
+// tensor map must describe a buffer of this GPU's own memory that the library
+// owns (never a peer GPU's or a caller's mapping), and the code that issues it
+// runs only in single-GPU processes (the library has no multi-GPU path).
 __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
                                                       uint16_t cta_mask) {
   asm volatile(

@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from moe_inputs import synth
+from moe_inputs import synth, bf16_bits_to_f64
+from oracle.routing import route
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +52,37 @@ def test_noalloc_route_matches_context_route(cfg, T1, T2):
         torch.cuda.synchronize()
         assert torch.equal(idx, idx_ref), f"call {call}"
         assert (w - w_ref).abs().max().item() <= 1e-5, f"call {call}"
+        # and against the fp64 oracle, which shares no code with either path
+        _, wr64, b64 = s.router(0)
+        oi, ow, _ = route(bf16_bits_to_f64(xb), wr64, b64, k)
+        assert np.array_equal(idx.cpu().numpy(), oi), f"call {call}"
+        assert np.abs(w.cpu().numpy() - ow).max() <= 1e-5, f"call {call}"
     layer.close()
+
+
+def test_noalloc_route_allocates_nothing():
+    # After a first call (which may load the library's module and with it
+    # the fixed scratch array), further calls change neither the device's
+    # free memory nor torch's allocation count.
+    from expert_cached_decode_gb300.layer import moe_route_topk_noalloc
+    s = synth(2)
+    wl = s.wl
+    wr, _, b = s.router(0)
+    wr_dev = torch.from_numpy(wr.view(np.int16)).view(torch.bfloat16).cuda()
+    b_dev = torch.from_numpy(b).cuda()
+    xb = s.tokens_many(0, [57], T=4)[0]
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    idx = torch.empty((4, wl.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((4, wl.top_k), dtype=torch.float32, device="cuda")
+    moe_route_topk_noalloc(x, wr_dev, b_dev, wl.top_k, idx, w)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    n0 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    for _ in range(3):
+        moe_route_topk_noalloc(x, wr_dev, b_dev, wl.top_k, idx, w)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == n0
 
 
 def test_noalloc_route_without_bias_and_size_limits():
