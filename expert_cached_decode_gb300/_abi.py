@@ -18,11 +18,15 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "
 
 ENTRY_POINTS = ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                 "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_layer_destroy",
-                "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure", "moe_last_error")
+                "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure",
+                "moe_debug_set_wait_limit", "moe_last_error")
 
 MOE_MISS_HOST_COPY = 0
 MOE_MISS_DEVICE_PULL = 1
 MOE_INJECT_MISS_COPY = 1
+MOE_INJECT_HOLD_ROUTER = 2
+MOE_INJECT_HOST_REGISTER = 3
+MOE_INJECT_DEVICE_ALLOC = 4
 
 
 class MoeLayerDesc(ctypes.Structure):
@@ -76,11 +80,12 @@ def load():
     L.moe_route_topk_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.moe_set_miss_mode.argtypes = [vp, i32]
     L.moe_debug_inject_failure.argtypes = [i32, i64]
+    L.moe_debug_set_wait_limit.argtypes = [vp, i64]
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     for name in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                  "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_route_topk_noalloc",
-                 "moe_set_miss_mode", "moe_debug_inject_failure"):
+                 "moe_set_miss_mode", "moe_debug_inject_failure", "moe_debug_set_wait_limit"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

@@ -97,13 +97,12 @@ struct moe_ctx {
   uint32_t* route_cnt = nullptr;
   Plan* plan = nullptr;
   Plan* plan_host = nullptr;  // pinned
-  uint16_t* hbuf = nullptr;      // [max_exp][16][f] fp16
-  float* obuf = nullptr;
-  uint32_t* counters = nullptr;  // decode calls | 2 sets of (h_ready | d_cnt | gbar)
+  float* ypart = nullptr;        // [num_sms][16][d] per-CTA partials of y
+  uint32_t* counters = nullptr;  // decode calls | 2 sets of kDecodeSetWords counters
   size_t counters_n = 0;
   int set_words = 0;
   uint32_t* err = nullptr;
-  int max_exp = 0;
+  uint64_t wait_ns = kWaitLimitNs;   // limit of every bounded device wait
   // prefill scratch (allocated on first use, sized for kMaxPrefillT tokens)
   float* p_logits = nullptr;
   int32_t* p_idx = nullptr;
@@ -146,12 +145,27 @@ extern "C" moe_status moe_debug_inject_failure(int32_t kind, int64_t nth) {
     g_inject_kind = 0;
     return MOE_OK;
   }
-  if (kind != MOE_INJECT_MISS_COPY || nth < 1)
+  if ((kind != MOE_INJECT_MISS_COPY && kind != MOE_INJECT_HOLD_ROUTER && kind != MOE_INJECT_HOST_REGISTER &&
+       kind != MOE_INJECT_DEVICE_ALLOC) ||
+      nth < 1)
     return fail(MOE_ERR_INVALID_ARG, "moe_debug_inject_failure: unknown kind %d or nth %lld < 1", kind,
                 (long long)nth);
   g_inject_kind = kind;
   g_inject_left = nth;
   return MOE_OK;
+}
+
+extern "C" moe_status moe_debug_set_wait_limit(moe_ctx* c, int64_t ns) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "NULL context");
+  if (ns <= 0) return fail(MOE_ERR_INVALID_ARG, "wait limit must be positive (got %lld ns)", (long long)ns);
+  c->wait_ns = (uint64_t)ns;
+  return MOE_OK;
+}
+
+// device allocation of create/configure (fails on an armed injection)
+static cudaError_t dev_alloc(void* p, size_t bytes) {
+  if (injected(MOE_INJECT_DEVICE_ALLOC)) return cudaErrorMemoryAllocation;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
 }
 
 constexpr int kMaxPrefillT = 16384;
@@ -200,15 +214,24 @@ static bool is_device_ptr(const void* p) {
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
 
+// frees the device buffers it holds when it goes out of scope
+struct DevTemp {
+  void* p[4] = {nullptr, nullptr, nullptr, nullptr};
+  ~DevTemp() {
+    for (void* q : p) cudaFree(q);
+  }
+};
+
 static moe_status repack_from(moe_ctx* c, const uint8_t* src_canonical, bool src_on_device, int n,
                               uint8_t* dst_base, const int32_t* dst_slot_host, int64_t dst_stride) {
   // copies n canonical experts (host or device) through a device staging
   // buffer and re-lays them out into dst (by slot index or contiguous)
   const int chunk = 32;
-  uint8_t* stage = nullptr;
-  int32_t* slots_dev = nullptr;
-  CUDA_TRY(cudaMalloc(&stage, (size_t)chunk * c->B));
-  CUDA_TRY(cudaMalloc(&slots_dev, chunk * sizeof(int32_t)));
+  DevTemp tmp;
+  CUDA_TRY(dev_alloc(&tmp.p[0], (size_t)chunk * c->B));
+  CUDA_TRY(dev_alloc(&tmp.p[1], chunk * sizeof(int32_t)));
+  uint8_t* stage = static_cast<uint8_t*>(tmp.p[0]);
+  int32_t* slots_dev = static_cast<int32_t*>(tmp.p[1]);
   for (int i0 = 0; i0 < n; i0 += chunk) {
     const int m = n - i0 < chunk ? n - i0 : chunk;
     CUDA_TRY(cudaMemcpy(stage, src_canonical + (size_t)i0 * c->B, (size_t)m * c->B,
@@ -231,8 +254,6 @@ static moe_status repack_from(moe_ctx* c, const uint8_t* src_canonical, bool src
     CUDA_TRY(launch_repack(ra, 0));
     CUDA_TRY(cudaDeviceSynchronize());
   }
-  cudaFree(stage);
-  cudaFree(slots_dev);
   return MOE_OK;
 }
 
@@ -241,7 +262,8 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   *out = nullptr;
   const moe_layer_desc& D = *desc;
   if (D.group != 32) return fail(MOE_ERR_UNIMPLEMENTED, "group must be 32 (got %d)", D.group);
-  if (D.d <= 0 || D.d % 256 != 0) return fail(MOE_ERR_UNIMPLEMENTED, "d must be a positive multiple of 256");
+  if (D.d <= 0 || D.d % 256 != 0 || D.d > 2048)
+    return fail(MOE_ERR_UNIMPLEMENTED, "d must be a positive multiple of 256, at most 2048");
   if (D.f <= 0 || D.f % 64 != 0 || D.f > 1024)
     return fail(MOE_ERR_UNIMPLEMENTED, "f must be a multiple of 64 in [64, 1024]");
   if (D.top_k < 2 || D.top_k > kMaxTopK || D.n_experts <= D.top_k || D.n_experts > kMaxE)
@@ -274,15 +296,25 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   } while (0)
   CREATE_TRY(cudaGetDevice(&c->device));
   CREATE_TRY(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+  {
+    // the decode kernel runs one CTA per SM and its grid-wide counters need
+    // all of them resident at once
+    bool fits = false;
+    CREATE_TRY(decode_ffn_fits(c->d, &fits));
+    if (!fits) {
+      moe_layer_destroy(c);
+      return fail(MOE_ERR_UNIMPLEMENTED, "the decode kernel does not fit one CTA per SM at d=%d", D.d);
+    }
+  }
   const size_t LE = (size_t)c->L * c->E;
-  CREATE_TRY(cudaMalloc(&c->router_w, LE * c->d * sizeof(uint16_t)));
+  CREATE_TRY(dev_alloc(&c->router_w, LE * c->d * sizeof(uint16_t)));
   CREATE_TRY(cudaMemcpy(c->router_w, D.router_w, LE * c->d * sizeof(uint16_t), cudaMemcpyDefault));
-  CREATE_TRY(cudaMalloc(&c->router_b, LE * sizeof(float)));
+  CREATE_TRY(dev_alloc(&c->router_b, LE * sizeof(float)));
   if (D.router_b)
     CREATE_TRY(cudaMemcpy(c->router_b, D.router_b, LE * sizeof(float), cudaMemcpyDefault));
   else
     CREATE_TRY(cudaMemset(c->router_b, 0, LE * sizeof(float)));
-  CREATE_TRY(cudaMalloc(&c->shared, (size_t)c->L * c->B));
+  CREATE_TRY(dev_alloc(&c->shared, (size_t)c->L * c->B));
   st = repack_from(c, static_cast<const uint8_t*>(D.shared_q), is_device_ptr(D.shared_q), c->L, c->shared,
                    nullptr, c->B);
   if (st != MOE_OK) {
@@ -295,7 +327,9 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
     cudaError_t e = cudaPointerGetAttributes(&at, D.host_pool);
     if (e != cudaSuccess) cudaGetLastError();
     if (e != cudaSuccess || at.type == cudaMemoryTypeUnregistered) {
-      e = cudaHostRegister(const_cast<void*>(D.host_pool), (size_t)c->P * c->B, cudaHostRegisterDefault);
+      e = injected(MOE_INJECT_HOST_REGISTER)
+              ? cudaErrorMemoryAllocation
+              : cudaHostRegister(const_cast<void*>(D.host_pool), (size_t)c->P * c->B, cudaHostRegisterDefault);
       if (e != cudaSuccess) {
         cudaGetLastError();
         moe_layer_destroy(c);
@@ -317,28 +351,26 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
     }
   }
   // scratch
-  c->max_exp = (kMaxDecodeT * c->k < c->E ? kMaxDecodeT * c->k : c->E) + 1;
-  CREATE_TRY(cudaMalloc(&c->logits, (size_t)kMaxDecodeT * c->E * sizeof(float)));
-  CREATE_TRY(cudaMalloc(&c->route_cnt, sizeof(uint32_t)));
+  CREATE_TRY(dev_alloc(&c->logits, (size_t)kMaxDecodeT * c->E * sizeof(float)));
+  CREATE_TRY(dev_alloc(&c->route_cnt, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
-  CREATE_TRY(cudaMalloc(&c->plan, sizeof(Plan)));
+  CREATE_TRY(dev_alloc(&c->plan, sizeof(Plan)));
   CREATE_TRY(cudaMemset(c->plan, 0, sizeof(Plan)));
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
-  CREATE_TRY(cudaMalloc(&c->hbuf, (size_t)c->max_exp * kMaxDecodeT * c->f * sizeof(uint16_t)));
-  CREATE_TRY(cudaMalloc(&c->obuf, (size_t)c->max_exp * kMaxDecodeT * c->d * sizeof(float)));
-  // h_ready[max_exp] | router barrier | d_cnt[d/32] | cache-mode flags:
-  // victims published, misses pulled, misses placed
-  c->set_words = c->max_exp + 1 + c->d / 32 + 3;
+  CREATE_TRY(dev_alloc(&c->ypart, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(float)));
+  // router counter | partials counter | cache-mode flags: victims published,
+  // misses pulled, misses placed
+  c->set_words = kDecodeSetWords;
   c->counters_n = 1 + 2 * (size_t)c->set_words;
-  CREATE_TRY(cudaMalloc(&c->counters, c->counters_n * sizeof(uint32_t)));
+  CREATE_TRY(dev_alloc(&c->counters, c->counters_n * sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
-  CREATE_TRY(cudaMalloc(&c->err, sizeof(uint32_t)));
+  CREATE_TRY(dev_alloc(&c->err, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->err, 0, sizeof(uint32_t)));
-  CREATE_TRY(cudaMalloc(&c->clock, sizeof(int64_t)));
+  CREATE_TRY(dev_alloc(&c->clock, sizeof(int64_t)));
   CREATE_TRY(cudaMemset(c->clock, 0, sizeof(int64_t)));
-  CREATE_TRY(cudaMalloc(&c->stats, (size_t)c->L * ST_N * sizeof(int64_t)));
+  CREATE_TRY(dev_alloc(&c->stats, (size_t)c->L * ST_N * sizeof(int64_t)));
   CREATE_TRY(cudaMemset(c->stats, 0, (size_t)c->L * ST_N * sizeof(int64_t)));
-  CREATE_TRY(cudaMalloc(&c->table, LE * sizeof(int32_t)));
+  CREATE_TRY(dev_alloc(&c->table, LE * sizeof(int32_t)));
   CREATE_TRY(cudaMemset(c->table, 0xff, LE * sizeof(int32_t)));
   CREATE_TRY(cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking));
   CREATE_TRY(cudaEventCreateWithFlags(&c->ev_route, cudaEventDisableTiming));
@@ -367,8 +399,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->route_cnt);
   cudaFree(c->plan);
   if (c->plan_host) cudaFreeHost(c->plan_host);
-  cudaFree(c->hbuf);
-  cudaFree(c->obuf);
+  cudaFree(c->ypart);
   cudaFree(c->counters);
   cudaFree(c->err);
   cudaFree(c->staging);
@@ -408,29 +439,54 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
       return fail(MOE_ERR_INVALID_ARG, "preload keys must be strictly ascending in [0, L*E)");
   }
   CUDA_TRY(cudaDeviceSynchronize());
+  // Every buffer of the new cache is allocated before the old one is
+  // released: when an allocation fails the context keeps its previous cache
+  // (slots, LRU state, counters) unchanged.
+  const bool all_res = (n_pre == LE);
+  const int staging_n = all_res ? 0 : (int)min_cap;
+  const int chunk = 32;
+  struct {
+    void* p[8] = {};
+  } nw;
+  auto free_new = [&]() {
+    for (void*& q : nw.p) {
+      cudaFree(q);
+      q = nullptr;
+    }
+  };
+  const size_t sizes[8] = {(size_t)capacity * c->B, capacity * sizeof(int32_t), capacity * sizeof(int64_t),
+                           capacity * sizeof(int32_t), capacity * sizeof(int32_t), (size_t)staging_n * c->B,
+                           (size_t)chunk * c->B, chunk * sizeof(int32_t)};
+  for (int i = 0; i < 8; ++i) {
+    if (sizes[i] == 0) continue;
+    cudaError_t e = dev_alloc(&nw.p[i], sizes[i]);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      free_new();
+      return fail(e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA,
+                  "moe_cache_configure: allocation of %zu bytes failed (%s); the previous cache is unchanged",
+                  sizes[i], cudaGetErrorString(e));
+    }
+  }
   cudaFree(c->slots);
   cudaFree(c->owner);
   cudaFree(c->stamp);
   cudaFree(c->lruq[0]);
   cudaFree(c->lruq[1]);
   cudaFree(c->staging);
-  c->slots = nullptr;
-  c->owner = nullptr;
-  c->stamp = nullptr;
-  c->lruq[0] = c->lruq[1] = nullptr;
-  c->staging = nullptr;
-  c->configured = false;
-  CUDA_TRY(cudaMalloc(&c->slots, (size_t)capacity * c->B));
-  CUDA_TRY(cudaMalloc(&c->owner, capacity * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->stamp, capacity * sizeof(int64_t)));
-  CUDA_TRY(cudaMalloc(&c->lruq[0], capacity * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->lruq[1], capacity * sizeof(int32_t)));
+  c->slots = static_cast<uint8_t*>(nw.p[0]);
+  c->owner = static_cast<int32_t*>(nw.p[1]);
+  c->stamp = static_cast<int64_t*>(nw.p[2]);
+  c->lruq[0] = static_cast<int32_t*>(nw.p[3]);
+  c->lruq[1] = static_cast<int32_t*>(nw.p[4]);
+  c->staging = static_cast<uint8_t*>(nw.p[5]);
+  DevTemp tmp;   // the preload's staging buffers, freed on every return below
+  tmp.p[0] = nw.p[6];
+  tmp.p[1] = nw.p[7];
+  c->configured = false;   // until the new cache is filled
   c->C = capacity;
-  c->all_resident = (n_pre == LE);
-  if (!c->all_resident) {
-    c->staging_n = (int)min_cap;
-    CUDA_TRY(cudaMalloc(&c->staging, (size_t)c->staging_n * c->B));
-  }
+  c->all_resident = all_res;
+  c->staging_n = staging_n;
   std::vector<int32_t> owner(capacity, -1), q(capacity), table(LE, -1);
   std::vector<int64_t> stamp(capacity, -1);
   for (int64_t s = 0; s < capacity; ++s) q[s] = (int32_t)s;
@@ -446,12 +502,9 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
   CUDA_TRY(cudaMemset(c->clock, 0, sizeof(int64_t)));
   CUDA_TRY(cudaMemset(c->stats, 0, (size_t)c->L * ST_N * sizeof(int64_t)));
   // preload: gather the canonical experts of the keys (pool entry key mod P)
-  const int chunk = 32;
   std::vector<int32_t> slot_ids(chunk);
-  uint8_t* stage = nullptr;
-  int32_t* slots_dev = nullptr;
-  CUDA_TRY(cudaMalloc(&stage, (size_t)chunk * c->B));
-  CUDA_TRY(cudaMalloc(&slots_dev, chunk * sizeof(int32_t)));
+  uint8_t* stage = static_cast<uint8_t*>(tmp.p[0]);
+  int32_t* slots_dev = static_cast<int32_t*>(tmp.p[1]);
   for (int64_t i0 = 0; i0 < n_pre; i0 += chunk) {
     const int m = (int)(n_pre - i0 < chunk ? n_pre - i0 : chunk);
     for (int j = 0; j < m; ++j) {
@@ -473,8 +526,6 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
     CUDA_TRY(launch_repack(ra, 0));
     CUDA_TRY(cudaDeviceSynchronize());
   }
-  cudaFree(stage);
-  cudaFree(slots_dev);
   CUDA_TRY(cudaDeviceSynchronize());
   c->configured = true;
   return MOE_OK;
@@ -515,30 +566,56 @@ static RouteArgs route_args(moe_ctx* c, int layer, const void* x, int T, int mod
   return ra;
 }
 
+// allocates every buffer of `specs` or none: on a failure the ones already
+// allocated are released and the targets stay NULL
+struct AllocSpec {
+  void** target;
+  size_t bytes;
+};
+static moe_status alloc_all(const AllocSpec* specs, int n) {
+  for (int i = 0; i < n; ++i) {
+    void* p = nullptr;
+    cudaError_t e = dev_alloc(&p, specs[i].bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      for (int j = 0; j < i; ++j) {
+        cudaFree(*specs[j].target);
+        *specs[j].target = nullptr;
+      }
+      return fail(e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "allocation of %zu bytes failed: %s",
+                  specs[i].bytes, cudaGetErrorString(e));
+    }
+    *specs[i].target = p;
+  }
+  return MOE_OK;
+}
+
 static moe_status ensure_prefill_scratch(moe_ctx* c) {
   if (c->p_logits) return MOE_OK;
-  CUDA_TRY(cudaMalloc(&c->p_logits, (size_t)kMaxPrefillT * c->E * sizeof(float)));
-  CUDA_TRY(cudaMalloc(&c->p_idx, (size_t)kMaxPrefillT * c->k * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->p_w, (size_t)kMaxPrefillT * c->k * sizeof(float)));
-  CUDA_TRY(cudaMalloc(&c->p_counts, (size_t)(c->E + 1) * sizeof(int32_t)));
-  return MOE_OK;
+  const AllocSpec specs[] = {
+      {reinterpret_cast<void**>(&c->p_logits), (size_t)kMaxPrefillT * c->E * sizeof(float)},
+      {reinterpret_cast<void**>(&c->p_idx), (size_t)kMaxPrefillT * c->k * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_w), (size_t)kMaxPrefillT * c->k * sizeof(float)},
+      {reinterpret_cast<void**>(&c->p_counts), (size_t)(c->E + 1) * sizeof(int32_t)}};
+  return alloc_all(specs, 4);
 }
 
 static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
   if (c->p_xg) return MOE_OK;
   const int64_t rows = (int64_t)kMaxPrefillT * (c->k + 1);
   c->p_max_tiles = (int64_t)(c->E + 1 + (rows + kPrefillBN - 1) / kPrefillBN);
-  CUDA_TRY(cudaMalloc(&c->p_xg, (size_t)rows * c->d * sizeof(uint16_t)));
-  CUDA_TRY(cudaMalloc(&c->p_hg, (size_t)rows * c->f * sizeof(uint16_t)));
-  CUDA_TRY(cudaMalloc(&c->p_hg_lo, (size_t)rows * c->f * sizeof(uint16_t)));
-  CUDA_TRY(cudaMalloc(&c->p_perm, (size_t)rows * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->p_wsort, (size_t)rows * sizeof(float)));
-  CUDA_TRY(cudaMalloc(&c->p_cursor, (size_t)c->E * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->p_group_slot, (size_t)(c->E + 1) * sizeof(int32_t)));
-  CUDA_TRY(cudaMalloc(&c->p_tiles_gu, (size_t)c->p_max_tiles * (c->f / 64) * sizeof(PrefillTile)));
-  CUDA_TRY(cudaMalloc(&c->p_tiles_dn, (size_t)c->p_max_tiles * (c->d / 128) * sizeof(PrefillTile)));
-  CUDA_TRY(cudaMalloc(&c->p_ntiles, 2 * sizeof(int32_t)));
-  return MOE_OK;
+  const AllocSpec specs[] = {
+      {reinterpret_cast<void**>(&c->p_xg), (size_t)rows * c->d * sizeof(uint16_t)},
+      {reinterpret_cast<void**>(&c->p_hg), (size_t)rows * c->f * sizeof(uint16_t)},
+      {reinterpret_cast<void**>(&c->p_hg_lo), (size_t)rows * c->f * sizeof(uint16_t)},
+      {reinterpret_cast<void**>(&c->p_perm), (size_t)rows * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_wsort), (size_t)rows * sizeof(float)},
+      {reinterpret_cast<void**>(&c->p_cursor), (size_t)c->E * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_group_slot), (size_t)(c->E + 1) * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_tiles_gu), (size_t)c->p_max_tiles * (c->f / 64) * sizeof(PrefillTile)},
+      {reinterpret_cast<void**>(&c->p_tiles_dn), (size_t)c->p_max_tiles * (c->d / 128) * sizeof(PrefillTile)},
+      {reinterpret_cast<void**>(&c->p_ntiles), 2 * sizeof(int32_t)}};
+  return alloc_all(specs, 10);
 }
 
 // Router logits (tcgen05) + top-k for T tokens; idx/w device outputs.
@@ -598,11 +675,10 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.k = c->k;
   fa.shared_weight = c->shared_weight;
   fa.plan = c->plan;
-  fa.hbuf = c->hbuf;
-  fa.obuf = c->obuf;
+  fa.ypart = c->ypart;
   fa.counters = c->counters;
   fa.set_words = c->set_words;
-  fa.max_exp = c->max_exp;
+  fa.wait_ns = c->wait_ns;
   fa.err = c->err;
   fa.grid = c->num_sms;
   // fused routing (every key resident, or misses pulled by the GPU)
@@ -753,6 +829,8 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
   if (T > kMaxDecodeT) return prefill_forward(c, layer, x, T, y, s, trace);
   if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
   FfnArgs fa = ffn_args(c, layer, x, T, y);
+  // test hook: CTA 0 of this call holds back its router arrival (fused routing)
+  fa.dbg_hold_router = injected(MOE_INJECT_HOLD_ROUTER) ? 1 : 0;
   if (c->all_resident) {
     fa.fused = 1;
     CUDA_TRY(launch_decode_ffn(fa, s, true));

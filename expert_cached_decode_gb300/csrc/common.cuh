@@ -77,12 +77,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier; false if the wait gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier; false if the wait gave up after
+// `limit_ns` of %globaltimer.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -124,17 +125,20 @@ __device__ __forceinline__ uint32_t ld_acquire_cta_u32(const uint32_t* p) {
   return v;
 }
 
-// Wait until *flag >= target (acquire); false if the wait gave up.
-__device__ __forceinline__ bool wait_flag_geq(const uint32_t* flag, uint32_t target) {
+// Wait until *flag >= target (acquire); false if the wait gave up after
+// `limit_ns` of %globaltimer.  The first polls run back to back (a grid
+// barrier usually completes within a few hundred nanoseconds).
+__device__ __forceinline__ bool wait_flag_geq(const uint32_t* flag, uint32_t target,
+                                              uint64_t limit_ns = kWaitLimitNs) {
   if (ld_acquire_u32(flag) >= target) return true;
   const uint64_t t0 = globaltimer();
+  int spins = 0;
   while (ld_acquire_u32(flag) < target) {
-    __nanosleep(64);
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (++spins > 64) __nanosleep(32);
+    if (globaltimer() - t0 > limit_ns) return false;
   }
   return true;
 }
-
 
 // orders this thread's earlier generic-proxy shared-memory accesses (and
 // those it synchronised with) before its later async-proxy (TMA) accesses
@@ -145,6 +149,36 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // named barrier among `count` threads (multiple of 32)
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// arrival on a named barrier without waiting (the waiting side uses named_bar)
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// named barrier that also counts the threads whose `pred` is true
+__device__ __forceinline__ int named_bar_count(int id, int count, bool pred) {
+  int n;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, %2, %3, p;\n\t}"
+      : "=r"(n)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return n;
+}
+
+// Barrier of the `nth` threads that run a block-level step: the whole CTA
+// (__syncthreads) when nth is 0, else named barrier 1 among nth threads.
+template <int NTH>
+__device__ __forceinline__ void step_bar() {
+  if constexpr (NTH == 0) __syncthreads();
+  else named_bar(1, NTH);
+}
+template <int NTH>
+__device__ __forceinline__ int step_bar_count(bool pred) {
+  if constexpr (NTH == 0) return __syncthreads_count(pred);
+  else return named_bar_count(1, NTH, pred);
 }
 
 // --------------------------------------------- programmatic dependent launch
@@ -194,8 +228,10 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
 //   bytes [384, 448): fp16 scales, row-group g8 (0..7) at 384 + 8*g8 holding
 //     the scales of rows g8, g8+8, g8+16, g8+24.
 // Section order in a slot: gate/up part, for row-block rb (f/32) and group gi
-// (d/32): the Wg block then the Wu block; then the down part, for row-block
-// rb (d/32) and group gi (f/32): the Wd block.
+// (d/32): the Wg block then the Wu block; then the down part, for input
+// group gi (f/32) and row-block rb (d/32): the Wd block.  So the gate/up
+// rows of one 32-row slice of f and the down columns of the same slice are
+// two contiguous runs of bytes.
 constexpr int kBlockBytes = 448;
 constexpr int kBlockCodeBytes = 384;
 
@@ -203,7 +239,7 @@ __host__ __device__ __forceinline__ int64_t gu_block_offset(int rb, int gi, int 
   return ((int64_t)(rb * (d / 32) + gi) * 2 + mat) * kBlockBytes;
 }
 __host__ __device__ __forceinline__ int64_t down_block_offset(int rb, int gi, int d, int f) {
-  return (int64_t)(f / 32) * (d / 32) * 2 * kBlockBytes + (int64_t)(rb * (f / 32) + gi) * kBlockBytes;
+  return (int64_t)(f / 32) * (d / 32) * 2 * kBlockBytes + (int64_t)(gi * (d / 32) + rb) * kBlockBytes;
 }
 
 // fp16 constants of the code -> value conversion (see dequant_block)

@@ -110,17 +110,19 @@ struct FfnArgs {
   int T, d, f, k;
   float shared_weight;
   Plan* plan;                   // read (after the routing kernel) or written (fused routing)
-  uint16_t* hbuf;               // [max_exp][T][f] fp16 h of each expert
-  float* obuf;                  // [max_exp][T][d] fp32 output of each expert
+  float* ypart;                 // [grid][T][d] per-CTA partials of y
   // per-call counters: word 0 counts decode calls; then two sets of
-  // set_words words (h_ready[max_exp] | router barrier | d_cnt[d/32]), used by
-  // alternate calls.  A call uses set (calls before it) & 1, and the set of
-  // the call before it is zeroed during the call (by the fused kernel's CTA 0,
-  // or by the commit kernel on the miss path).
+  // set_words words (router counter | partials counter | cache-mode flags:
+  // victims published, misses pulled, misses placed), used by alternate
+  // calls.  A call uses set (calls before it) & 1, and the set of the call
+  // before it is zeroed during the call (by the fused kernel's CTA 0, or by
+  // the commit kernel on the host-copy miss path).
   uint32_t* counters;
-  int set_words, max_exp;
+  int set_words;
   uint32_t* err;
   int grid;
+  uint64_t wait_ns;             // limit of every bounded device wait
+  int dbg_hold_router;          // test hook: CTA 0 never arrives on the router counter
   // fused routing (kFusedResident, kFusedCached): router, slot table, LRU stamps, counters
   int fused;
   const uint16_t* wr;           // [E][d] bf16 (this layer)
@@ -142,6 +144,9 @@ struct FfnArgs {
   uint8_t* staging;             // [staging_n][expert_bytes] canonical copies of this call's misses
   int staging_n;
 };
+
+// words of one per-call counter set of the decode kernel
+constexpr int kDecodeSetWords = 5;
 
 // decode kernel modes
 enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2 };
@@ -239,5 +244,7 @@ cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs
 cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
                                 cudaStream_t s, int grid);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
+// whether one CTA of every decode-kernel variant fits on an SM at hidden size d
+cudaError_t decode_ffn_fits(int d, bool* fits);
 
 }  // namespace moe

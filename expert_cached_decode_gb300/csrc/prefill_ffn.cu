@@ -258,10 +258,10 @@ __device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lan
 // accumulator of 256 columns carries g and u side by side in tensor-memory
 // lanes, and two accumulators (double buffer) fit the 512 columns; the SwiGLU
 // epilogue writes Hg.  DOWN = true: 128 rows of Wd, weighted atomic combine
-// into y.  Producer warp p expands, for every k block of parity p/4, the two
-// blocks of its 32-row band p%4 (gate/up: band b is row block 2m + b%2 of Wg
-// for b < 2, of Wu otherwise, and the producer takes input group 2kb + b/2...
-// see psrc).
+// into y.  Producer warp p expands, for every k block of parity p/4, two
+// blocks that are contiguous in the slot (gate/up: the Wg and Wu blocks of
+// row block 2m + p%2, input group 2kb + (p/2)%2; down: row blocks
+// 4m + 2((p/2)%2) and the next one of input group 2kb + p%2; see psrc).
 template <bool DOWN>
 __global__ void __launch_bounds__(pg::THREADS, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
@@ -334,10 +334,10 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     return group < a.E ? a.slots + (int64_t)a.group_slot[group] * a.expert_bytes : a.shared_expert;
   };
   // packed source of producer p for (tile, kb): two blocks, contiguous
-  //   down:    Wd row block 4m + p%4, input groups 2kb and 2kb+1;
+  //   down:    Wd input group 2kb + p%2, row blocks 4m + 2((p/2)%2) and the next;
   //   gate/up: row block 2m + p%2, input group 2kb + (p/2)%2, Wg then Wu.
   auto psrc = [&](const PrefillTile& tl, int p, int kb) -> const uint8_t* {
-    if (DOWN) return weights(tl.group) + down_block_offset(tl.m * 4 + (p & 3), 2 * kb, a.d, a.f);
+    if (DOWN) return weights(tl.group) + down_block_offset(tl.m * 4 + 2 * ((p >> 1) & 1), 2 * kb + (p & 1), a.d, a.f);
     return weights(tl.group) + gu_block_offset(tl.m * 2 + (p & 1), 2 * kb + ((p >> 1) & 1), 0, a.d);
   };
 
@@ -464,9 +464,9 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
     // stmatrix row addresses: lane L writes row L%8 of sub-tile L/8
     const uint32_t gx = (uint32_t)(lane & 7) << 4;
     // tile rows of this producer's first block, and the k chunk of each block
-    //   down:    rows (p%4)*32, k chunks 0 and 4 (input groups 2kb, 2kb+1);
+    //   down:    rows ((p/2)%2)*64 and the next 32, k chunk 4*(p%2) (input group 2kb + p%2);
     //   gate/up: Wg rows (p%2)*32, Wu rows 64 + (p%2)*32, k chunk 4*((p/2)%2).
-    const int row0 = DOWN ? (p & 3) * 32 : (p & 1) * 32;
+    const int row0 = DOWN ? ((p >> 1) & 1) * 64 : (p & 1) * 32;
     const uint32_t lane_off = (uint32_t)((row0 + 8 * ((lane >> 3) & 1) + (lane & 7)) * 128);
     const bool hi_group = !DOWN && ((p >> 1) & 1);
     int ti_issue = blockIdx.x, kb_issue = par;
@@ -519,8 +519,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
         const uint8_t* src = my_stage + ps * PCHUNK;
         if (DOWN) {
-          dequant_block_to_tile<0>(src, lane, tile_lane, gx);
-          dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane, gx);
+          if (p & 1) {
+            dequant_block_to_tile<4>(src, lane, tile_lane, gx);
+            dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane + 32 * 128, gx);
+          } else {
+            dequant_block_to_tile<0>(src, lane, tile_lane, gx);
+            dequant_block_to_tile<0>(src + kBlockBytes, lane, tile_lane + 32 * 128, gx);
+          }
         } else if (!hi_group) {
           dequant_block_to_tile<0>(src, lane, tile_lane, gx);                                // Wg
           dequant_block_to_tile<0>(src + kBlockBytes, lane, tile_lane + GU_ROWS * 128, gx);  // Wu

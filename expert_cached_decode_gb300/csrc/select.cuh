@@ -95,14 +95,18 @@ __device__ __forceinline__ int sel_act_index(const SelSmem* s, int id) {
   return s->word_base[id >> 5] + __popc(s->mask[id >> 5] & ((1u << (id & 31)) - 1u));
 }
 
-// Every thread of the block calls this; warps below kSelWarps select.
+// Every participating thread calls this: the whole block when NTH is 0,
+// else the first NTH threads (warps 0 .. NTH/32-1, synchronised by named
+// barrier 1); warps below kSelWarps select.
 // Reads the logits rows [T][E] from global memory through L2 (they were
 // written by other CTAs of this kernel or of the same launch); warps take
 // tokens in turn: top-k (ties to the lower id), weights, ids ascending; then
 // warp 0 forms U.
 // `tl` (timeline builds only) receives %globaltimer stamps of the steps.
+template <int NTH = 0>
 __device__ __forceinline__ void select_call(const float* logits, int T, int E, int K, SelSmem* s,
                                             unsigned long long* tl = nullptr) {
+  const int nthreads = NTH == 0 ? (int)blockDim.x : NTH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #ifdef MOE_TIMELINE
 #define SEL_TL(i) \
@@ -110,8 +114,8 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
 #else
 #define SEL_TL(i) ((void)0)
 #endif
-  for (int i = threadIdx.x; i < kMaxE / 32; i += blockDim.x) s->mask[i] = 0;
-  __syncthreads();
+  for (int i = threadIdx.x; i < kMaxE / 32; i += nthreads) s->mask[i] = 0;
+  step_bar<NTH>();
   for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
     float* row = s->row[warp];
 #pragma unroll 16
@@ -140,7 +144,7 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
     }
     if (t == 0) SEL_TL(2);
   }
-  __syncthreads();
+  step_bar<NTH>();
   SEL_TL(3);
   const int n_words = (E + 31) / 32;
   if (warp == 0) {
@@ -163,7 +167,7 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
       s->act[pos++] = lane * 32 + bit;
     }
   }
-  __syncthreads();
+  step_bar<NTH>();
   SEL_TL(4);
 #undef SEL_TL
 }

@@ -104,6 +104,10 @@ class MoELayer:
     def moe_sync(self):
         check(self._lib.moe_sync(self.ctx), "moe_sync")
 
+    def moe_debug_set_wait_limit(self, ns):
+        """Test hook: limit (ns) of every bounded device wait of this context."""
+        check(self._lib.moe_debug_set_wait_limit(self.ctx, int(ns)), "moe_debug_set_wait_limit")
+
     def moe_cache_stats(self, per_layer=False):
         tot = MoeStats()
         pl = (MoeStats * self.L)() if per_layer else None

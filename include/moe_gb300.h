@@ -61,8 +61,8 @@ typedef enum {
 } moe_status;
 
 /* Shapes and weights of one MoE stack (n_layers layers of one shape).
- * Supported shapes: group == 32, d % 256 == 0, f % 64 == 0, f <= 1024,
- * 2 <= top_k <= 16, top_k < n_experts <= 1024. */
+ * Supported shapes: group == 32, d % 256 == 0, d <= 2048, f % 64 == 0,
+ * f <= 1024, 2 <= top_k <= 16, top_k < n_experts <= 1024. */
 typedef struct {
   int32_t d;               /* hidden size */
   int32_t f;               /* expert intermediate size */
@@ -114,7 +114,10 @@ typedef struct {
 
 /* Create a context: copies router weights, bias and shared experts to the
  * device (re-laid out), pins or registers the host pool.  *out receives the
- * context.  Errors: INVALID_ARG (shapes, NULL pointers), OOM, HOST_PIN, CUDA. */
+ * context.  On any error nothing stays allocated or registered and *out is
+ * NULL.  Errors: INVALID_ARG (shapes, NULL pointers), OOM, HOST_PIN, CUDA,
+ * UNIMPLEMENTED (also when one decode CTA per SM does not fit: the decode
+ * kernel's grid-wide counters need all of its CTAs resident at once). */
 moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out);
 
 /* Size the expert cache to capacity_slots (each B_x bytes of device memory)
@@ -122,8 +125,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out);
  * ascending) into slots 0, 1, ... from the host pool.  Resets the LRU state,
  * the logical clock and the counters.  When every key of the stack is
  * preloaded no miss can occur and moe_forward never waits on the host.
- * Synchronous.  Errors: INVALID_ARG (capacity < k*16 distinct picks of one
- * call, n_preload > capacity, unsorted keys), OOM, CUDA. */
+ * Synchronous.  Every buffer of the new cache is allocated before the old
+ * one is released, so on MOE_ERR_OOM the previous cache (slots, LRU state,
+ * counters) is unchanged and usable.  Errors: INVALID_ARG (capacity < k*16
+ * distinct picks of one call, n_preload > capacity, unsorted keys), OOM,
+ * CUDA. */
 moe_status moe_cache_configure(moe_ctx* ctx, int64_t capacity_slots,
                                const int32_t* preload_keys, int64_t n_preload);
 
@@ -164,12 +170,35 @@ typedef enum { MOE_MISS_HOST_COPY = 0, MOE_MISS_DEVICE_PULL = 1 } moe_miss_mode;
 moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
 
 /* Test hook: make the nth (>= 1) future event of `kind` fail once, then
- * disarm; kind 0 disarms.  MOE_INJECT_MISS_COPY: the issue of a miss copy in
- * the host-copy miss mode fails, so moe_forward returns MOE_ERR_CUDA before
- * any cache state changes.  Process-wide, not thread-safe.  Errors:
- * INVALID_ARG for an unknown kind or nth < 1. */
-enum { MOE_INJECT_MISS_COPY = 1 };
+ * disarm; kind 0 disarms.  Process-wide, not thread-safe.  Errors:
+ * INVALID_ARG for an unknown kind or nth < 1.
+ *   MOE_INJECT_MISS_COPY: the issue of a miss copy in the host-copy miss mode
+ *     fails, so moe_forward returns MOE_ERR_CUDA before any cache state
+ *     changes;
+ *   MOE_INJECT_HOLD_ROUTER: in a decode layer-call with routing inside the
+ *     kernel, CTA 0 never arrives on the grid-wide counter of the router
+ *     logits, so every CTA's bounded wait on it runs out (after the limit of
+ *     moe_debug_set_wait_limit); the call returns MOE_OK (it is asynchronous)
+ *     and the next moe_sync reports MOE_ERR_TIMEOUT;
+ *   MOE_INJECT_HOST_REGISTER: moe_layer_create's registration of a pageable
+ *     host pool fails (MOE_ERR_HOST_PIN, nothing left allocated or
+ *     registered);
+ *   MOE_INJECT_DEVICE_ALLOC: a device allocation of moe_layer_create or
+ *     moe_cache_configure fails (MOE_ERR_OOM; create leaves nothing
+ *     allocated, configure leaves the previous cache unchanged). */
+enum {
+  MOE_INJECT_MISS_COPY = 1,
+  MOE_INJECT_HOLD_ROUTER = 2,
+  MOE_INJECT_HOST_REGISTER = 3,
+  MOE_INJECT_DEVICE_ALLOC = 4
+};
 moe_status moe_debug_inject_failure(int32_t kind, int64_t nth);
+
+/* Test hook: the limit, in nanoseconds of the GPU's global timer, of every
+ * bounded device-side wait of this context's decode kernel (default 2 s).
+ * A wait that runs out sets the context's error word and the kernel returns;
+ * moe_sync then reports MOE_ERR_TIMEOUT.  Errors: INVALID_ARG for ns <= 0. */
+moe_status moe_debug_set_wait_limit(moe_ctx* ctx, int64_t ns);
 
 /* Wait for all work of the context and report a deferred device error
  * (MOE_ERR_TIMEOUT if a bounded device wait gave up).  After a device error

@@ -136,20 +136,36 @@ def test_decode_many_calls_sampled(decode):
     assert st["distinct_hits"] - before["distinct_hits"] == 64 * wl.top_k
 
 
-@pytest.mark.parametrize("f", [64, 192, 320, 256])
-def test_ffn_widths_row_blocks_per_down_tile(f):
-    # f = 64, 192, 320 put 8 row blocks in a down tile (one consumer warp
-    # each), f = 256 two; the tiny shape otherwise
+@pytest.mark.parametrize("d,f", [(256, 64), (256, 192), (256, 320), (512, 128), (768, 64), (1280, 96)])
+def test_shapes_slices_and_down_stages(d, f):
+    # f/32 slices per expert from 2 to 10; d/32 row blocks of the down part
+    # from 8 (half a stage) over 24 (a stage and a half) to 40 (two and a half
+    # stages); one and two token tiles
     import dataclasses
     from moe_inputs import WORKLOADS, BIAS_LAMBDA
-    wl = dataclasses.replace(WORKLOADS[1], f=f)
+    wl = dataclasses.replace(WORKLOADS[1], d=d, f=f)
     s = Synth(wl, bias_lambda=BIAS_LAMBDA)
     layer = make_layer(s)
     try:
         layer.moe_cache_configure(wl.capacity, np.arange(wl.keys))
         memo = ExpertMemo(s, wl.keys)
-        for T in (1, 5):
+        for T in (1, 5, 9, 16):
             xb = s.tokens_many(0, [900 + T], T=T)[0]
             _check_call(s, layer, memo, xb)
     finally:
         layer.close()
+
+
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_decode_is_deterministic(decode, T):
+    # the same call twice gives bitwise the same y (fixed-order combine)
+    s, layer, memo = decode
+    xb = s.tokens_many(0, [700 + T], T=T)[0]
+    x = to_device_bf16(xb)
+    y1 = torch.empty((T, s.wl.d), dtype=torch.float32, device="cuda")
+    y2 = torch.empty_like(y1)
+    layer.moe_forward(0, x, y1)
+    layer.moe_forward(0, to_device_bf16(s.tokens_many(0, [1], T=T)[0]), y2)   # another call between
+    layer.moe_forward(0, x, y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
