@@ -113,6 +113,8 @@ struct moe_ctx {
   uint16_t* p_hg_lo = nullptr;   // [T*(k+1)][f] fp16 (lo part of h)
   int32_t* p_perm = nullptr;
   float* p_wsort = nullptr;
+  int32_t* p_inv = nullptr;      // [T*k] sorted row of each pick
+  float* p_osort = nullptr;      // [T*k][d] weighted output of each routed pick
   int32_t* p_cursor = nullptr;
   int32_t* p_group_slot = nullptr;
   PrefillTile* p_tiles_gu = nullptr;
@@ -412,6 +414,8 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->p_hg_lo);
   cudaFree(c->p_perm);
   cudaFree(c->p_wsort);
+  cudaFree(c->p_inv);
+  cudaFree(c->p_osort);
   cudaFree(c->p_cursor);
   cudaFree(c->p_group_slot);
   cudaFree(c->p_tiles_gu);
@@ -610,12 +614,14 @@ static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
       {reinterpret_cast<void**>(&c->p_hg_lo), (size_t)rows * c->f * sizeof(uint16_t)},
       {reinterpret_cast<void**>(&c->p_perm), (size_t)rows * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_wsort), (size_t)rows * sizeof(float)},
+      {reinterpret_cast<void**>(&c->p_inv), (size_t)kMaxPrefillT * c->k * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_osort), (size_t)kMaxPrefillT * c->k * c->d * sizeof(float)},
       {reinterpret_cast<void**>(&c->p_cursor), (size_t)c->E * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_group_slot), (size_t)(c->E + 1) * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_tiles_gu), (size_t)c->p_max_tiles * (c->f / 64) * sizeof(PrefillTile)},
       {reinterpret_cast<void**>(&c->p_tiles_dn), (size_t)c->p_max_tiles * (c->d / 128) * sizeof(PrefillTile)},
       {reinterpret_cast<void**>(&c->p_ntiles), 2 * sizeof(int32_t)}};
-  return alloc_all(specs, 10);
+  return alloc_all(specs, sizeof(specs) / sizeof(specs[0]));
 }
 
 // Router logits (tcgen05) + top-k for T tokens; idx/w device outputs.
@@ -767,12 +773,12 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   sa.cursor = c->p_cursor;
   sa.perm = c->p_perm;
   sa.wsort = c->p_wsort;
+  sa.inv = c->p_inv;
   sa.T = T;
   sa.k = c->k;
   sa.shared_weight = c->shared_weight;
   CUDA_TRY(launch_prefill_scatter(sa, s));
   CUDA_TRY(launch_prefill_gather(static_cast<const uint16_t*>(x), c->p_perm, c->p_xg, rows, c->d, s));
-  CUDA_TRY(cudaMemsetAsync(y, 0, (size_t)T * c->d * sizeof(float), s));
   CUtensorMap tx, th, thl;
   // token tiles are loaded in two halves, one by each CTA of a cluster pair
   st = make_tmap_2d(&tx, c->p_xg, rows, c->d, kPrefillBN / 2, false);
@@ -792,12 +798,21 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   ga.perm = c->p_perm;
   ga.wsort = c->p_wsort;
   ga.y = y;
+  ga.osort = c->p_osort;
   ga.E = c->E;
   ga.d = c->d;
   ga.f = c->f;
   ga.err = c->err;
   CUDA_TRY(launch_prefill_gate_up(tx, ga, s, c->num_sms));
   CUDA_TRY(launch_prefill_down(th, thl, ga, s, c->num_sms));
+  PrefillCombineArgs cb{};
+  cb.osort = c->p_osort;
+  cb.inv = c->p_inv;
+  cb.y = y;
+  cb.T = T;
+  cb.k = c->k;
+  cb.d = c->d;
+  CUDA_TRY(launch_prefill_combine(cb, s));
   if (trace) {
     const int n = T * c->k;
     std::vector<int32_t> gslot(c->E + 1);

@@ -196,6 +196,7 @@ struct PrefillScatterArgs {
   int32_t* cursor;
   int32_t* perm;           // [T*k + T] token of each sorted row
   float* wsort;            // [T*k + T] combine weight of each sorted row
+  int32_t* inv;            // [T*k] sorted row of pick t*k + i
   int T, k;
   float shared_weight;
 };
@@ -212,9 +213,17 @@ struct PrefillGemmArgs {
   uint16_t* hg_lo;         // [rows][f] fp16 lo part of h
   const int32_t* perm;
   const float* wsort;
-  float* y;                // [T][d]
+  float* y;                // [T][d]: the shared expert's weighted output (down GEMM)
+  float* osort;            // [T*k][d]: weighted output of each routed pick, by sorted row
   int E, d, f;
   uint32_t* err;
+};
+
+struct PrefillCombineArgs {
+  const float* osort;      // [T*k][d]
+  const int32_t* inv;      // [T*k] sorted row of each pick
+  float* y;                // [T][d], holds the shared expert's part on entry
+  int T, k, d;
 };
 
 // Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
@@ -243,6 +252,7 @@ cudaError_t launch_prefill_gather(const uint16_t* x, const int32_t* perm, uint16
 cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs& a, cudaStream_t s, int grid);
 cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
                                 cudaStream_t s, int grid);
+cudaError_t launch_prefill_combine(const PrefillCombineArgs& a, cudaStream_t s);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
 // whether one CTA of every decode-kernel variant fits on an SM at hidden size d
 cudaError_t decode_ffn_fits(int d, bool* fits);

@@ -6,7 +6,12 @@
 // (a 12,288-token chunk is the pages' single-GPU prefill size, page
 // "一张 RTX 4090 跑千亿模型", §加个草稿层):
 //   gate/up:  [g|u]^T[f x n_e] = [Wg|Wu][f x d] . X_e^T   -> h = silu(g)*u (fp16)
-//   down:     o^T[d x n_e] = Wd[d x f] . H_e^T            -> y[t] += w[t,e] * o[t]
+//   down:     o^T[d x n_e] = Wd[d x f] . H_e^T            -> w[t,e] * o[t]
+// The down GEMM writes the shared expert's weighted output straight into y
+// and each routed pick's into its own row of a per-pick buffer; a combine
+// kernel then adds, per token, its picks in ascending expert id (the decode
+// path's order), so y is the same whatever order tiles and the counting sort
+// ran in.
 // h is carried as an fp16 pair (hi = RN(h), lo = RN(h - hi)) and the down
 // GEMM accumulates Wd.hi + Wd.lo, so h keeps ~22 bits; the fp16 weight
 // RN(q * scale) is the only rounding of an operand.
@@ -140,6 +145,7 @@ __global__ void prefill_scatter_kernel(PrefillScatterArgs a) {
     const int pos = atomicAdd(&a.cursor[e], 1);
     a.perm[pos] = i / a.k;
     a.wsort[pos] = a.w[i];
+    a.inv[i] = pos;
   } else if (i < picks + a.T) {
     const int t = i - picks;
     a.perm[picks + t] = t;
@@ -641,12 +647,24 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               tokc = ctok[q];
               wc = cw[q];
             }
-          float* ycol = a.y + tl.m * BM + quarter * 32 + lane;
+          // routed expert: the weighted output of each pick goes to its own
+          // sorted row of osort (summed per token later, in a fixed order);
+          // the shared expert (every token once): straight into y
+          const int drow = tl.m * BM + quarter * 32 + lane;
+          if (tl.group < a.E) {
+            float* ocol = a.osort + (size_t)(tl.row0 + col0) * a.d + drow;
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int tok = __shfl_sync(0xffffffffu, tokc, jj);
-            const float w = __shfl_sync(0xffffffffu, wc, jj);
-            if (col0 + jj < tl.nlen) red_add_f32(ycol + (size_t)tok * a.d, __uint_as_float(r[jj]) * w);
+            for (int jj = 0; jj < 16; ++jj) {
+              const float w = __shfl_sync(0xffffffffu, wc, jj);
+              if (col0 + jj < tl.nlen) ocol[(size_t)jj * a.d] = __uint_as_float(r[jj]) * w;
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int tok = __shfl_sync(0xffffffffu, tokc, jj);
+              const float w = __shfl_sync(0xffffffffu, wc, jj);
+              if (col0 + jj < tl.nlen) a.y[(size_t)tok * a.d + drow] = __uint_as_float(r[jj]) * w;
+            }
           }
         }
       }
@@ -740,6 +758,33 @@ static cudaError_t launch_gemm(const CUtensorMap& tmB, const CUtensorMap& tmB2, 
   return cudaLaunchKernelEx(&cfg, prefill_gemm_kernel<DOWN>, tmB, tmB2, a);
 }
 
+// y[t] += the weighted outputs of token t's routed picks, added in pick
+// order (ascending expert id) after the shared expert's part, so y does not
+// depend on the order in which tiles or the counting sort ran.  One thread
+// per 4 consecutive outputs; every pick's load is issued before the sum.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillCombineArgs a) {
+  const int d4 = a.d / 4;
+  const int64_t n = (int64_t)a.T * d4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / d4), c = (int)(i - (int64_t)t * d4);
+    float4 acc = reinterpret_cast<const float4*>(a.y + (size_t)t * a.d)[c];
+    float4 o[kMaxTopK];
+#pragma unroll
+    for (int kk = 0; kk < kMaxTopK; ++kk)
+      if (kk < a.k) o[kk] = __ldcs(reinterpret_cast<const float4*>(a.osort + (size_t)a.inv[t * a.k + kk] * a.d) + c);
+#pragma unroll
+    for (int kk = 0; kk < kMaxTopK; ++kk) {
+      if (kk < a.k) {
+        acc.x += o[kk].x;
+        acc.y += o[kk].y;
+        acc.z += o[kk].z;
+        acc.w += o[kk].w;
+      }
+    }
+    reinterpret_cast<float4*>(a.y + (size_t)t * a.d)[c] = acc;
+  }
+}
+
 cudaError_t launch_prefill_plan(const PrefillPlanArgs& a, cudaStream_t s) {
   prefill_plan_kernel<<<1, 1024, 0, s>>>(a);
   return cudaGetLastError();
@@ -748,6 +793,13 @@ cudaError_t launch_prefill_plan(const PrefillPlanArgs& a, cudaStream_t s) {
 cudaError_t launch_prefill_scatter(const PrefillScatterArgs& a, cudaStream_t s) {
   const int n = a.T * a.k + a.T;
   prefill_scatter_kernel<<<(n + 255) / 256, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_combine(const PrefillCombineArgs& a, cudaStream_t s) {
+  const int64_t n = (int64_t)a.T * (a.d / 4);
+  const int64_t blocks = (n + 255) / 256;
+  prefill_combine_kernel<<<(unsigned)(blocks < 65536 ? blocks : 65535), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -88,9 +88,11 @@ def test_decode_layer_parity_full_size(decode):
 
 def test_decode_stamps_follow_calls(decode):
     s, layer, memo = decode
+    tr, _, _ = _check_call(s, layer, memo, s.tokens(0, 5))
     owner, stamp = layer.moe_cache_export()
     assert np.array_equal(owner, np.arange(512))
-    assert stamp.max() >= 0
+    # the call's ten experts carry the latest logical clock
+    assert np.all(stamp[tr["idx"][0]] == stamp.max()) and stamp.max() >= 0
 
 
 @pytest.mark.parametrize("T", [5, 16])
