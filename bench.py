@@ -24,10 +24,16 @@ prefill (by default at T=1 with the default call count; --no-prefill drops
 it): the 12,288-token chunk and the chunk-size sweep, expert FLOP rate
 against the measured bf16 tensor peak.
 
+stack (by default at T=1 with the default call count; --no-stack drops it):
+the two 48-layer stacks with the 8,445-slot cache starting empty, misses
+pulled by the GPU from the host pool -- the verify stack (T=5, Zipf s=1.1)
+and the concurrent stack (T=16, Zipf s=0.8) -- 3 warm-up passes over 2,000
+calls, then the timed pass; tokens/s of the whole 48-layer stack against
+max(distinct-expert bytes / HBM, miss bytes / measured H2D).
+
 --impl reference times the CPU oracle itself (the pages publish no code and
 no number for this step; the oracle is the only reference implementation).
---stack additionally runs the 48-layer verify and concurrent stacks,
---stack-sweep the verify-width x cache-capacity sweep.
+--stack-sweep adds the verify-width x cache-capacity sweep.
 """
 
 import argparse
@@ -68,7 +74,7 @@ def peaks():
 
 
 # the sources the decode kernel is compiled from
-DECODE_SOURCES = ("decode_ffn.cu", "select.cuh", "common.cuh", "internal.h")
+DECODE_SOURCES = ("decode_ffn.cu", "select.cuh", "common.cuh", "internal.h", "repack.cuh")
 
 
 def source_hash():
@@ -620,14 +626,13 @@ def run_gpu(args):
                        "l2": "inputs larger than L2: 512 resident experts = 1.06 GB > 129 MB L2 "
                              "(the shared expert and the router stay L2-resident across calls)",
                        "graph": "10,000 moe_forward calls captured once, replayed per step",
-                       "parallelism": "single GPU",
-                       "stack_tokens_per_s_derived": value / 48.0},
+                       "parallelism": "single GPU"},
             "gpu_launches": CALLS * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": recorded_traffic(),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                          "kernel": "decode_ffn_kernel with fused routing: one launch per call (average launch "
-                                   "duration = call duration, launch gaps included)",
+                                   "duration = call duration, launch gaps included; back to back, CUDA graph)",
                          "alg_bytes_per_launch": alg_bytes, "router_bytes": ROUTER_BYTES},
             "e2e": {"value": e2e_value, "unit": "tokens/s",
                     "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(y_host.numel() * 4)},
@@ -644,7 +649,7 @@ def run_gpu(args):
                 line["stack_sweep"] = run_stack_sweep(calls=args.stack_sweep)
             except Exception as ex:   # reported, not hidden
                 line["stack_sweep"] = {"error": str(ex)[:300]}
-        if args.stack:
+        if args.stack and T == 1 and CALLS == DEFAULT_CALLS:
             try:
                 cfgs = (3, 4) if args.stack_config == 0 else (args.stack_config,)
                 modes = (1, 0) if args.stack_mode < 0 else (args.stack_mode,)
@@ -678,15 +683,17 @@ def main():
                     help="also time the 12,288-token prefill chunk and sweep (the default at T=1)")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-steps", type=int, default=5)
-    ap.add_argument("--stack", action="store_true",
-                    help="also run the 48-layer stacks (T=5 Zipf 1.1, T=16 Zipf 0.8) with the 8,445-slot cache")
+    ap.add_argument("--stack", action="store_true", default=True,
+                    help="also run the 48-layer stacks (T=5 Zipf 1.1, T=16 Zipf 0.8) with the 8,445-slot cache "
+                         "(the default at T=1)")
+    ap.add_argument("--no-stack", dest="stack", action="store_false")
     ap.add_argument("--stack-pool", type=int, default=2048,
                     help="host-pool entries for --stack: expert (l, e) reads entry (512 l + e) mod P; "
                          "0 = one per (layer, expert), 50.7 GB, slow to fill (default 2048, 4.2 GB)")
     ap.add_argument("--stack-config", type=int, default=0, choices=(0, 3, 4),
                     help="--stack: 3 = verify stack only, 4 = concurrent stack only (default both)")
-    ap.add_argument("--stack-mode", type=int, default=-1, choices=(-1, 0, 1),
-                    help="--stack: 1 = GPU pulls misses, 0 = host-issued copies (default both)")
+    ap.add_argument("--stack-mode", type=int, default=1, choices=(-1, 0, 1),
+                    help="--stack: 1 = GPU pulls misses (default), 0 = host-issued copies, -1 = both")
     ap.add_argument("--stack-sweep", type=int, default=0, metavar="CALLS",
                     help="verify width (T = 1, 4, 7) x cache capacity (9,057 / 8,445 / 6,144) sweep on the "
                          "verify stack, CALLS calls per pass")

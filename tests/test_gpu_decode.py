@@ -138,7 +138,7 @@ def test_decode_many_calls_sampled(decode):
     assert st["distinct_hits"] - before["distinct_hits"] == 64 * wl.top_k
 
 
-@pytest.mark.parametrize("d,f", [(256, 64), (256, 192), (256, 320), (512, 128), (768, 64), (1280, 96)])
+@pytest.mark.parametrize("d,f", [(256, 64), (256, 192), (256, 320), (512, 128), (768, 64), (1280, 128)])
 def test_shapes_slices_and_down_stages(d, f):
     # f/32 slices per expert from 2 to 10; d/32 row blocks of the down part
     # from 8 (half a stage) over 24 (a stage and a half) to 40 (two and a half
