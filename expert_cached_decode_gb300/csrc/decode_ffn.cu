@@ -44,10 +44,15 @@
 // row blocks w*16/CW + j (+ 16 per stage) of y for the whole call.
 //
 // With a cache that can miss, CTA 0 takes no units and runs the cache (LRU
-// victims, commit, next LRU order, plan) and CTAs 1..G-1 pull the call's
-// misses from the host pool into their victim slots before the routed
-// units.  With host-issued miss copies the kernel follows the routing kernel
-// and reads its plan.  All waits are bounded.
+// victims, commit, next LRU order, plan).  CTAs 1..G-1 order their routed
+// units resident experts first and their producers start streaming them at
+// once; the consumers first share the fetch of the call's misses: jobs of 32
+// rows of one matrix, read from the registered host pool (contiguous runs of
+// the canonical layout) and re-laid out straight into the victim slot, each
+// finished job counted per miss.  A producer waits for a missing expert's
+// count before it streams that expert's units.  With host-issued miss copies
+// the kernel follows the routing kernel and reads its plan.  All waits are
+// bounded.
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -77,8 +82,8 @@ struct DCfg {
 __host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
 
 // bytes of the shared-memory region whose uses never overlap in time: x
-// rows for the router, the selection scratch, the gate/up partials, the
-// miss-pull scratch and the combine partials
+// rows for the router, the selection scratch, the gate/up partials, a miss
+// fetch job and the combine partials
 template <int NT>
 __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
   using C = DCfg<NT>;
@@ -87,6 +92,8 @@ __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
   const size_t red = (size_t)C::CW * C::NQ * 32 * 4;
   const size_t pull = (size_t)2 * kMaxPicks * 4;
   const size_t cmb = (size_t)C::CW * 32 * 4;
+  const size_t job = (size_t)14 * (d > 1024 ? d : 1024);   // one fetch job of a miss (f <= 1024)
+  b = b > job ? b : job;
   b = b > sel ? b : sel;
   b = b > red ? b : red;
   b = b > pull ? b : pull;
@@ -202,7 +209,7 @@ __device__ __forceinline__ int group_exclusive_scan(int v, int* s_warp, int* tot
 // ascending expert id, take the least recently used slots in (stamp, slot id)
 // order, which is the order of q (least recent first) with the hits skipped.
 // The call's touched slots (hits and victims) move, in slot-id order, to the
-// recent end of q.  The victims are published first (xbar[0]), because CTAs
+// recent end of q.  The victims are published first (vict[0]), because CTAs
 // 1..G-1 wait for them before pulling the misses; then the commit (table,
 // owners, stamps), the next order, the plan and the statistics.  `scratch`
 // is shared memory this CTA does not otherwise use.
@@ -210,7 +217,7 @@ template <int NTH>
 __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m, const int* s_act_expert,
                                               int* s_act_slot, const int* s_pick_act, const float* s_w,
                                               long long clk, uint32_t calls, uint8_t* scratch,
-                                              size_t scratch_bytes, uint32_t* xbar) {
+                                              size_t scratch_bytes, uint32_t* vict) {
   __shared__ int s_warp[NTH / 32 + 1];
   __shared__ int s_evict;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -297,7 +304,7 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
   named_bar(1, NTH);
   if (m > 0 && tid == 0) {
     MOE_TL(g_ffn_timeline, 0, 28);
-    red_release_add(&xbar[0], 1u);   // covers the plan's victim entries (after the barrier)
+    red_release_add(&vict[0], 1u);   // covers the plan's victim entries (after the barrier)
   }
   // commit: evicted keys leave the table before the misses enter it
   for (int j = tid; j < m; j += NTH) {
@@ -358,84 +365,86 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
   }
 }
 
-// One arrival of this CTA on a grid counter, then the wait for all GT CTAs
-// (bounded); false if the wait gave up.  The NTH threads of named barrier 1
-// call it.
-template <int NTH>
-__device__ __forceinline__ bool group_grid_barrier(uint32_t* bar, uint32_t GT, const FfnArgs& a, int* s_flag) {
-  named_bar(1, NTH);
-  if (threadIdx.x == 0) {
-    red_release_add(bar, 1u);   // covers this CTA's writes (after the block barrier)
-    const bool ok = wait_flag_geq(bar, GT, a.wait_ns);
-    if (!ok) set_error(a.err, DEV_TIMEOUT_FLAG);
-    *s_flag = ok;
+// One job of a missing expert's fetch: 32 consecutive rows of one matrix of
+// the canonical expert in the host pool (their codes and their scales are
+// two contiguous runs there), re-laid out into the blocks of those rows in
+// the expert's victim slot.  Jobs of miss j: Wg row blocks 0..f/32-1, Wu row
+// blocks 0..f/32-1, Wd row blocks 0..d/32-1.
+struct PullJob {
+  const uint8_t* codes;    // host pool: 32 rows x G groups x 12 B
+  const uint8_t* scales;   // host pool: 32 rows x G groups x 2 B
+  uint8_t* slot;           // the victim slot (device layout)
+  int code_bytes, G, mat, rb, miss;
+};
+
+__device__ __forceinline__ PullJob pull_job(const FfnArgs& a, int q) {
+  const int d = a.d, f = a.f, RG = f / 32, RD = d / 32, JPM = 2 * RG + RD;
+  const int j = q / JPM, r = q - j * JPM;
+  const int e = __ldcg(&a.plan->miss_expert[j]);
+  const int v = __ldcg(&a.plan->miss_slot[j]);
+  const int64_t entry = ((int64_t)a.layer * a.E + e) % a.pool_entries;
+  const uint8_t* src = a.host_pool + entry * a.expert_bytes;
+  const int64_t gq = (int64_t)f * (d / 32) * 12, dq = (int64_t)d * (f / 32) * 12, gs = (int64_t)f * (d / 32) * 2;
+  PullJob J;
+  J.miss = j;
+  J.slot = const_cast<uint8_t*>(a.slots) + (int64_t)v * a.expert_bytes;
+  if (r < 2 * RG) {
+    J.mat = r / RG;
+    J.rb = r - J.mat * RG;
+    J.G = d / 32;
+    J.codes = src + J.mat * gq + (int64_t)J.rb * 32 * J.G * 12;
+    J.scales = src + 2 * gq + dq + J.mat * gs + (int64_t)J.rb * 32 * J.G * 2;
+  } else {
+    J.mat = 2;
+    J.rb = r - 2 * RG;
+    J.G = f / 32;
+    J.codes = src + 2 * gq + (int64_t)J.rb * 32 * J.G * 12;
+    J.scales = src + 2 * gq + dq + 2 * gs + (int64_t)J.rb * 32 * J.G * 2;
   }
-  named_bar(1, NTH);
-  return *s_flag != 0;
+  J.code_bytes = 32 * J.G * 12;
+  return J;
 }
 
-// CTAs 1..G-1 (tile index ct of GT) of a call with m > 0 misses: wait for
-// CTA 0's victims, pull the misses' canonical bytes from the host pool into
-// staging, a grid barrier, re-lay them out into their victim slots, a grid
-// barrier.  False if a wait gave up (the error word is set).
-template <int NTH>
-__device__ __forceinline__ bool pull_and_place_misses(const FfnArgs& a, int m, int n_act, int* s_act_slot,
-                                                      uint32_t* xbar, int GT, int ct, int* scratch) {
-  int* s_mslot = scratch;   // shared memory not in use during this step
-  int* s_mexp = s_mslot + kMaxPicks;
-  __shared__ int s_flag;
+// Jobs [q0, q1) of this call's misses, by the NTH consumer threads: the job's
+// bytes come from the host pool in 16-byte loads (the next job's loads are
+// in flight while this one is re-laid out) into shared memory `sm`, each warp
+// then writes whole blocks into the victim slot, and ready[miss] counts the
+// finished jobs (release, after a barrier of all NTH threads).  Every byte of
+// a job sits in at most KPC chunks per thread.
+template <int NTH, int KPC>
+__device__ __forceinline__ void pull_jobs(const FfnArgs& a, int q0, int q1, uint8_t* sm, uint32_t* ready) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const Plan* P = a.plan;
-  if (m > a.staging_n) {   // cannot happen (m <= T*k and m <= E); never write past the staging slots
-    if (tid == 0) set_error(a.err, DEV_BAD_PLAN);
-    return false;
-  }
-  if (tid == 0) {
-    const bool ok = wait_flag_geq(&xbar[0], 1u, a.wait_ns);
-    if (!ok) set_error(a.err, DEV_TIMEOUT_FLAG);
-    s_flag = ok;
-  }
-  named_bar(1, NTH);
-  if (!s_flag) return false;
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 29);
-  for (int j = tid; j < m; j += NTH) {
-    s_mslot[j] = __ldcg(&P->miss_slot[j]);
-    s_mexp[j] = __ldcg(&P->miss_expert[j]);
-  }
-  for (int i = tid; i < n_act; i += NTH)
-    if (s_act_slot[i] < 0) s_act_slot[i] = __ldcg(&P->act_slot[i]);
-  named_bar(1, NTH);
-  // host pool -> staging, 16 bytes per thread and step, four loads in flight
-  const int64_t per = a.expert_bytes / 16;
-  const int64_t nthr = (int64_t)GT * NTH;
-  for (int j = 0; j < m; ++j) {
-    const int64_t entry = ((int64_t)a.layer * a.E + s_mexp[j]) % a.pool_entries;
-    const uint4* src = reinterpret_cast<const uint4*>(a.host_pool + entry * a.expert_bytes);
-    uint4* dst = reinterpret_cast<uint4*>(a.staging + (int64_t)j * a.expert_bytes);
-    int64_t c = (int64_t)ct * NTH + tid;
-    for (; c + 3 * nthr < per; c += 4 * nthr) {
-      const uint4 v0 = src[c], v1 = src[c + nthr], v2 = src[c + 2 * nthr], v3 = src[c + 3 * nthr];
-      dst[c] = v0;
-      dst[c + nthr] = v1;
-      dst[c + 2 * nthr] = v2;
-      dst[c + 3 * nthr] = v3;
+  uint4 rg[KPC];
+  auto load = [&](const PullJob& J) {
+    const int ncb = J.code_bytes / 16, n = ncb + J.G * 4;   // scales: 32 rows x G x 2 B = G * 4 chunks
+#pragma unroll
+    for (int i = 0; i < KPC; ++i) {
+      const int c = tid + i * NTH;
+      if (c < n)
+        rg[i] = c < ncb ? reinterpret_cast<const uint4*>(J.codes)[c]
+                        : reinterpret_cast<const uint4*>(J.scales)[c - ncb];
     }
-    for (; c < per; c += nthr) dst[c] = src[c];
+  };
+  if (q0 < q1) load(pull_job(a, q0));
+  for (int q = q0; q < q1; ++q) {
+    const PullJob J = pull_job(a, q);
+    const int n = J.code_bytes / 16 + J.G * 4;
+#pragma unroll
+    for (int i = 0; i < KPC; ++i) {
+      const int c = tid + i * NTH;
+      if (c < n) reinterpret_cast<uint4*>(sm)[c] = rg[i];
+    }
+    named_bar(1, NTH);
+    if (q + 1 < q1) load(pull_job(a, q + 1));
+    for (int gi = warp; gi < J.G; gi += NTH / 32) {
+      const uint32_t* cw = reinterpret_cast<const uint32_t*>(sm + (size_t)(lane * J.G + gi) * 12);
+      const uint16_t sc = reinterpret_cast<const uint16_t*>(sm + J.code_bytes)[lane * J.G + gi];
+      const int64_t off = J.mat < 2 ? gu_block_offset(J.rb, gi, J.mat, a.d) : down_block_offset(J.rb, gi, a.d, a.f);
+      pack_block(cw[0], cw[1], cw[2], sc, lane, J.slot + off);
+    }
+    named_bar(1, NTH);
+    if (tid == 0) red_release_add(&ready[J.miss], 1u);   // covers every warp's blocks (after the barrier)
   }
-  if (!group_grid_barrier<NTH>(&xbar[1], (uint32_t)GT, a, &s_flag)) return false;
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 30);
-  // staging -> victim slots in the device block layout, one block per warp
-  const int nb = (a.f / 32) * (a.d / 32) * 2 + (a.d / 32) * (a.f / 32);
-  const int64_t nwarps = (int64_t)GT * (NTH / 32);
-  uint8_t* slots = const_cast<uint8_t*>(a.slots);
-  for (int64_t gw = (int64_t)ct * (NTH / 32) + warp; gw < (int64_t)nb * m; gw += nwarps) {
-    const int ex = (int)(gw / nb), bi = (int)(gw % nb);
-    repack_block(a.staging + (int64_t)ex * a.expert_bytes, slots + (int64_t)s_mslot[ex] * a.expert_bytes, bi, a.d,
-                 a.f, lane);
-  }
-  const bool ok = group_grid_barrier<NTH>(&xbar[2], (uint32_t)GT, a, &s_flag);
-  if (tid == 0) MOE_TL(g_ffn_timeline, blockIdx.x, 31);
-  return ok;
 }
 
 // MODE kPlanRead: the routing plan comes from memory (routing kernel and
@@ -474,6 +483,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   __shared__ float s_w[kMaxPicks];        // [T][k] routing weights
   __shared__ int s_act_expert[kMaxPicks]; // expert id of each distinct routed expert
   __shared__ int s_tab[kMaxE];            // the layer's slot-table row (fused routing)
+  __shared__ int s_order[kMaxPicks];      // distinct experts in unit order (resident ones first)
+  __shared__ int s_mrank[kMaxPicks];      // position of each distinct expert in the miss list, -1 if resident
   __shared__ int s_n_act, s_u0, s_u1;
   __shared__ uint32_t s_calls;
   __shared__ long long s_clock;
@@ -545,7 +556,26 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     if (ok) {
       MOE_TL(g_ffn_timeline, cta, 4);
       const int u0 = s_u0, u1 = s_u1;
-      for (int u = u0; u < u1 && ok; ++u) ok = issue_unit(expert_base(u / RG), u % RG);
+      const uint32_t jpm = (uint32_t)(2 * RG + RD);   // fetch jobs per missing expert
+      const uint32_t* ready = a.counters + 1 + (size_t)(s_calls & 1u) * a.set_words + 3;
+      for (int u = u0; u < u1 && ok; ++u) {
+        const int ai = s_order[u / RG];
+        const int j = CACHED ? s_mrank[ai] : -1;
+        const uint8_t* eb;
+        if (j < 0) {
+          eb = expert_base(ai);
+        } else {
+          // a missing expert: every job of its fetch is done (other CTAs'
+          // generic stores, ordered before the bulk copies by the proxy fence)
+          if (!wait_flag_geq(&ready[j], jpm, lim)) {
+            ok = false;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          eb = a.slots + (int64_t)__ldcg(&a.plan->miss_slot[j]) * a.expert_bytes;
+        }
+        ok = issue_unit(eb, u % RG);
+      }
     }
     if (!ok && !s_abort) {
       set_error(a.err, DEV_TIMEOUT_BARRIER);
@@ -693,7 +723,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   uint32_t* const cset = a.counters + 1 + (size_t)call_set * a.set_words;
   uint32_t* const gbar_r = cset;        // CTAs past the router rows
   uint32_t* const gbar_p = cset + 1;    // tile CTAs whose partial of y is written
-  uint32_t* const xbar = cset + 2;      // cache mode: victims published, misses pulled, misses placed
+  uint32_t* const vict = cset + 2;      // cache mode: the misses' victims are published
+  uint32_t* const ready = cset + 3;     // cache mode: finished fetch jobs of each miss
   if (FUSED && cta == 0) {
     uint32_t* other = a.counters + 1 + (size_t)(call_set ^ 1u) * a.set_words;
     for (int i = tid; i < a.set_words; i += NCT) other[i] = 0;
@@ -794,29 +825,63 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         named_bar(1, NCT);
       }
       if (tid == 0) MOE_TL(g_ffn_timeline, cta, 7);
-      if (CACHED) {
-        const int n_act = s_n_act;
-        const int n_miss = named_bar_count(1, NCT, tid < n_act && s_act_slot[tid] < 0);
-        if (cta == 0) {
-          if (!s_cab)
-            cache_manager<NCT>(a, n_act, n_miss, s_act_expert, s_act_slot, s_pick_act, s_w, s_clock, s_calls, ring,
-                               (size_t)NS * kStageBytes, xbar);
-          return;   // CTA 0 takes no units
+      const int n_act = s_n_act;
+      // unit order: resident experts first, then the misses (ascending id
+      // within each), and each miss's position in the miss list
+      if (warp == 0) {
+        int nh = 0, nm = 0;
+        for (int i0 = 0; i0 < n_act; i0 += 32) {
+          const int i = i0 + lane;
+          const bool miss = CACHED && i < n_act && s_act_slot[i] < 0;
+          const uint32_t bm = __ballot_sync(0xffffffffu, miss);
+          const uint32_t bh = __ballot_sync(0xffffffffu, i < n_act && !miss);
+          const uint32_t below = (1u << lane) - 1u;
+          if (i < n_act) s_mrank[i] = miss ? nm + __popc(bm & below) : -1;
+          if (i < n_act && !miss) s_order[nh + __popc(bh & below)] = i;
+          nh += __popc(bh);
+          nm += __popc(bm);
         }
-        if (n_miss > 0 && !s_cab &&
-            !pull_and_place_misses<NCT>(a, n_miss, n_act, s_act_slot, xbar, GT, ct, reinterpret_cast<int*>(ovl))) {
-          if (tid == 0) s_abort = 1;
+        for (int i0 = 0; i0 < n_act; i0 += 32) {
+          const int i = i0 + lane;
+          const bool miss = CACHED && i < n_act && s_act_slot[i] < 0;
+          const uint32_t bm = __ballot_sync(0xffffffffu, miss);
+          if (miss) s_order[nh + __popc(bm & ((1u << lane) - 1u))] = i;
+          nh += __popc(bm);
         }
-        if (tid == 0) s_cab = s_abort;
-        named_bar(1, NCT);
       }
-      // this CTA's routed units, handed to the producer
+      const int n_miss = named_bar_count(1, NCT, CACHED && tid < n_act && s_act_slot[tid] < 0);
+      if (CACHED && cta == 0) {
+        if (!s_cab)
+          cache_manager<NCT>(a, n_act, n_miss, s_act_expert, s_act_slot, s_pick_act, s_w, s_clock, s_calls, ring,
+                             (size_t)NS * kStageBytes, vict);
+        return;   // CTA 0 takes no units
+      }
+      // this CTA's routed units, handed to the producer (it streams the
+      // resident experts' units at once and waits per missing expert)
       if (tid == 0) {
-        const int NU = s_cab ? 0 : s_n_act * RG;
+        const int NU = s_cab ? 0 : n_act * RG;
         s_u0 = routed_first(ct, NU, RG, GT);
         s_u1 = routed_first(ct + 1, NU, RG, GT);
         mbar_arrive(plan_ready);
         MOE_TL(g_ffn_timeline, cta, 8);
+      }
+      if (CACHED && n_miss > 0) {
+        // fetch jobs of the misses, spread over the tile CTAs, once CTA 0 has
+        // published the victims
+        if (tid == 0) {
+          if (!s_cab && !wait_flag_geq(vict, 1u, lim)) {
+            set_error(a.err, DEV_TIMEOUT_FLAG);
+            s_abort = 1;
+          }
+          s_cab = s_abort;
+        }
+        named_bar(1, NCT);
+        if (!s_cab) {
+          const int J = n_miss * (2 * RG + RD);
+          constexpr int KPC = (14 * 2048 / 16 + NCT - 1) / NCT;   // 16-byte chunks per thread of a job
+          pull_jobs<NCT, KPC>(a, (int)((int64_t)ct * J / GT), (int)((int64_t)(ct + 1) * J / GT), ovl, ready);
+        }
+        if (tid == 0) MOE_TL(g_ffn_timeline, cta, 12);
       }
       named_bar(1, NCT);
       u = s_u0;
@@ -824,7 +889,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       continue;
     }
     // ================= one unit: expert ai (-1: shared), slice rb ==========
-    const int ai = routed ? u / RG : -1;
+    const int ai = routed ? s_order[u / RG] : -1;
     // gate/up: each warp sums its blocks' input groups
     float acc[BPW][NT][2][4];
 #pragma unroll

@@ -112,9 +112,8 @@ struct FfnArgs {
   Plan* plan;                   // read (after the routing kernel) or written (fused routing)
   float* ypart;                 // [grid][T][d] per-CTA partials of y
   // per-call counters: word 0 counts decode calls; then two sets of
-  // set_words words (router counter | partials counter | cache-mode flags:
-  // victims published, misses pulled, misses placed), used by alternate
-  // calls.  A call uses set (calls before it) & 1, and the set of the call
+  // set_words words (router counter | partials counter | cache mode: victims
+  // published | finished fetch jobs of each miss), used by alternate calls.  A call uses set (calls before it) & 1, and the set of the call
   // before it is zeroed during the call (by the fused kernel's CTA 0, or by
   // the commit kernel on the host-copy miss path).
   uint32_t* counters;
@@ -145,8 +144,9 @@ struct FfnArgs {
   int staging_n;
 };
 
-// words of one per-call counter set of the decode kernel
-constexpr int kDecodeSetWords = 5;
+// words of one per-call counter set of the decode kernel: router counter,
+// partials counter, victims published, finished fetch jobs of each miss
+constexpr int kDecodeSetWords = 3 + kMaxPicks;
 
 // decode kernel modes
 enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2 };

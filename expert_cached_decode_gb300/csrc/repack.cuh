@@ -22,6 +22,50 @@ __device__ __forceinline__ uint32_t field3(uint32_t w0, uint32_t w1, uint32_t w2
   return (uint32_t)((lo >> b) | ((uint64_t)w2 << (64 - b))) & 7u;
 }
 
+// One block from its 32 rows: lane r holds row r's 12-byte group (r0, r1,
+// r2) and its scale; every lane gathers, by shuffles, the codes of its mma
+// fragment pairs and writes its three words, lanes 0-7 the scales.  One whole
+// warp calls it.
+__device__ __forceinline__ void pack_block(uint32_t r0, uint32_t r1, uint32_t r2, uint16_t my_scale, int lane,
+                                           uint8_t* out) {
+  const int g = lane >> 2, c = lane & 3;
+  uint32_t W[3] = {0u, 0u, 0u};
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const int mt = p >> 3, ks = (p >> 2) & 1, r = p & 3;
+    const int prow = mt * 16 + g + 8 * (r & 1);
+    const int k0 = ks * 16 + 2 * c + 8 * (r >> 1);
+    const uint32_t s0 = __shfl_sync(0xffffffffu, r0, prow);
+    const uint32_t s1 = __shfl_sync(0xffffffffu, r1, prow);
+    const uint32_t s2 = __shfl_sync(0xffffffffu, r2, prow);
+    const uint32_t ulo = field3(s0, s1, s2, k0);
+    const uint32_t uhi = field3(s0, s1, s2, k0 + 1);
+    if (p < 15) {
+      const int j = p / 5, fld = p % 5;
+      W[j] |= (ulo << (3 * fld)) | (uhi << (16 + 3 * fld));
+    } else {
+#pragma unroll
+      for (int b = 0; b < 3; ++b) W[b] |= (((ulo >> b) & 1u) << 15) | (((uhi >> b) & 1u) << 31);
+    }
+  }
+  uint32_t* dw = reinterpret_cast<uint32_t*>(out);
+  dw[lane] = W[0];
+  dw[32 + lane] = W[1];
+  dw[64 + lane] = W[2];
+  // scales: lane g8 < 8 writes rows g8, g8+8, g8+16, g8+24
+  const uint32_t sv = my_scale;
+  const uint32_t s_a = __shfl_sync(0xffffffffu, sv, lane & 7);
+  const uint32_t s_b = __shfl_sync(0xffffffffu, sv, (lane & 7) + 8);
+  const uint32_t s_c = __shfl_sync(0xffffffffu, sv, (lane & 7) + 16);
+  const uint32_t s_d = __shfl_sync(0xffffffffu, sv, (lane & 7) + 24);
+  if (lane < 8) {
+    uint2 o;
+    o.x = s_a | (s_b << 16);
+    o.y = s_c | (s_d << 16);
+    *reinterpret_cast<uint2*>(out + kBlockCodeBytes + 8 * lane) = o;
+  }
+}
+
 // Block bi of the expert at `src` (canonical) into the expert at `dst`
 // (device layout); blocks 0 .. 2(f/32)(d/32)-1 are gate/up (row block, group,
 // Wg then Wu), the rest down (row block, group).  One whole warp calls it.
@@ -56,44 +100,7 @@ __device__ __forceinline__ void repack_block(const uint8_t* src, uint8_t* dst, i
   const uint32_t* gp = reinterpret_cast<const uint32_t*>(src + sec_q[mat] + g_index * 12);
   const uint32_t r0 = __ldcg(gp), r1 = __ldcg(gp + 1), r2 = __ldcg(gp + 2);
   const uint16_t my_scale = __ldcg(reinterpret_cast<const unsigned short*>(src + sec_s[mat] + g_index * 2));
-
-  const int g = lane >> 2, c = lane & 3;
-  uint32_t W[3] = {0u, 0u, 0u};
-#pragma unroll
-  for (int p = 0; p < 16; ++p) {
-    const int mt = p >> 3, ks = (p >> 2) & 1, r = p & 3;
-    const int prow = mt * 16 + g + 8 * (r & 1);
-    const int k0 = ks * 16 + 2 * c + 8 * (r >> 1);
-    const uint32_t s0 = __shfl_sync(0xffffffffu, r0, prow);
-    const uint32_t s1 = __shfl_sync(0xffffffffu, r1, prow);
-    const uint32_t s2 = __shfl_sync(0xffffffffu, r2, prow);
-    const uint32_t ulo = field3(s0, s1, s2, k0);
-    const uint32_t uhi = field3(s0, s1, s2, k0 + 1);
-    if (p < 15) {
-      const int j = p / 5, fld = p % 5;
-      W[j] |= (ulo << (3 * fld)) | (uhi << (16 + 3 * fld));
-    } else {
-#pragma unroll
-      for (int b = 0; b < 3; ++b) W[b] |= (((ulo >> b) & 1u) << 15) | (((uhi >> b) & 1u) << 31);
-    }
-  }
-  uint8_t* out = dst + dst_off;
-  uint32_t* dw = reinterpret_cast<uint32_t*>(out);
-  dw[lane] = W[0];
-  dw[32 + lane] = W[1];
-  dw[64 + lane] = W[2];
-  // scales: lane g8 < 8 writes rows g8, g8+8, g8+16, g8+24
-  const uint32_t sv = my_scale;
-  const uint32_t s_a = __shfl_sync(0xffffffffu, sv, lane & 7);
-  const uint32_t s_b = __shfl_sync(0xffffffffu, sv, (lane & 7) + 8);
-  const uint32_t s_c = __shfl_sync(0xffffffffu, sv, (lane & 7) + 16);
-  const uint32_t s_d = __shfl_sync(0xffffffffu, sv, (lane & 7) + 24);
-  if (lane < 8) {
-    uint2 o;
-    o.x = s_a | (s_b << 16);
-    o.y = s_c | (s_d << 16);
-    *reinterpret_cast<uint2*>(out + kBlockCodeBytes + 8 * lane) = o;
-  }
+  pack_block(r0, r1, r2, my_scale, lane, dst + dst_off);
 }
 
 }  // namespace moe
