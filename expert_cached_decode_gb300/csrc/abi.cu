@@ -31,6 +31,7 @@
 #include "moe_gb300.h"
 #include "common.cuh"
 #include "internal.h"
+#include "fetch.cuh"
 
 using namespace moe;
 
@@ -114,6 +115,10 @@ struct moe_ctx {
   int32_t* p_perm = nullptr;
   float* p_wsort = nullptr;
   int32_t* p_inv = nullptr;      // [T*k] sorted row of each pick
+  int32_t* p_miss_expert = nullptr;   // [E] the chunk's misses (cache that can miss)
+  int32_t* p_miss_slot = nullptr;
+  int32_t* p_evicted = nullptr;
+  int32_t* p_info = nullptr;          // [4] misses, distinct, token hits, token misses
   float* p_osort = nullptr;      // [T*k][d] weighted output of each routed pick
   int32_t* p_cursor = nullptr;
   int32_t* p_group_slot = nullptr;
@@ -415,6 +420,10 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->p_perm);
   cudaFree(c->p_wsort);
   cudaFree(c->p_inv);
+  cudaFree(c->p_miss_expert);
+  cudaFree(c->p_miss_slot);
+  cudaFree(c->p_evicted);
+  cudaFree(c->p_info);
   cudaFree(c->p_osort);
   cudaFree(c->p_cursor);
   cudaFree(c->p_group_slot);
@@ -615,6 +624,10 @@ static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
       {reinterpret_cast<void**>(&c->p_perm), (size_t)rows * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_wsort), (size_t)rows * sizeof(float)},
       {reinterpret_cast<void**>(&c->p_inv), (size_t)kMaxPrefillT * c->k * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_miss_expert), (size_t)c->E * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_miss_slot), (size_t)c->E * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_evicted), (size_t)c->E * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_info), 4 * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_osort), (size_t)kMaxPrefillT * c->k * c->d * sizeof(float)},
       {reinterpret_cast<void**>(&c->p_cursor), (size_t)c->E * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_group_slot), (size_t)(c->E + 1) * sizeof(int32_t)},
@@ -731,12 +744,19 @@ static moe_status fill_trace(moe_ctx* c, cudaStream_t s, int T, moe_trace* tr) {
   return MOE_OK;
 }
 
-// Prefill layer-call (T > 16, every key resident): routing on the tensor
-// cores, counting sort by expert, gather, gate/up and down grouped GEMMs.
+// Prefill layer-call (T > 16): routing on the tensor cores; with a cache
+// that can miss, the chunk's cache step (one key per routed expert with
+// tokens) and the fetch of its misses into their victim slots; counting sort
+// by expert, gather, gate/up and down grouped GEMMs, fixed-order combine.
 static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, float* y, cudaStream_t s,
                                   moe_trace* trace) {
-  if (!c->all_resident)
-    return fail(MOE_ERR_UNIMPLEMENTED, "prefill (T > %d) needs every expert resident in this build", kMaxDecodeT);
+  if (!c->all_resident) {
+    if (!c->host_pool_dev)
+      return fail(MOE_ERR_UNIMPLEMENTED, "prefill on a cache that can miss needs a device-mapped host pool");
+    if (c->C < c->E)
+      return fail(MOE_ERR_UNIMPLEMENTED, "prefill on a cache that can miss needs capacity >= n_experts (%d < %d)",
+                  (int)c->C, c->E);
+  }
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(y) % 16)
     return fail(MOE_ERR_INVALID_ARG, "x and y must be 16-byte aligned");
   if (c->f % 128 != 0)
@@ -748,6 +768,35 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   CUDA_TRY(cudaMemsetAsync(c->p_counts, 0, (size_t)(c->E + 1) * sizeof(int32_t), s));
   st = prefill_route(c, layer, x, T, c->p_idx, c->p_w, c->p_counts, s);
   if (st != MOE_OK) return st;
+  if (!c->all_resident) {
+    // the chunk is one layer-call of the cache: decide and commit, then
+    // fetch the misses into their victim slots before the GEMMs read them
+    PrefillCacheArgs ca{};
+    ca.counts = c->p_counts;
+    ca.table = c->table;
+    ca.owner = c->owner;
+    ca.stamp = c->stamp;
+    ca.q_in = c->lruq[c->qcur];
+    ca.q_out = c->lruq[c->qcur ^ 1];
+    ca.q_staged = c->C <= 32768;
+    ca.C = (int)c->C;
+    ca.E = c->E;
+    ca.layer = layer;
+    ca.clock = c->clock;
+    ca.stats = c->stats + (size_t)layer * ST_N;
+    ca.expert_bytes = c->B;
+    ca.group_slot = c->p_group_slot;
+    ca.miss_expert = c->p_miss_expert;
+    ca.miss_slot = c->p_miss_slot;
+    ca.evicted_key = c->p_evicted;
+    ca.info = c->p_info;
+    ca.err = c->err;
+    CUDA_TRY(launch_prefill_cache(ca, s));
+    c->qcur ^= 1;
+    const MissFetch mf{c->p_miss_expert, c->p_miss_slot, c->host_pool_dev, c->P, c->slots, c->B,
+                       layer, c->E, c->d, c->f};
+    CUDA_TRY(launch_prefill_fetch(mf, c->p_info, s, c->num_sms));
+  }
   PrefillPlanArgs pa{};
   pa.counts = c->p_counts;
   pa.cursor = c->p_cursor;
@@ -765,6 +814,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   pa.d = c->d;
   pa.f = c->f;
   pa.layer = layer;
+  pa.account = c->all_resident ? 1 : 0;
   pa.err = c->err;
   CUDA_TRY(launch_prefill_plan(pa, s));
   PrefillScatterArgs sa{};
@@ -830,6 +880,20 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
     trace->n_distinct = distinct;
     trace->token_hits = n;
     trace->token_misses = 0;
+    if (!c->all_resident) {
+      int32_t info[4];
+      CUDA_TRY(cudaMemcpy(info, c->p_info, sizeof(info), cudaMemcpyDeviceToHost));
+      const int m = info[0];
+      if (trace->miss_expert) CUDA_TRY(cudaMemcpy(trace->miss_expert, c->p_miss_expert, m * sizeof(int32_t),
+                                                  cudaMemcpyDeviceToHost));
+      if (trace->miss_slot)
+        CUDA_TRY(cudaMemcpy(trace->miss_slot, c->p_miss_slot, m * sizeof(int32_t), cudaMemcpyDeviceToHost));
+      if (trace->evicted_key)
+        CUDA_TRY(cudaMemcpy(trace->evicted_key, c->p_evicted, m * sizeof(int32_t), cudaMemcpyDeviceToHost));
+      trace->n_miss = m;
+      trace->token_hits = info[2];
+      trace->token_misses = info[3];
+    }
   }
   return MOE_OK;
 }

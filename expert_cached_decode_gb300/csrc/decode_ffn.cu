@@ -57,6 +57,7 @@
 #include "internal.h"
 #include "select.cuh"
 #include "repack.cuh"
+#include "fetch.cuh"
 
 namespace moe {
 
@@ -92,7 +93,7 @@ __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
   const size_t red = (size_t)C::CW * C::NQ * 32 * 4;
   const size_t pull = (size_t)2 * kMaxPicks * 4;
   const size_t cmb = (size_t)C::CW * 32 * 4;
-  const size_t job = (size_t)14 * (d > 1024 ? d : 1024);   // one fetch job of a miss (f <= 1024)
+  const size_t job = fetch_job_bytes(d, 1024);   // one fetch job of a miss (f <= 1024)
   b = b > job ? b : job;
   b = b > sel ? b : sel;
   b = b > red ? b : red;
@@ -362,88 +363,6 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
     a.stats[ST_MISS_BYTES] += (int64_t)m * a.expert_bytes;
     *a.clock = clk + 1;
     *a.counters = calls + 1;   // every CTA read the count before the router barrier
-  }
-}
-
-// One job of a missing expert's fetch: 32 consecutive rows of one matrix of
-// the canonical expert in the host pool (their codes and their scales are
-// two contiguous runs there), re-laid out into the blocks of those rows in
-// the expert's victim slot.  Jobs of miss j: Wg row blocks 0..f/32-1, Wu row
-// blocks 0..f/32-1, Wd row blocks 0..d/32-1.
-struct PullJob {
-  const uint8_t* codes;    // host pool: 32 rows x G groups x 12 B
-  const uint8_t* scales;   // host pool: 32 rows x G groups x 2 B
-  uint8_t* slot;           // the victim slot (device layout)
-  int code_bytes, G, mat, rb, miss;
-};
-
-__device__ __forceinline__ PullJob pull_job(const FfnArgs& a, int q) {
-  const int d = a.d, f = a.f, RG = f / 32, RD = d / 32, JPM = 2 * RG + RD;
-  const int j = q / JPM, r = q - j * JPM;
-  const int e = __ldcg(&a.plan->miss_expert[j]);
-  const int v = __ldcg(&a.plan->miss_slot[j]);
-  const int64_t entry = ((int64_t)a.layer * a.E + e) % a.pool_entries;
-  const uint8_t* src = a.host_pool + entry * a.expert_bytes;
-  const int64_t gq = (int64_t)f * (d / 32) * 12, dq = (int64_t)d * (f / 32) * 12, gs = (int64_t)f * (d / 32) * 2;
-  PullJob J;
-  J.miss = j;
-  J.slot = const_cast<uint8_t*>(a.slots) + (int64_t)v * a.expert_bytes;
-  if (r < 2 * RG) {
-    J.mat = r / RG;
-    J.rb = r - J.mat * RG;
-    J.G = d / 32;
-    J.codes = src + J.mat * gq + (int64_t)J.rb * 32 * J.G * 12;
-    J.scales = src + 2 * gq + dq + J.mat * gs + (int64_t)J.rb * 32 * J.G * 2;
-  } else {
-    J.mat = 2;
-    J.rb = r - 2 * RG;
-    J.G = f / 32;
-    J.codes = src + 2 * gq + (int64_t)J.rb * 32 * J.G * 12;
-    J.scales = src + 2 * gq + dq + 2 * gs + (int64_t)J.rb * 32 * J.G * 2;
-  }
-  J.code_bytes = 32 * J.G * 12;
-  return J;
-}
-
-// Jobs [q0, q1) of this call's misses, by the NTH consumer threads: the job's
-// bytes come from the host pool in 16-byte loads (the next job's loads are
-// in flight while this one is re-laid out) into shared memory `sm`, each warp
-// then writes whole blocks into the victim slot, and ready[miss] counts the
-// finished jobs (release, after a barrier of all NTH threads).  Every byte of
-// a job sits in at most KPC chunks per thread.
-template <int NTH, int KPC>
-__device__ __forceinline__ void pull_jobs(const FfnArgs& a, int q0, int q1, uint8_t* sm, uint32_t* ready) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint4 rg[KPC];
-  auto load = [&](const PullJob& J) {
-    const int ncb = J.code_bytes / 16, n = ncb + J.G * 4;   // scales: 32 rows x G x 2 B = G * 4 chunks
-#pragma unroll
-    for (int i = 0; i < KPC; ++i) {
-      const int c = tid + i * NTH;
-      if (c < n)
-        rg[i] = c < ncb ? reinterpret_cast<const uint4*>(J.codes)[c]
-                        : reinterpret_cast<const uint4*>(J.scales)[c - ncb];
-    }
-  };
-  if (q0 < q1) load(pull_job(a, q0));
-  for (int q = q0; q < q1; ++q) {
-    const PullJob J = pull_job(a, q);
-    const int n = J.code_bytes / 16 + J.G * 4;
-#pragma unroll
-    for (int i = 0; i < KPC; ++i) {
-      const int c = tid + i * NTH;
-      if (c < n) reinterpret_cast<uint4*>(sm)[c] = rg[i];
-    }
-    named_bar(1, NTH);
-    if (q + 1 < q1) load(pull_job(a, q + 1));
-    for (int gi = warp; gi < J.G; gi += NTH / 32) {
-      const uint32_t* cw = reinterpret_cast<const uint32_t*>(sm + (size_t)(lane * J.G + gi) * 12);
-      const uint16_t sc = reinterpret_cast<const uint16_t*>(sm + J.code_bytes)[lane * J.G + gi];
-      const int64_t off = J.mat < 2 ? gu_block_offset(J.rb, gi, J.mat, a.d) : down_block_offset(J.rb, gi, a.d, a.f);
-      pack_block(cw[0], cw[1], cw[2], sc, lane, J.slot + off);
-    }
-    named_bar(1, NTH);
-    if (tid == 0) red_release_add(&ready[J.miss], 1u);   // covers every warp's blocks (after the barrier)
   }
 }
 
@@ -879,7 +798,9 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         if (!s_cab) {
           const int J = n_miss * (2 * RG + RD);
           constexpr int KPC = (14 * 2048 / 16 + NCT - 1) / NCT;   // 16-byte chunks per thread of a job
-          pull_jobs<NCT, KPC>(a, (int)((int64_t)ct * J / GT), (int)((int64_t)(ct + 1) * J / GT), ovl, ready);
+          const MissFetch mf{a.plan->miss_expert, a.plan->miss_slot, a.host_pool, a.pool_entries,
+                             const_cast<uint8_t*>(a.slots), a.expert_bytes, a.layer, a.E, d, f};
+          pull_jobs<NCT, KPC>(mf, (int)((int64_t)ct * J / GT), (int)((int64_t)(ct + 1) * J / GT), ovl, ready);
         }
         if (tid == 0) MOE_TL(g_ffn_timeline, cta, 12);
       }

@@ -187,6 +187,28 @@ struct PrefillPlanArgs {
   int64_t* clock;
   int64_t* stats;
   int T, E, k, d, f, layer;
+  int account;             // stamp the experts and count the call (0: the cache step did)
+  uint32_t* err;
+};
+
+// cache step of a prefill chunk (every routed expert with tokens is one key)
+struct PrefillCacheArgs {
+  const int32_t* counts;   // [E] picks per routed expert
+  int32_t* table;          // [L*E]
+  int32_t* owner;          // [C]
+  int64_t* stamp;          // [C]
+  const int32_t* q_in;     // [C] slots, least recently used first
+  int32_t* q_out;          // [C] the order after this call
+  int q_staged;            // q_in is staged in shared memory (C <= 32768)
+  int C, E, layer;
+  int64_t* clock;
+  int64_t* stats;          // [ST_N] of this layer
+  int64_t expert_bytes;
+  int32_t* group_slot;     // [E] out: slot of each routed expert with tokens, -1 otherwise
+  int32_t* miss_expert;    // [E] out: misses, ascending
+  int32_t* miss_slot;      // [E] out: victim slot of each miss
+  int32_t* evicted_key;    // [E] out: key the victim held (-1: empty)
+  int32_t* info;           // [4] out: misses, distinct experts, token hits, token misses
   uint32_t* err;
 };
 
@@ -253,6 +275,9 @@ cudaError_t launch_prefill_gate_up(const CUtensorMap& tmX, const PrefillGemmArgs
 cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo, const PrefillGemmArgs& a,
                                 cudaStream_t s, int grid);
 cudaError_t launch_prefill_combine(const PrefillCombineArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_cache(const PrefillCacheArgs& a, cudaStream_t s);
+struct MissFetch;
+cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, cudaStream_t s, int num_sms);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
 // whether one CTA of every decode-kernel variant fits on an SM at hidden size d
 cudaError_t decode_ffn_fits(int d, bool* fits);

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillPlanArgs a) {
       ++act;
       slot = a.table[(size_t)a.layer * E + g];
       if (slot < 0) set_error(a.err, DEV_NOT_RESIDENT);
-      else a.stamp[slot] = *a.clock;
+      else if (a.account) a.stamp[slot] = *a.clock;
     }
     a.group_slot[g] = slot;
   }
@@ -130,10 +130,12 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillPlanArgs a) {
     for (int w = 0; w < 32; ++w) n_act += s_warp[w];
     a.n_tiles[0] = n_ntiles * MG;
     a.n_tiles[1] = n_ntiles * MD;
-    a.stats[ST_CALLS] += 1;
-    a.stats[ST_TOK_HIT] += (int64_t)a.T * a.k;
-    a.stats[ST_DIST_HIT] += n_act;
-    *a.clock += 1;
+    if (a.account) {
+      a.stats[ST_CALLS] += 1;
+      a.stats[ST_TOK_HIT] += (int64_t)a.T * a.k;
+      a.stats[ST_DIST_HIT] += n_act;
+      *a.clock += 1;
+    }
   }
 }
 

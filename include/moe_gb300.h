@@ -142,8 +142,14 @@ moe_status moe_route_topk(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32
 
 /* One layer-call: route, look up / fill the cache, run the experts and write
  * y[T][d] (fp32, device).  x[T][d] bf16 (device); x and y 16-byte aligned.  1 <= T <= 16 uses the
- * decode path; larger T (up to 16,384) the prefill path, which needs every
- * key resident and f % 128 == 0 (MOE_ERR_UNIMPLEMENTED otherwise).  Asynchronous on
+ * decode path; larger T (up to 16,384) the prefill path, which needs
+ * f % 128 == 0 and, on a cache that can miss, a device-mapped host pool and
+ * capacity >= n_experts (MOE_ERR_UNIMPLEMENTED otherwise): the chunk is one
+ * layer-call of the cache (its distinct experts are the keys) and its misses
+ * are read by the GPU into their victim slots before the grouped GEMMs.  The
+ * result does not depend on the order in which the GPU ran its work: every
+ * output is summed in a fixed order (shared expert, then the token's picks
+ * in ascending expert id).  Asynchronous on
  * `stream` when every key is resident (see moe_cache_configure) and, with the
  * default MOE_MISS_DEVICE_PULL, also when misses can occur (one kernel launch
  * routes, plans and commits the cache, pulls the misses and runs the

@@ -30,7 +30,12 @@ pytestmark = pytest.mark.gpu
 POOL_ENTRIES = 2048
 
 
-def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None, miss_mode=None):
+def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None, miss_mode=None,
+              prefill=None):
+    """... then, with prefill=(layer, T), one prefill chunk of T tokens at that
+    layer on the warm cache: its cache step (slots, misses, victims, evicted
+    keys, counts) bit-exact against the oracle's and every output within
+    2e-3 * rms."""
     wl = WORKLOADS[cfg_id]
     if overrides:
         wl = dataclasses.replace(wl, **overrides)
@@ -73,12 +78,36 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
                     if (b, l) in ffn_sample:
                         want = oracle_y(memo, l, xs[l, b], oi, ow)
                         assert_close_rms(y.cpu().numpy(), want, what=f"y call {b} layer {l}")
+    if prefill is not None:
+        from moe_inputs import bf16_bits_to_f64
+        from oracle.routing import route
+        from oracle.ffn import layer_forward
+        lp, Tp = prefill
+        xb = s.tokens_many(lp, [10 ** 6], T=Tp)[0]
+        yp = torch.empty((Tp, wl.d), dtype=torch.float32, device="cuda")
+        tr = layer.moe_forward(lp, to_device_bf16(xb), yp, trace=True)
+        _, wr64, b = s.router(lp)
+        pi, pw, _ = route(bf16_bits_to_f64(xb), wr64, b, k)
+        assert np.array_equal(tr["idx"], pi)
+        assert np.abs(tr["w"] - pw).max() <= W_TOL
+        res = so.cache.step(so.key(lp, pi), passes * calls * L)
+        keys = so.key(lp, pi)
+        assert np.array_equal(tr["slot"], res.slots[np.searchsorted(res.keys, keys)])
+        assert np.array_equal(tr["miss_expert"], res.miss_keys - lp * wl.n_experts)
+        assert np.array_equal(tr["miss_slot"], res.miss_slots)
+        assert np.array_equal(tr["evicted_key"], res.evicted)
+        assert tr["token_hits"] == res.token_hits and tr["token_misses"] == res.token_misses
+        assert tr["n_distinct"] == res.keys.size and res.miss_keys.size > 0
+        want = layer_forward(bf16_bits_to_f64(xb), pi, pw, lambda e: so.expert_weights(lp, e), so.shared_weights(lp))
+        assert_close_rms(yp.cpu().numpy(), want, what=f"prefill chunk of {Tp} tokens at layer {lp}")
     owner, stamp = layer.moe_cache_export()
     assert np.array_equal(owner, so.cache.owner)
     assert np.array_equal(stamp, so.cache.stamp)
     tot = layer.moe_cache_stats()
-    assert tot["layer_calls"] == passes * calls * L
-    assert tot["token_hits"] + tot["token_misses"] == passes * calls * L * T * k
+    n_calls = passes * calls * L + (prefill is not None)
+    picks = passes * calls * L * T * k + (prefill[1] * k if prefill is not None else 0)
+    assert tot["layer_calls"] == n_calls
+    assert tot["token_hits"] + tot["token_misses"] == picks
     layer.close()
     return meas["hits"] / meas["picks"], tot, st
 
@@ -90,7 +119,8 @@ def test_small_stack_with_evictions(miss_mode, tokens):
     # one-token calls take the selection's single-token path
     over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=tokens, capacity=40, calls=60)
     rate, tot, _ = run_stack(3, passes=2, pool_entries=96, overrides=over,
-                             ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode)
+                             ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode,
+                             prefill=(2, 300) if miss_mode == MOE_MISS_DEVICE_PULL else None)
     assert tot["evictions"] > 0 and tot["token_misses"] > 0
     assert 0.0 < rate < 1.0
 
@@ -99,7 +129,9 @@ def test_verify_stack_full():
     # T=5 verify batch, Zipf s=1.1, 3 warm-up passes + the measured pass
     wl = WORKLOADS[3]
     sample = {(0, 0), (1, 47), (1000, 23), (1999, 5)}
-    rate, tot, st = run_stack(3, passes=wl.warm_passes + 1, pool_entries=POOL_ENTRIES, ffn_sample=sample)
+    # then a 12,288-token prefill chunk at layer 7 on the warm 8,445-slot cache
+    rate, tot, st = run_stack(3, passes=wl.warm_passes + 1, pool_entries=POOL_ENTRIES, ffn_sample=sample,
+                              prefill=(7, 12288))
     print(f"verify stack: measured-pass token hit rate {rate:.4f}; totals {tot}")
     # the pages' regime: 94-99% (one RTX 4090) and 91-95% at 48% coverage
     assert 0.93 <= rate <= 0.97
