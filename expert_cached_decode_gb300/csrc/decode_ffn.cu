@@ -708,7 +708,11 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         named_bar(1, NCT);
         if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
         if (!s_cab) {
+#ifdef MOE_TIMELINE
+          select_call<NCT>(a.logits, T, E, K, sel, &g_ffn_timeline[cta][16]);
+#else
           select_call<NCT>(a.logits, T, E, K, sel);
+#endif
           const int n_act = sel->n_act;
           for (int i = tid; i < T * K; i += NCT) {
             const int id = sel->sel_id[i / K][i % K];
@@ -840,6 +844,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 13);
     // partials -> shared memory, [warp][q][lane] with q = ((j*NT + nt)*2 + mt)*4 + i
 #pragma unroll
     for (int j = 0; j < BPW; ++j)
@@ -886,6 +891,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       hs[tok * kHsRow + row] = __float2half_rn(hv);
     }
     named_bar(1, NCT);
+    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 14);
     // B fragments of the down products (k = the slice's 32 rows of f)
     uint2 hf[NT][2];
 #pragma unroll
@@ -915,6 +921,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         ++it;
       }
     }
+    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 15);
     ++u;
   }
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 9);
@@ -959,16 +966,16 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     const int t = item / RD, rbd = item - t * RD;
     const float* src = a.ypart + (size_t)t * d + rbd * 32 + lane;
     float v = 0.f;
-    int c = c0;
-    for (; c + 4 <= c1; c += 4) {
-      const float v0 = __ldcg(src + (size_t)c * cstride), v1 = __ldcg(src + (size_t)(c + 1) * cstride);
-      const float v2 = __ldcg(src + (size_t)(c + 2) * cstride), v3 = __ldcg(src + (size_t)(c + 3) * cstride);
-      v += v0;
-      v += v1;
-      v += v2;
-      v += v3;
+    // every load of a batch in flight before the sum (one batch covers a
+    // warp's share on grids of up to 160 CTAs)
+    constexpr int kBatch = (160 + CW - 1) / CW;
+    for (int cb = c0; cb < c1; cb += kBatch) {
+      float pv[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) pv[q] = cb + q < c1 ? __ldcg(src + (size_t)(cb + q) * cstride) : 0.f;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) v += pv[q];
     }
-    for (; c < c1; ++c) v += __ldcg(src + (size_t)c * cstride);
     cmb[warp * 32 + lane] = v;
     named_bar(1, NCT);
     if (warp == 0) {
