@@ -15,8 +15,8 @@
 // the router's logits and the final sum of the per-CTA partials.
 //
 // One persistent CTA per SM.  Warps: CW consumer warps, a producer warp
-// (one thread streams every unit through a ring of 16-block stages with bulk
-// TMA copies, mbarrier completion) and a control warp.  Per call:
+// (one thread streams every unit through a ring of stages of 2*CW blocks with
+// bulk TMA copies, mbarrier completion) and a control warp.  Per call:
 //   1. the producer starts the shared expert's units of this CTA at once
 //      (static weights, issued even before the previous call has finished);
 //   2. consumers stage x (bf16 for the router, fp16 mma fragments for the
@@ -34,14 +34,14 @@
 // units are split in contiguous ranges so that every CTA's total count of
 // units is even.
 //
-// Inside a unit: gate/up stages give each consumer warp 16/CW blocks (one
-// input group; Wg and Wu of it when CW = 8, one of them when CW = 16).
-// Codes are expanded to exact fp16 q in registers (one LOP3 + one HFMA2 per
-// code pair), multiplied on the tensor cores (mma.sync m16n8k16, fp32
-// accumulate) and scaled per group in fp32.  The warps' partial sums meet in
-// shared memory, are added in warp order and give h (fp16, times the token's
-// routing weight) as the B operand of the down stages, where warp w owns the
-// row blocks w*16/CW + j (+ 16 per stage) of y for the whole call.
+// Inside a unit: every gate/up stage gives each consumer warp two blocks, the
+// Wg and Wu blocks of one input group.  Codes are expanded to exact fp16 q in
+// registers (one LOP3 + one HFMA2 per code pair), multiplied on the tensor
+// cores (mma.sync m16n8k16, fp32 accumulate) and scaled per group in fp32.
+// The warps' partial sums meet in shared memory, are added in warp order and
+// give h (fp16, times the token's routing weight) as the B operand of the
+// down stages, where warp w owns the row blocks 2w + j (+ 2*CW per stage) of
+// y for the whole call.
 //
 // With a cache that can miss, CTA 0 takes no units and runs the cache (LRU
 // victims, commit, next LRU order, plan).  CTAs 1..G-1 order their routed
@@ -65,18 +65,19 @@ namespace moe {
 __device__ unsigned long long g_ffn_timeline[512][32];
 #endif
 
-constexpr int kStageBlocks = 16;
-constexpr int kStageBytes = kStageBlocks * kBlockBytes;   // 7,168
-constexpr int kMaxSDN = 4;                                 // down stages of a unit (d <= 2048)
+constexpr int kMaxRD = 64;                                 // row blocks of d (d <= 2048)
 constexpr int kHsRow = 40;                                 // fp16 per token row of a unit's h (32 + pad)
 
 template <int NT>
 struct DCfg {
   static constexpr int CW = NT == 1 ? 16 : 8;      // consumer warps
-  static constexpr int BPW = 16 / CW;              // blocks of a stage per consumer warp
+  static constexpr int SB = 2 * CW;                // blocks per ring stage: two per consumer warp
+  static constexpr int BPW = 2;                    // blocks of a stage per consumer warp
+  static constexpr int SBYTES = SB * kBlockBytes;  // bytes per ring stage
   static constexpr int THREADS = (CW + 2) * 32;    // + producer and control warps
-  static constexpr int NS = NT == 1 ? 20 : 10;     // ring stages
+  static constexpr int NS = NT == 1 ? 10 : 10;     // ring stages (140 KB / 70 KB)
   static constexpr int NQ = BPW * 8 * NT;          // gate/up partial floats per lane
+  static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
 
 // elements per staged x row (bf16, router input): 32 bytes of padding
@@ -105,7 +106,7 @@ __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
 template <int NT>
 __host__ __device__ __forceinline__ size_t ffn_smem_bytes(int d) {
   using C = DCfg<NT>;
-  return (size_t)C::NS * kStageBytes + (size_t)NT * d * 16 + overlay_bytes<NT>(d) + (size_t)NT * 8 * kHsRow * 2 +
+  return (size_t)C::NS * C::SBYTES + (size_t)NT * d * 16 + overlay_bytes<NT>(d) + (size_t)NT * 8 * kHsRow * 2 +
          (2 * C::NS + 1) * 8;
 }
 
@@ -373,7 +374,8 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
 template <int NT, int MODE>
 __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArgs a) {
   using Cfg = DCfg<NT>;
-  constexpr int CW = Cfg::CW, BPW = Cfg::BPW, NS = Cfg::NS, NQ = Cfg::NQ;
+  constexpr int CW = Cfg::CW, BPW = Cfg::BPW, NS = Cfg::NS, NQ = Cfg::NQ, SB = Cfg::SB, MAXSDN = Cfg::MAXSDN;
+  constexpr int SBYTES = Cfg::SBYTES;
   constexpr int NCT = CW * 32;   // consumer threads (named barrier 1)
   constexpr bool FUSED = MODE != kPlanRead;
   constexpr bool CACHED = MODE == kFusedCached;
@@ -381,12 +383,13 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   const int d = a.d, f = a.f, T = a.T, K = a.k;
   const int RG = f / 32;            // f slices = units per expert
   const int RD = d / 32;            // row blocks of d
-  const int SGU = d / 256;          // gate/up stages per unit
-  const int SDN = (RD + 15) / 16;   // down stages per unit
+  const int NGU = d / 16;           // gate/up blocks per unit
+  const int SGU = (NGU + SB - 1) / SB;   // gate/up stages per unit (the last may be partial)
+  const int SDN = (RD + SB - 1) / SB;    // down stages per unit
   const int nks = d / 16;
   const uint64_t lim = a.wait_ns;
   uint8_t* ring = smem;
-  uint2* xfrag = reinterpret_cast<uint2*>(smem + (size_t)NS * kStageBytes);
+  uint2* xfrag = reinterpret_cast<uint2*>(smem + (size_t)NS * SBYTES);
   uint8_t* ovl = reinterpret_cast<uint8_t*>(xfrag) + (size_t)NT * d * 16;
   __half* hs = reinterpret_cast<__half*>(ovl + overlay_bytes<NT>(d));
   uint64_t* full = reinterpret_cast<uint64_t*>(hs + NT * 8 * kHsRow);
@@ -453,16 +456,18 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         const uint8_t* src;
         uint32_t bytes;
         if (st < SGU) {
-          src = gu + (size_t)st * kStageBytes;
-          bytes = kStageBytes;
+          const int b0 = st * SB;
+          const int nb = NGU - b0 < SB ? NGU - b0 : SB;
+          src = gu + (size_t)b0 * kBlockBytes;
+          bytes = (uint32_t)nb * kBlockBytes;
         } else {
-          const int b0 = (st - SGU) * kStageBlocks;
-          const int nb = RD - b0 < kStageBlocks ? RD - b0 : kStageBlocks;
+          const int b0 = (st - SGU) * SB;
+          const int nb = RD - b0 < SB ? RD - b0 : SB;
           src = dn + (size_t)b0 * kBlockBytes;
           bytes = (uint32_t)nb * kBlockBytes;
         }
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(ring + (size_t)s * kStageBytes, src, bytes, &full[s]);
+        bulk_g2s(ring + (size_t)s * SBYTES, src, bytes, &full[s]);
       }
       return true;
     };
@@ -670,10 +675,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
 
   // ---- units: the CTA's shared-expert units, then (after the routing
   // result) its routed units.  Warp w owns the row blocks
-  // sd*16 + w*BPW + j of y (sd < SDN, j < BPW) in every down stage.
-  float yacc[kMaxSDN][BPW][NT][2][4];
+  // sd*SB + w*BPW + j of y (sd < SDN, j < BPW) in every down stage.
+  float yacc[MAXSDN][BPW][NT][2][4];
 #pragma unroll
-  for (int sd = 0; sd < kMaxSDN; ++sd)
+  for (int sd = 0; sd < MAXSDN; ++sd)
 #pragma unroll
     for (int j = 0; j < BPW; ++j)
 #pragma unroll
@@ -776,7 +781,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       if (CACHED && cta == 0) {
         if (!s_cab)
           cache_manager<NCT>(a, n_act, n_miss, s_act_expert, s_act_slot, s_pick_act, s_w, s_clock, s_calls, ring,
-                             (size_t)NS * kStageBytes, vict);
+                             (size_t)NS * SBYTES, vict);
         return;   // CTA 0 takes no units
       }
       // this CTA's routed units, handed to the producer (it streams the
@@ -829,9 +834,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     for (int st = 0; st < SGU; ++st, ++it) {
       const int s = it % NS;
       stage_wait(s, (it / NS) & 1);
-      if (!s_abort) {
-        const uint8_t* sp = ring + (size_t)s * kStageBytes;
-        const int gi = st * 8 + ((warp * BPW) >> 1);   // input group of this warp's blocks
+      // this warp's two blocks: Wg and Wu of input group st*SB/2 + warp
+      if (!s_abort && st * SB + warp * BPW < NGU) {
+        const uint8_t* sp = ring + (size_t)s * SBYTES;
+        const int gi = st * (SB / 2) + warp;
         uint2 bx[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -862,18 +868,11 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     for (int p = tid; p < 256 * NT; p += NCT) {
       const int ln = p & 31, r8 = p >> 5;   // r8 = (nt*2 + mt)*4 + i
       float g = 0.f, uu = 0.f;
-      if (BPW == 1) {   // even warps hold Wg partials, odd warps Wu partials
+      // every warp holds both (j = 0: Wg, j = 1: Wu)
 #pragma unroll
-        for (int v = 0; v < CW / 2; ++v) {
-          g += red[((size_t)(2 * v) * NQ + r8) * 32 + ln];
-          uu += red[((size_t)(2 * v + 1) * NQ + r8) * 32 + ln];
-        }
-      } else {          // every warp holds both (j = 0: Wg, j = 1: Wu)
-#pragma unroll
-        for (int w = 0; w < CW; ++w) {
-          g += red[((size_t)w * NQ + r8) * 32 + ln];
-          uu += red[((size_t)w * NQ + NT * 8 + r8) * 32 + ln];
-        }
+      for (int w = 0; w < CW; ++w) {
+        g += red[((size_t)w * NQ + r8) * 32 + ln];
+        uu += red[((size_t)w * NQ + NT * 8 + r8) * 32 + ln];
       }
       const int i = r8 & 3, mt = (r8 >> 2) & 1, nt = r8 >> 3;
       const int row = mt * 16 + (ln >> 2) + 8 * (i >> 1);
@@ -902,18 +901,18 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       hf[nt][1].x = hr[cq + 8];
       hf[nt][1].y = hr[cq + 12];
     }
-    // down: row blocks sd*16 + b of d, b = warp*BPW + j
+    // down: row blocks sd*SB + b of d, b = warp*BPW + j
 #pragma unroll
-    for (int sd = 0; sd < kMaxSDN; ++sd) {
+    for (int sd = 0; sd < MAXSDN; ++sd) {
       if (sd < SDN) {
         const int s = it % NS;
         stage_wait(s, (it / NS) & 1);
         if (!s_abort) {
-          const uint8_t* sp = ring + (size_t)s * kStageBytes;
+          const uint8_t* sp = ring + (size_t)s * SBYTES;
 #pragma unroll
           for (int j = 0; j < BPW; ++j) {
             const int b = warp * BPW + j;
-            if (sd * kStageBlocks + b < RD) block_mma<NT>(sp + b * kBlockBytes, lane, hf, yacc[sd][j]);
+            if (sd * SB + b < RD) block_mma<NT>(sp + b * kBlockBytes, lane, hf, yacc[sd][j]);
           }
         }
         __syncwarp();
@@ -929,10 +928,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   // ---- this CTA's partial of y -> ypart[ct][t][row] ------------------------
   float* const yp = a.ypart + (size_t)ct * T * d;
 #pragma unroll
-  for (int sd = 0; sd < kMaxSDN; ++sd)
+  for (int sd = 0; sd < MAXSDN; ++sd)
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
-      const int rbd = sd * kStageBlocks + warp * BPW + j;
+      const int rbd = sd * SB + warp * BPW + j;
       if (sd < SDN && rbd < RD) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -999,7 +998,7 @@ template <int NT, int MODE>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   constexpr int NCT = DCfg<NT>::CW * 32;
   const size_t smem = ffn_smem_bytes<NT>(a.d);
-  if (a.d % 256 != 0 || a.d > kStageBlocks * 32 * kMaxSDN || a.f % 32 != 0 || a.T > NT * 8 || a.T * a.k > NCT)
+  if (a.d % 256 != 0 || a.d > kMaxRD * 32 || a.f % 32 != 0 || a.T > NT * 8 || a.T * a.k > NCT)
     return cudaErrorInvalidValue;
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_ffn_kernel<NT, MODE>), smem);
   if (e != cudaSuccess) return e;
