@@ -53,6 +53,8 @@
 // count before it streams that expert's units.  With host-issued miss copies
 // the kernel follows the routing kernel and reads its plan.  All waits are
 // bounded.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -80,6 +82,164 @@ struct DCfg {
   static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
 
+// Selection of one call (shared memory): the per-warp candidates of the
+// first level (one token), the chosen experts of every token and the
+// distinct set U.
+struct DSel {
+  uint32_t ckey[16][kMaxTopK];        // level-1 candidates of each warp
+  int cid[16][kMaxTopK];
+  uint32_t mask[kMaxE / 32];          // chosen experts of the call
+  int word_base[kMaxE / 32];          // distinct experts below word i
+  int sel_id[kMaxDecodeT][kMaxTopK];  // per token, ascending id
+  float sel_w[kMaxDecodeT][kMaxTopK];
+  int act[kMaxPicks];                 // distinct experts U, ascending
+  int n_act;
+};
+
+// Index in U of chosen expert `id`.
+__device__ __forceinline__ int dsel_act_index(const DSel* s, int id) {
+  return s->word_base[id >> 5] + __popc(s->mask[id >> 5] & ((1u << (id & 31)) - 1u));
+}
+
+// K rounds over the (key, id) pairs held by a warp (VPL per lane; key 0 =
+// no entry; keys are order-preserving images of the logits): each round the
+// largest remaining key leaves, ties to the lower id.  Lane r receives the
+// r-th largest pair.
+template <int VPL>
+__device__ __forceinline__ void warp_rounds_topk(uint32_t (&key)[VPL], const int (&id)[VPL], int K, int lane,
+                                                 uint32_t& out_key, int& out_id) {
+  out_key = 0;
+  out_id = 0x7fffffff;
+  for (int r = 0; r < K; ++r) {
+    uint32_t bk = 0;
+    int bid = 0x7fffffff, bi = -1;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      if (key[i] != 0 && (key[i] > bk || (key[i] == bk && id[i] < bid))) {
+        bk = key[i];
+        bid = id[i];
+        bi = i;
+      }
+    }
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, bk == mx ? (uint32_t)bid : 0xffffffffu);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (i == bi && bk == mx && (uint32_t)bid == win) key[i] = 0;   // ids are distinct: one owner
+    if (lane == r) {
+      out_key = mx;
+      out_id = (int)win;
+    }
+  }
+}
+
+// lane r < K holds the r-th largest (key, id) of token t: routing weights
+// (softmax over the chosen logits, which equals the renormalised softmax
+// over all E), ids in ascending order, the call's expert mask
+__device__ __forceinline__ void dsel_finish(DSel* s, int t, int K, int lane, uint32_t key, int id) {
+  const float v = key_float(key);
+  const float top = __shfl_sync(0xffffffffu, v, 0);
+  const float ex = lane < K ? expf(v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  int rank = 0;
+  for (int j = 0; j < K; ++j) rank += __shfl_sync(0xffffffffu, id, j) < id ? 1 : 0;
+  if (lane < K) {
+    s->sel_id[t][rank] = id;
+    s->sel_w[t][rank] = ex / sum;
+    atomicOr(&s->mask[id >> 5], 1u << (id & 31));
+  }
+}
+
+// Top-k of every token of the call from the logits rows [T][E] (written by
+// every CTA of this launch, read through L2), by the NTH threads of named
+// barrier 1 (CW warps).  One token: every warp finds the top-k of its share
+// of the row, then warp 0 the top-k of the CW*K candidates.  Several tokens:
+// one warp per token, K rounds over the whole row.  Then U.
+template <int NTH, int CW>
+__device__ __forceinline__ void dsel_call(const float* logits, int T, int E, int K, DSel* s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kMaxE / 32; i += NTH) s->mask[i] = 0;
+  if (T == 1) {
+    constexpr int V1 = (kMaxE + 32 * CW - 1) / (32 * CW);
+    uint32_t key[V1];
+    int id[V1];
+#pragma unroll
+    for (int i = 0; i < V1; ++i) {
+      id[i] = (warp * V1 + i) * 32 + lane;
+      key[i] = id[i] < E ? float_key(ld_cg_f32(logits + id[i])) : 0u;
+    }
+    uint32_t ck;
+    int ci;
+    warp_rounds_topk<V1>(key, id, K, lane, ck, ci);
+    if (lane < K) {
+      s->ckey[warp][lane] = ck;
+      s->cid[warp][lane] = ci;
+    }
+    named_bar(1, NTH);
+    if (warp == 0) {
+      constexpr int V2 = (CW * kMaxTopK + 31) / 32;
+      uint32_t k2[V2];
+      int i2[V2];
+#pragma unroll
+      for (int j = 0; j < V2; ++j) {
+        const int c = lane + 32 * j;
+        const bool ok = c < CW * K;
+        k2[j] = ok ? s->ckey[c / K][c % K] : 0u;
+        i2[j] = ok ? s->cid[c / K][c % K] : 0x7fffffff;
+      }
+      uint32_t fk;
+      int fi;
+      warp_rounds_topk<V2>(k2, i2, K, lane, fk, fi);
+      dsel_finish(s, 0, K, lane, fk, fi);
+    }
+  } else {
+    named_bar(1, NTH);   // the mask is clear
+    auto rows = [&](auto vr) {
+      constexpr int VR = decltype(vr)::value;
+      for (int t = warp; t < T; t += CW) {
+        uint32_t key[VR];
+        int id[VR];
+#pragma unroll
+        for (int i = 0; i < VR; ++i) {
+          id[i] = i * 32 + lane;
+          key[i] = id[i] < E ? float_key(ld_cg_f32(logits + (size_t)t * E + id[i])) : 0u;
+        }
+        uint32_t ck;
+        int ci;
+        warp_rounds_topk<VR>(key, id, K, lane, ck, ci);
+        dsel_finish(s, t, K, lane, ck, ci);
+      }
+    };
+    if (E <= 512) rows(std::integral_constant<int, 16>{});
+    else rows(std::integral_constant<int, kMaxE / 32>{});
+  }
+  named_bar(1, NTH);
+  const int n_words = (E + 31) / 32;
+  if (warp == 0) {
+    const uint32_t m = lane < n_words ? s->mask[lane] : 0u;
+    const int c = __popc(m);
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    const int base = inc - c;
+    if (lane < n_words) s->word_base[lane] = base;
+    if (lane == 31) s->n_act = inc;
+    uint32_t mm = m;
+    int pos = base;
+    while (mm) {
+      const int bit = __ffs(mm) - 1;
+      mm &= mm - 1;
+      s->act[pos++] = lane * 32 + bit;
+    }
+  }
+  named_bar(1, NTH);
+}
+
 // elements per staged x row (bf16, router input): 32 bytes of padding
 __host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
 
@@ -90,7 +250,7 @@ template <int NT>
 __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
   using C = DCfg<NT>;
   size_t b = (size_t)NT * 8 * x_row_elems(d) * 2;
-  const size_t sel = (sizeof(SelSmem) + 15) & ~size_t(15);
+  const size_t sel = (sizeof(DSel) + 15) & ~size_t(15);
   const size_t red = (size_t)C::CW * C::NQ * 32 * 4;
   const size_t pull = (size_t)2 * kMaxPicks * 4;
   const size_t cmb = (size_t)C::CW * 32 * 4;
@@ -143,33 +303,51 @@ __device__ __forceinline__ void scales4(const uint8_t* bp, int lane, float s[4])
   s[3] = hi.y;   // row g+24
 }
 
-// One 32x32 block: acc[nt][mt] += scale(row) * (A_block . B_frag[nt]), the
-// product in fp32 on the tensor cores, the scale of the lane's rows g, g+8,
-// g+16, g+24 applied in fp32.
+// Two 32x32 blocks of one warp: acc_j[nt][mt] += scale(row) * (A_j . B[nt])
+// for j = 0, 1 (blocks at bp0, bp1, with the same B fragments), products in
+// fp32 on the tensor cores, the scale of the lane's rows g, g+8, g+16, g+24
+// applied in fp32.  Both blocks' codes are expanded before the products, and
+// the first k-step of every tile is issued before the second, so eight
+// independent products overlap their latency.
 template <int NT>
-__device__ __forceinline__ void block_mma(const uint8_t* bp, int lane, const uint2 (&bx)[NT][2],
-                                          float (&acc)[NT][2][4]) {
-  const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
-  const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
-  float s[4];
-  scales4(bp, lane, s);
-  uint32_t A[16];
-  dequant_block(w0, w1, w2, A);
+__device__ __forceinline__ void block_pair_mma(const uint8_t* bp0, const uint8_t* bp1, int lane,
+                                               const uint2 (&bx)[NT][2], float (&acc0)[NT][2][4],
+                                               float (&acc1)[NT][2][4]) {
+  const uint32_t* w0p = reinterpret_cast<const uint32_t*>(bp0);
+  const uint32_t* w1p = reinterpret_cast<const uint32_t*>(bp1);
+  const uint32_t a0 = w0p[lane], a1 = w0p[32 + lane], a2 = w0p[64 + lane];
+  const uint32_t b0 = w1p[lane], b1 = w1p[32 + lane], b2 = w1p[64 + lane];
+  float s0[4], s1[4];
+  scales4(bp0, lane, s0);
+  scales4(bp1, lane, s1);
+  uint32_t A0[16], A1[16];
+  dequant_block(a0, a1, a2, A0);
+  dequant_block(b0, b1, b2, A1);
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+  float D0[NT][2][4], D1[NT][2][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      float D[4];
-      mma_16816(D, &A[mt * 8], bx[nt][0].x, bx[nt][0].y, zero);
-      mma_16816(D, &A[mt * 8 + 4], bx[nt][1].x, bx[nt][1].y, D);
-      const float sa = s[2 * mt], sb = s[2 * mt + 1];
-      acc[nt][mt][0] = fmaf(sa, D[0], acc[nt][mt][0]);
-      acc[nt][mt][1] = fmaf(sa, D[1], acc[nt][mt][1]);
-      acc[nt][mt][2] = fmaf(sb, D[2], acc[nt][mt][2]);
-      acc[nt][mt][3] = fmaf(sb, D[3], acc[nt][mt][3]);
+      mma_16816(D0[nt][mt], &A0[mt * 8], bx[nt][0].x, bx[nt][0].y, zero);
+      mma_16816(D1[nt][mt], &A1[mt * 8], bx[nt][0].x, bx[nt][0].y, zero);
     }
-  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      mma_16816(D0[nt][mt], &A0[mt * 8 + 4], bx[nt][1].x, bx[nt][1].y, D0[nt][mt]);
+      mma_16816(D1[nt][mt], &A1[mt * 8 + 4], bx[nt][1].x, bx[nt][1].y, D1[nt][mt]);
+    }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc0[nt][mt][i] = fmaf(s0[2 * mt + (i >> 1)], D0[nt][mt][i], acc0[nt][mt][i]);
+        acc1[nt][mt][i] = fmaf(s1[2 * mt + (i >> 1)], D1[nt][mt][i], acc1[nt][mt][i]);
+      }
 }
 
 // exclusive prefix sum over the NTH threads of named barrier 1 (every one of
@@ -396,7 +574,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   uint64_t* empty = full + NS;
   uint64_t* plan_ready = empty + NS;
   uint16_t* xraw = reinterpret_cast<uint16_t*>(ovl);   // router input rows
-  SelSmem* sel = reinterpret_cast<SelSmem*>(ovl);      // selection
+  DSel* sel = reinterpret_cast<DSel*>(ovl);            // selection
   float* red = reinterpret_cast<float*>(ovl);          // gate/up partials [CW][NQ][32]
   float* cmb = reinterpret_cast<float*>(ovl);          // combine partials [CW][32]
 
@@ -408,6 +586,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   __shared__ int s_order[kMaxPicks];      // distinct experts in unit order (resident ones first)
   __shared__ int s_mrank[kMaxPicks];      // position of each distinct expert in the miss list, -1 if resident
   __shared__ int s_n_act, s_u0, s_u1;
+  __shared__ float s_wu[16];              // routing weight of each token for the current unit's expert
   __shared__ uint32_t s_calls;
   __shared__ long long s_clock;
   // s_abort: set by any warp whose bounded wait gave up (consumers then skip
@@ -445,7 +624,9 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     if (lane != 0 || ct < 0) return;
     uint32_t it = 0;
     bool ok = true;
+    const uint64_t pol_stream = l2_evict_first_policy(), pol_keep = l2_evict_last_policy();
     auto issue_unit = [&](const uint8_t* eb, int rb) -> bool {
+      const uint64_t pol = eb == a.shared_expert ? pol_keep : pol_stream;
       const uint8_t* gu = eb + gu_block_offset(rb, 0, 0, d);
       const uint8_t* dn = eb + down_block_offset(0, rb, d, f);
       for (int st = 0; st < SGU + SDN; ++st, ++it) {
@@ -467,7 +648,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
           bytes = (uint32_t)nb * kBlockBytes;
         }
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(ring + (size_t)s * SBYTES, src, bytes, &full[s]);
+        bulk_g2s_hint(ring + (size_t)s * SBYTES, src, bytes, &full[s], pol);
       }
       return true;
     };
@@ -691,11 +872,15 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   uint32_t it = 0;   // ring stage counter (the producer's order)
   bool routed = false;
   int u = sh0, u_end = sh1;
-  auto stage_wait = [&](int s, uint32_t par) {
-    if (!s_abort && !mbar_wait(&full[s], par, lim)) {
+  // waits for stage s (bounded); false once any warp of the CTA gave up
+  auto stage_wait = [&](int s, uint32_t par) -> bool {
+    if (s_abort) return false;
+    if (!mbar_wait(&full[s], par, lim)) {
       set_error(a.err, DEV_TIMEOUT_BARRIER);
       s_abort = 1;
+      return false;
     }
+    return true;
   };
   for (;;) {
     if (u >= u_end) {
@@ -713,15 +898,12 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         named_bar(1, NCT);
         if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
         if (!s_cab) {
-#ifdef MOE_TIMELINE
-          select_call<NCT>(a.logits, T, E, K, sel, &g_ffn_timeline[cta][16]);
-#else
-          select_call<NCT>(a.logits, T, E, K, sel);
-#endif
+          dsel_call<NCT, CW>(a.logits, T, E, K, sel);
+          if (tid == 0) MOE_TL(g_ffn_timeline, cta, 16);
           const int n_act = sel->n_act;
           for (int i = tid; i < T * K; i += NCT) {
             const int id = sel->sel_id[i / K][i % K];
-            s_pick_act[i] = sel_act_index(sel, id);
+            s_pick_act[i] = dsel_act_index(sel, id);
             s_w[i] = sel->sel_w[i / K][i % K];
           }
           for (int i = tid; i < n_act; i += NCT) {
@@ -820,6 +1002,20 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
     // ================= one unit: expert ai (-1: shared), slice rb ==========
     const int ai = routed ? s_order[u / RG] : -1;
+    // the routing weight of each token for this expert (0 for a token not
+    // routed to it); read in the h step, after the next barrier
+    if (warp == 0 && lane < NT * 8) {
+      float wt = 0.f;
+      if (lane < T) {
+        if (ai < 0) {
+          wt = a.shared_weight;
+        } else {
+          for (int k2 = 0; k2 < K; ++k2)
+            if (s_pick_act[lane * K + k2] == ai) wt = s_w[lane * K + k2];
+        }
+      }
+      s_wu[lane] = wt;
+    }
     // gate/up: each warp sums its blocks' input groups
     float acc[BPW][NT][2][4];
 #pragma unroll
@@ -833,9 +1029,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
 #pragma unroll 1
     for (int st = 0; st < SGU; ++st, ++it) {
       const int s = it % NS;
-      stage_wait(s, (it / NS) & 1);
       // this warp's two blocks: Wg and Wu of input group st*SB/2 + warp
-      if (!s_abort && st * SB + warp * BPW < NGU) {
+      if (stage_wait(s, (it / NS) & 1) && st * SB + warp * BPW < NGU) {
         const uint8_t* sp = ring + (size_t)s * SBYTES;
         const int gi = st * (SB / 2) + warp;
         uint2 bx[NT][2];
@@ -844,8 +1039,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
           bx[nt][0] = xfrag[((size_t)nt * nks + gi * 2 + 0) * 32 + lane];
           bx[nt][1] = xfrag[((size_t)nt * nks + gi * 2 + 1) * 32 + lane];
         }
-#pragma unroll
-        for (int j = 0; j < BPW; ++j) block_mma<NT>(sp + (warp * BPW + j) * kBlockBytes, lane, bx, acc[j]);
+        block_pair_mma<NT>(sp + (warp * BPW) * kBlockBytes, sp + (warp * BPW + 1) * kBlockBytes, lane, bx, acc[0],
+                           acc[1]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -877,16 +1072,9 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       const int i = r8 & 3, mt = (r8 >> 2) & 1, nt = r8 >> 3;
       const int row = mt * 16 + (ln >> 2) + 8 * (i >> 1);
       const int tok = nt * 8 + 2 * (ln & 3) + (i & 1);
-      float wt = 0.f;
-      if (tok < T) {
-        if (ai < 0) {
-          wt = a.shared_weight;
-        } else {
-          for (int k2 = 0; k2 < K; ++k2)
-            if (s_pick_act[tok * K + k2] == ai) wt = s_w[tok * K + k2];
-        }
-      }
-      const float hv = g / (1.f + expf(-g)) * uu * wt;
+      // silu with the fast exponential and division (relative error ~2^-21,
+      // far below the fp16 rounding of h)
+      const float hv = __fdividef(g, 1.f + __expf(-g)) * uu * s_wu[tok];
       hs[tok * kHsRow + row] = __float2half_rn(hv);
     }
     named_bar(1, NCT);
@@ -906,14 +1094,11 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     for (int sd = 0; sd < MAXSDN; ++sd) {
       if (sd < SDN) {
         const int s = it % NS;
-        stage_wait(s, (it / NS) & 1);
-        if (!s_abort) {
+        if (stage_wait(s, (it / NS) & 1)) {
           const uint8_t* sp = ring + (size_t)s * SBYTES;
-#pragma unroll
-          for (int j = 0; j < BPW; ++j) {
-            const int b = warp * BPW + j;
-            if (sd * SB + b < RD) block_mma<NT>(sp + b * kBlockBytes, lane, hf, yacc[sd][j]);
-          }
+          const int b = warp * BPW;   // RD and the stage's blocks are even: both or neither
+          if (sd * SB + b < RD)
+            block_pair_mma<NT>(sp + b * kBlockBytes, sp + (b + 1) * kBlockBytes, lane, hf, yacc[sd][0], yacc[sd][1]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);

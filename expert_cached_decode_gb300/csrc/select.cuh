@@ -17,12 +17,15 @@ namespace moe {
 
 // Lane chunks j = jb + lane*8 + 256*u (u < 8) of a 2048-wide block of a
 // router row (zero past d).
+// Router rows are read by every call of their layer: they are kept in L2
+// with the evict-last policy.
 __device__ __forceinline__ void router_load_block(const uint16_t* __restrict__ wrow, int jb, int d, int lane,
                                                   uint4 (&wv)[8]) {
+  const uint64_t pol = l2_evict_last_policy();
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
     const int j = jb + lane * 8 + 256 * u;
-    wv[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(wrow + j)) : make_uint4(0u, 0u, 0u, 0u);
+    wv[u] = j < d ? ld_nc_v4_hint(wrow + j, pol) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
