@@ -53,8 +53,6 @@
 // count before it streams that expert's units.  With host-issued miss copies
 // the kernel follows the routing kernel and reads its plan.  All waits are
 // bounded.
-#include <type_traits>
-
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -82,144 +80,88 @@ struct DCfg {
   static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
 
-// Selection of one call (shared memory): the per-warp candidates of the
-// first level (one token), the chosen experts of every token and the
-// distinct set U.
-struct DSel {
-  uint32_t ckey[16][kMaxTopK];        // level-1 candidates of each warp
-  int cid[16][kMaxTopK];
-  uint32_t mask[kMaxE / 32];          // chosen experts of the call
-  int word_base[kMaxE / 32];          // distinct experts below word i
-  int sel_id[kMaxDecodeT][kMaxTopK];  // per token, ascending id
-  float sel_w[kMaxDecodeT][kMaxTopK];
-  int act[kMaxPicks];                 // distinct experts U, ascending
-  int n_act;
-};
-
 // Index in U of chosen expert `id`.
-__device__ __forceinline__ int dsel_act_index(const DSel* s, int id) {
-  return s->word_base[id >> 5] + __popc(s->mask[id >> 5] & ((1u << (id & 31)) - 1u));
-}
+__device__ __forceinline__ int dsel_act_index(const SelSmem* s, int id) { return sel_act_index(s, id); }
 
-// K rounds over the (key, id) pairs held by a warp (VPL per lane; key 0 =
-// no entry; keys are order-preserving images of the logits): each round the
-// largest remaining key leaves, ties to the lower id.  Lane r receives the
-// r-th largest pair.
-template <int VPL>
-__device__ __forceinline__ void warp_rounds_topk(uint32_t (&key)[VPL], const int (&id)[VPL], int K, int lane,
-                                                 uint32_t& out_key, int& out_id) {
-  out_key = 0;
-  out_id = 0x7fffffff;
-  for (int r = 0; r < K; ++r) {
-    uint32_t bk = 0;
-    int bid = 0x7fffffff, bi = -1;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      if (key[i] != 0 && (key[i] > bk || (key[i] == bk && id[i] < bid))) {
-        bk = key[i];
-        bid = id[i];
-        bi = i;
-      }
-    }
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t win = __reduce_min_sync(0xffffffffu, bk == mx ? (uint32_t)bid : 0xffffffffu);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (i == bi && bk == mx && (uint32_t)bid == win) key[i] = 0;   // ids are distinct: one owner
-    if (lane == r) {
-      out_key = mx;
-      out_id = (int)win;
-    }
-  }
-}
-
-// lane r < K holds the r-th largest (key, id) of token t: routing weights
-// (softmax over the chosen logits, which equals the renormalised softmax
-// over all E), ids in ascending order, the call's expert mask
-__device__ __forceinline__ void dsel_finish(DSel* s, int t, int K, int lane, uint32_t key, int id) {
-  const float v = key_float(key);
-  const float top = __shfl_sync(0xffffffffu, v, 0);
-  const float ex = lane < K ? expf(v - top) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  int rank = 0;
-  for (int j = 0; j < K; ++j) rank += __shfl_sync(0xffffffffu, id, j) < id ? 1 : 0;
-  if (lane < K) {
-    s->sel_id[t][rank] = id;
-    s->sel_w[t][rank] = ex / sum;
-    atomicOr(&s->mask[id >> 5], 1u << (id & 31));
-  }
-}
-
-// Top-k of every token of the call from the logits rows [T][E] (written by
-// every CTA of this launch, read through L2), by the NTH threads of named
-// barrier 1 (CW warps).  One token: every warp finds the top-k of its share
-// of the row, then warp 0 the top-k of the CW*K candidates.  Several tokens:
-// one warp per token, K rounds over the whole row.  Then U.
+// Selection of a one-token call by all CW warps of the NTH threads of named
+// barrier 1 (the same result as select_call: the k largest logits, ties to
+// the lower id, weights renormalised, ids ascending, then U).  Keys are
+// (order-preserving value bits, ~id), all distinct.  Each warp takes the
+// maximum of its share of the row; the k-th largest of the CW warp maxima
+// is a threshold that at least k keys reach and every one of the k largest
+// reaches; the keys at or above it (a few, in general) are ranked against
+// each other.  Needs k <= CW.
 template <int NTH, int CW>
-__device__ __forceinline__ void dsel_call(const float* logits, int T, int E, int K, DSel* s) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kMaxE / 32; i += NTH) s->mask[i] = 0;
-  if (T == 1) {
-    constexpr int V1 = (kMaxE + 32 * CW - 1) / (32 * CW);
-    uint32_t key[V1];
-    int id[V1];
+__device__ __forceinline__ void select_one_token(const float* logits, int E, int K, SelSmem* s) {
+  constexpr int V = (kMaxE + 32 * CW - 1) / (32 * CW);   // keys per lane
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* wmax = &s->topk[0][0];                       // [CW] warp maxima, [CW] the threshold
+  uint64_t* cand = reinterpret_cast<uint64_t*>(&s->row[0][0]);   // up to E candidates
+  int* ncand = reinterpret_cast<int*>(&s->topk[1][0]);
+  uint64_t* top = &s->topk[2][0];                        // [K] the chosen keys, largest first
+  uint64_t key[V];
+  uint64_t m = 0;
 #pragma unroll
-    for (int i = 0; i < V1; ++i) {
-      id[i] = (warp * V1 + i) * 32 + lane;
-      key[i] = id[i] < E ? float_key(ld_cg_f32(logits + id[i])) : 0u;
-    }
-    uint32_t ck;
-    int ci;
-    warp_rounds_topk<V1>(key, id, K, lane, ck, ci);
-    if (lane < K) {
-      s->ckey[warp][lane] = ck;
-      s->cid[warp][lane] = ci;
-    }
-    named_bar(1, NTH);
-    if (warp == 0) {
-      constexpr int V2 = (CW * kMaxTopK + 31) / 32;
-      uint32_t k2[V2];
-      int i2[V2];
+  for (int i = 0; i < V; ++i) {
+    const int id = (warp * V + i) * 32 + lane;
+    key[i] = id < E ? ((uint64_t)float_key(ld_cg_f32(logits + id)) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
+    m = key[i] > m ? key[i] : m;
+  }
 #pragma unroll
-      for (int j = 0; j < V2; ++j) {
-        const int c = lane + 32 * j;
-        const bool ok = c < CW * K;
-        k2[j] = ok ? s->ckey[c / K][c % K] : 0u;
-        i2[j] = ok ? s->cid[c / K][c % K] : 0x7fffffff;
-      }
-      uint32_t fk;
-      int fi;
-      warp_rounds_topk<V2>(k2, i2, K, lane, fk, fi);
-      dsel_finish(s, 0, K, lane, fk, fi);
-    }
-  } else {
-    named_bar(1, NTH);   // the mask is clear
-    auto rows = [&](auto vr) {
-      constexpr int VR = decltype(vr)::value;
-      for (int t = warp; t < T; t += CW) {
-        uint32_t key[VR];
-        int id[VR];
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t n = shfl_u64(m, (lane + o) & 31);
+    m = n > m ? n : m;
+  }
+  if (lane == 0) wmax[warp] = m;
+  for (int i = tid; i < kMaxE / 32; i += NTH) s->mask[i] = 0;
+  if (tid == 0) *ncand = 0;
+  named_bar(1, NTH);
+  if (warp == 0) {   // the K-th largest warp maximum (warps without keys hold 0)
+    const uint64_t mine = lane < CW ? wmax[lane] : 0ull;
+    int above = 0;
 #pragma unroll
-        for (int i = 0; i < VR; ++i) {
-          id[i] = i * 32 + lane;
-          key[i] = id[i] < E ? float_key(ld_cg_f32(logits + (size_t)t * E + id[i])) : 0u;
-        }
-        uint32_t ck;
-        int ci;
-        warp_rounds_topk<VR>(key, id, K, lane, ck, ci);
-        dsel_finish(s, t, K, lane, ck, ci);
-      }
-    };
-    if (E <= 512) rows(std::integral_constant<int, 16>{});
-    else rows(std::integral_constant<int, kMaxE / 32>{});
+    for (int j = 0; j < CW; ++j) above += wmax[j] > mine ? 1 : 0;
+    const uint32_t holder = __ballot_sync(0xffffffffu, lane < CW && mine != 0 && above == K - 1);
+    // fewer than K warps hold keys (a row shorter than K warps' shares):
+    // every key is a candidate
+    const uint64_t tau = holder ? shfl_u64(mine, __ffs(holder) - 1) : 1ull;
+    if (lane == 0) wmax[CW] = tau;
   }
   named_bar(1, NTH);
-  const int n_words = (E + 31) / 32;
+  const uint64_t tau = wmax[CW];
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (key[i] >= tau && key[i] != 0) cand[atomicAdd(ncand, 1)] = key[i];
+  named_bar(1, NTH);
+  const int nc = *ncand;
+  for (int c = tid; c < nc; c += NTH) {
+    const uint64_t me = cand[c];
+    int r = 0;
+    for (int j = 0; j < nc; ++j) r += cand[j] > me ? 1 : 0;
+    if (r < K) top[r] = me;
+  }
+  named_bar(1, NTH);
   if (warp == 0) {
-    const uint32_t m = lane < n_words ? s->mask[lane] : 0u;
-    const int c = __popc(m);
+    const uint64_t kk = lane < K ? top[lane] : 0ull;
+    const float v = lane < K ? key_float((uint32_t)(kk >> 32)) : -INFINITY;
+    const int id = lane < K ? (int)~(uint32_t)kk : 0x7fffffff;
+    const float topv = __shfl_sync(0xffffffffu, v, 0);
+    const float ex = lane < K ? expf(v - topv) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    int rank = 0;
+    for (int j = 0; j < K; ++j) rank += __shfl_sync(0xffffffffu, id, j) < id ? 1 : 0;
+    if (lane < K) {
+      s->sel_id[0][rank] = id;
+      s->sel_w[0][rank] = ex / sum;
+      atomicOr(&s->mask[id >> 5], 1u << (id & 31));
+    }
+    __syncwarp();
+    // U: the chosen experts in ascending id
+    const int n_words = (E + 31) / 32;
+    const uint32_t mw = lane < n_words ? s->mask[lane] : 0u;
+    const int c = __popc(mw);
     int inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -229,7 +171,7 @@ __device__ __forceinline__ void dsel_call(const float* logits, int T, int E, int
     const int base = inc - c;
     if (lane < n_words) s->word_base[lane] = base;
     if (lane == 31) s->n_act = inc;
-    uint32_t mm = m;
+    uint32_t mm = mw;
     int pos = base;
     while (mm) {
       const int bit = __ffs(mm) - 1;
@@ -250,7 +192,7 @@ template <int NT>
 __host__ __device__ __forceinline__ size_t overlay_bytes(int d) {
   using C = DCfg<NT>;
   size_t b = (size_t)NT * 8 * x_row_elems(d) * 2;
-  const size_t sel = (sizeof(DSel) + 15) & ~size_t(15);
+  const size_t sel = (sizeof(SelSmem) + 15) & ~size_t(15);
   const size_t red = (size_t)C::CW * C::NQ * 32 * 4;
   const size_t pull = (size_t)2 * kMaxPicks * 4;
   const size_t cmb = (size_t)C::CW * 32 * 4;
@@ -574,7 +516,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   uint64_t* empty = full + NS;
   uint64_t* plan_ready = empty + NS;
   uint16_t* xraw = reinterpret_cast<uint16_t*>(ovl);   // router input rows
-  DSel* sel = reinterpret_cast<DSel*>(ovl);            // selection
+  SelSmem* sel = reinterpret_cast<SelSmem*>(ovl);      // selection
   float* red = reinterpret_cast<float*>(ovl);          // gate/up partials [CW][NQ][32]
   float* cmb = reinterpret_cast<float*>(ovl);          // combine partials [CW][32]
 
@@ -898,7 +840,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         named_bar(1, NCT);
         if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
         if (!s_cab) {
-          dsel_call<NCT, CW>(a.logits, T, E, K, sel);
+          if (T == 1 && K <= CW)
+            select_one_token<NCT, CW>(a.logits, E, K, sel);
+          else
+            select_call<NCT>(a.logits, T, E, K, sel);
           if (tid == 0) MOE_TL(g_ffn_timeline, cta, 16);
           const int n_act = sel->n_act;
           for (int i = tid; i < T * K; i += NCT) {
@@ -1002,6 +947,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
     // ================= one unit: expert ai (-1: shared), slice rb ==========
     const int ai = routed ? s_order[u / RG] : -1;
+#ifdef MOE_TIMELINE
+    const int tlu = routed ? u - s_u0 : -1;   // stamps of the first two routed units
+    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 17);
+#endif
     // the routing weight of each token for this expert (0 for a token not
     // routed to it); read in the h step, after the next barrier
     if (warp == 0 && lane < NT * 8) {
@@ -1045,7 +994,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 13);
+#ifdef MOE_TIMELINE
+    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 13);
+    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 18);
+#endif
     // partials -> shared memory, [warp][q][lane] with q = ((j*NT + nt)*2 + mt)*4 + i
 #pragma unroll
     for (int j = 0; j < BPW; ++j)
@@ -1078,7 +1030,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       hs[tok * kHsRow + row] = __float2half_rn(hv);
     }
     named_bar(1, NCT);
-    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 14);
+#ifdef MOE_TIMELINE
+    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 14);
+    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 19);
+#endif
     // B fragments of the down products (k = the slice's 32 rows of f)
     uint2 hf[NT][2];
 #pragma unroll
@@ -1105,7 +1060,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         ++it;
       }
     }
-    if (tid == 0 && routed && u == s_u0) MOE_TL(g_ffn_timeline, cta, 15);
+#ifdef MOE_TIMELINE
+    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 15);
+    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 20);
+#endif
     ++u;
   }
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 9);
