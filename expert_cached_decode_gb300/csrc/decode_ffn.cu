@@ -70,12 +70,12 @@ constexpr int kHsRow = 40;                                 // fp16 per token row
 
 template <int NT>
 struct DCfg {
-  static constexpr int CW = NT == 1 ? 16 : 8;      // consumer warps
+  static constexpr int CW = 8;                     // consumer warps
   static constexpr int SB = 2 * CW;                // blocks per ring stage: two per consumer warp
   static constexpr int BPW = 2;                    // blocks of a stage per consumer warp
   static constexpr int SBYTES = SB * kBlockBytes;  // bytes per ring stage
   static constexpr int THREADS = (CW + 2) * 32;    // + producer and control warps
-  static constexpr int NS = NT == 1 ? 10 : 10;     // ring stages (140 KB / 70 KB)
+  static constexpr int NS = NT == 1 ? 20 : 10;     // ring stages (140 KB / 70 KB)
   static constexpr int NQ = BPW * 8 * NT;          // gate/up partial floats per lane
   static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
@@ -86,49 +86,52 @@ __device__ __forceinline__ int dsel_act_index(const SelSmem* s, int id) { return
 // Selection of a one-token call by all CW warps of the NTH threads of named
 // barrier 1 (the same result as select_call: the k largest logits, ties to
 // the lower id, weights renormalised, ids ascending, then U).  Keys are
-// (order-preserving value bits, ~id), all distinct.  Each warp takes the
-// maximum of its share of the row; the k-th largest of the CW warp maxima
+// (order-preserving value bits, ~id), all distinct.  Each half-warp takes
+// the maximum of its share of the row; the k-th largest of the 2*CW maxima
 // is a threshold that at least k keys reach and every one of the k largest
 // reaches; the keys at or above it (a few, in general) are ranked against
-// each other.  Needs k <= CW.
+// each other.  Needs k <= 2*CW.
 template <int NTH, int CW>
 __device__ __forceinline__ void select_one_token(const float* logits, int E, int K, SelSmem* s) {
   constexpr int V = (kMaxE + 32 * CW - 1) / (32 * CW);   // keys per lane
+  constexpr int NG = 2 * CW;                             // groups: half-warps
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint64_t* wmax = &s->topk[0][0];                       // [CW] warp maxima, [CW] the threshold
+  uint64_t* wmax = &s->topk[0][0];                       // [NG] group maxima, [NG] the threshold
   uint64_t* cand = reinterpret_cast<uint64_t*>(&s->row[0][0]);   // up to E candidates
   int* ncand = reinterpret_cast<int*>(&s->topk[1][0]);
   uint64_t* top = &s->topk[2][0];                        // [K] the chosen keys, largest first
   uint64_t key[V];
   uint64_t m = 0;
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int id = (warp * V + i) * 32 + lane;
+  for (int i = 0; i < V; ++i) {   // ids interleaved over the warps: every warp holds keys when E >= CW
+    const int id = (i * 32 + lane) * CW + warp;
     key[i] = id < E ? ((uint64_t)float_key(ld_cg_f32(logits + id)) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
     m = key[i] > m ? key[i] : m;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t n = shfl_u64(m, (lane + o) & 31);
+  for (int o = 8; o > 0; o >>= 1) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)m, o);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(m >> 32), o);
+    const uint64_t n = ((uint64_t)hi << 32) | lo;
     m = n > m ? n : m;
   }
-  if (lane == 0) wmax[warp] = m;
+  if ((lane & 15) == 0) wmax[2 * warp + (lane >> 4)] = m;
   for (int i = tid; i < kMaxE / 32; i += NTH) s->mask[i] = 0;
   if (tid == 0) *ncand = 0;
   named_bar(1, NTH);
-  if (warp == 0) {   // the K-th largest warp maximum (warps without keys hold 0)
-    const uint64_t mine = lane < CW ? wmax[lane] : 0ull;
+  if (warp == 0) {   // the K-th largest group maximum (groups without keys hold 0)
+    const uint64_t mine = lane < NG ? wmax[lane] : 0ull;
     int above = 0;
 #pragma unroll
-    for (int j = 0; j < CW; ++j) above += wmax[j] > mine ? 1 : 0;
-    const uint32_t holder = __ballot_sync(0xffffffffu, lane < CW && mine != 0 && above == K - 1);
+    for (int j = 0; j < NG; ++j) above += wmax[j] > mine ? 1 : 0;
+    const uint32_t holder = __ballot_sync(0xffffffffu, lane < NG && mine != 0 && above == K - 1);
     // fewer than K warps hold keys (a row shorter than K warps' shares):
     // every key is a candidate
     const uint64_t tau = holder ? shfl_u64(mine, __ffs(holder) - 1) : 1ull;
-    if (lane == 0) wmax[CW] = tau;
+    if (lane == 0) wmax[NG] = tau;
   }
   named_bar(1, NTH);
-  const uint64_t tau = wmax[CW];
+  const uint64_t tau = wmax[NG];
 #pragma unroll
   for (int i = 0; i < V; ++i)
     if (key[i] >= tau && key[i] != 0) cand[atomicAdd(ncand, 1)] = key[i];
@@ -840,7 +843,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         named_bar(1, NCT);
         if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
         if (!s_cab) {
-          if (T == 1 && K <= CW)
+          if (T == 1 && K <= 2 * CW)
             select_one_token<NCT, CW>(a.logits, E, K, sel);
           else
             select_call<NCT>(a.logits, T, E, K, sel);
