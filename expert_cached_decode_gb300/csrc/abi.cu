@@ -98,7 +98,8 @@ struct moe_ctx {
   uint32_t* route_cnt = nullptr;
   Plan* plan = nullptr;
   Plan* plan_host = nullptr;  // pinned
-  float* ypart = nullptr;        // [num_sms][16][d] per-CTA partials of y
+  uint64_t* ypart = nullptr;     // [num_sms][16][d] per-CTA partials of y, (call tag, value) words
+  uint64_t* tlogits = nullptr;   // [16][E] router logits of the decode kernel, (call tag, value) words
   uint32_t* counters = nullptr;  // decode calls | 2 sets of kDecodeSetWords counters
   size_t counters_n = 0;
   int set_words = 0;
@@ -364,7 +365,11 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(dev_alloc(&c->plan, sizeof(Plan)));
   CREATE_TRY(cudaMemset(c->plan, 0, sizeof(Plan)));
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
-  CREATE_TRY(dev_alloc(&c->ypart, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(float)));
+  CREATE_TRY(dev_alloc(&c->ypart, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(uint64_t)));
+  CREATE_TRY(dev_alloc(&c->tlogits, (size_t)kMaxDecodeT * c->E * sizeof(uint64_t)));
+  // tag 0xffffffff: no call's tag, so nothing reads as written before it is
+  CREATE_TRY(cudaMemset(c->ypart, 0xff, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(uint64_t)));
+  CREATE_TRY(cudaMemset(c->tlogits, 0xff, (size_t)kMaxDecodeT * c->E * sizeof(uint64_t)));
   // router counter | partials counter | cache-mode flags: victims published,
   // misses pulled, misses placed
   c->set_words = kDecodeSetWords;
@@ -407,6 +412,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->plan);
   if (c->plan_host) cudaFreeHost(c->plan_host);
   cudaFree(c->ypart);
+  cudaFree(c->tlogits);
   cudaFree(c->counters);
   cudaFree(c->err);
   cudaFree(c->staging);
@@ -703,7 +709,7 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   // fused routing (every key resident, or misses pulled by the GPU)
   fa.wr = c->router_w + (size_t)layer * c->E * c->d;
   fa.bias = c->router_b + (size_t)layer * c->E;
-  fa.logits = c->logits;
+  fa.tlogits = c->tlogits;
   fa.E = c->E;
   fa.layer = layer;
   fa.table = c->table;
@@ -1040,6 +1046,10 @@ static moe_status check_device_error(moe_ctx* c) {
   if (e != 0) {
     CUDA_TRY(cudaMemset(c->err, 0, sizeof(uint32_t)));
     CUDA_TRY(cudaMemset(c->counters, 0, c->counters_n * sizeof(uint32_t)));
+    // the call count restarts: no word a call of the failed run wrote may
+    // carry a tag a later call uses
+    CUDA_TRY(cudaMemset(c->ypart, 0xff, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(uint64_t)));
+    CUDA_TRY(cudaMemset(c->tlogits, 0xff, (size_t)kMaxDecodeT * c->E * sizeof(uint64_t)));
     CUDA_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
     CUDA_TRY(cudaDeviceSynchronize());
     // with a cache that can miss, a call that gave up may have committed

@@ -173,6 +173,39 @@ __device__ __forceinline__ bool wait_flag_geq(const uint32_t* flag, uint32_t tar
   return true;
 }
 
+// 64-bit relaxed (gpu scope) accesses: a (tag, value) word written by one
+// CTA and polled by others; the word is read and written whole, so a reader
+// that sees the tag sees the value that came with it.
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t tag_word(uint32_t tag, float v) {
+  return ((uint64_t)tag << 32) | __float_as_uint(v);
+}
+// Value of a tagged word once it carries `tag` (polled, bounded by limit_ns
+// of %globaltimer); `first` is the word already loaded.  On a time-out
+// returns 0 and sets *failed.
+__device__ __forceinline__ float tagged_value(const uint64_t* p, uint64_t first, uint32_t tag, uint64_t limit_ns,
+                                              bool* failed) {
+  uint64_t v = first;
+  if ((uint32_t)(v >> 32) != tag) {
+    const uint64_t t0 = globaltimer();
+    do {
+      if (globaltimer() - t0 > limit_ns) {
+        *failed = true;
+        return 0.f;
+      }
+      v = ld_relaxed_u64(p);
+    } while ((uint32_t)(v >> 32) != tag);
+  }
+  return __uint_as_float((uint32_t)v);
+}
+
 // orders this thread's earlier generic-proxy shared-memory accesses (and
 // those it synchronised with) before its later async-proxy (TMA) accesses
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -71,12 +71,12 @@ constexpr int kHsRow = 40;                                 // fp16 per token row
 template <int NT>
 struct DCfg {
   static constexpr int CW = 8;                     // consumer warps
-  static constexpr int SB = 2 * CW;                // blocks per ring stage: two per consumer warp
-  static constexpr int BPW = 2;                    // blocks of a stage per consumer warp
+  static constexpr int SB = 32;                    // blocks per ring stage (14 KB bulk copies)
+  static constexpr int BPW = SB / CW;              // blocks of a stage per consumer warp (4)
   static constexpr int SBYTES = SB * kBlockBytes;  // bytes per ring stage
   static constexpr int THREADS = (CW + 2) * 32;    // + producer and control warps
-  static constexpr int NS = NT == 1 ? 20 : 10;     // ring stages (140 KB / 70 KB)
-  static constexpr int NQ = BPW * 8 * NT;          // gate/up partial floats per lane
+  static constexpr int NS = NT == 1 ? 10 : 5;      // ring stages (140 KB / 70 KB)
+  static constexpr int NQ = 2 * 8 * NT;            // gate/up partial floats per lane (g and u)
   static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
 
@@ -92,7 +92,8 @@ __device__ __forceinline__ int dsel_act_index(const SelSmem* s, int id) { return
 // reaches; the keys at or above it (a few, in general) are ranked against
 // each other.  Needs k <= 2*CW.
 template <int NTH, int CW>
-__device__ __forceinline__ void select_one_token(const float* logits, int E, int K, SelSmem* s) {
+__device__ __forceinline__ void select_one_token(const uint64_t* logits, uint32_t tag, uint64_t lim, bool* failed,
+                                                 int E, int K, SelSmem* s) {
   constexpr int V = (kMaxE + 32 * CW - 1) / (32 * CW);   // keys per lane
   constexpr int NG = 2 * CW;                             // groups: half-warps
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -102,10 +103,18 @@ __device__ __forceinline__ void select_one_token(const float* logits, int E, int
   uint64_t* top = &s->topk[2][0];                        // [K] the chosen keys, largest first
   uint64_t key[V];
   uint64_t m = 0;
+  uint64_t w[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) {   // ids interleaved over the warps: every warp holds keys when E >= CW
     const int id = (i * 32 + lane) * CW + warp;
-    key[i] = id < E ? ((uint64_t)float_key(ld_cg_f32(logits + id)) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
+    w[i] = id < E ? ld_relaxed_u64(logits + id) : 0ull;
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int id = (i * 32 + lane) * CW + warp;
+    key[i] = id < E ? ((uint64_t)float_key(tagged_value(logits + id, w[i], tag, lim, failed)) << 32) |
+                          (uint32_t)(~(uint32_t)id)
+                    : 0ull;
     m = key[i] > m ? key[i] : m;
   }
 #pragma unroll
@@ -184,6 +193,18 @@ __device__ __forceinline__ void select_one_token(const float* logits, int E, int
   }
   named_bar(1, NTH);
 }
+
+// loader of tagged logits rows for select_call: polls each word for the
+// call's tag (bounded); a time-out is recorded in *failed
+struct TaggedLogits {
+  const uint64_t* p;
+  uint32_t tag;
+  uint64_t lim;
+  bool* failed;
+  __device__ __forceinline__ float operator()(size_t i) const {
+    return tagged_value(p + i, ld_relaxed_u64(p + i), tag, lim, failed);
+  }
+};
 
 // elements per staged x row (bf16, router input): 32 bytes of padding
 __host__ __device__ __forceinline__ int x_row_elems(int d) { return d + 16; }
@@ -771,8 +792,6 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   // (the previous call's, complete by now) for the next call
   const uint32_t call_set = FUSED ? (s_calls & 1u) : ((s_calls - 1u) & 1u);
   uint32_t* const cset = a.counters + 1 + (size_t)call_set * a.set_words;
-  uint32_t* const gbar_r = cset;        // CTAs past the router rows
-  uint32_t* const gbar_p = cset + 1;    // tile CTAs whose partial of y is written
   uint32_t* const vict = cset + 2;      // cache mode: the misses' victims are published
   uint32_t* const ready = cset + 3;     // cache mode: finished fetch jobs of each miss
   if (FUSED && cta == 0) {
@@ -790,12 +809,17 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         router_load_block(wrow, 0, d, lane, wfirst);
         wbias = a.bias[e];
       }
-      router_row(wrow, wfirst, xraw, xs, wbias, T, d, E, e, lane, a.logits);
+      // each logit goes out as one (call tag, value) word: readers poll the
+      // word itself, so no counter and no fence separates router and
+      // selection.  A test hook can hold back CTA 0's logits so that every
+      // reader's bounded wait runs out.
+      uint64_t* const tl = a.tlogits;
+      const uint32_t tag = s_calls;
+      const bool hold = a.dbg_hold_router && cta == 0;
+      router_row(wrow, wfirst, xraw, xs, wbias, T, d, lane, [&](int t, float v) {
+        if (!hold) st_relaxed_u64(tl + (size_t)t * E + e, tag_word(tag, v));
+      });
     }
-    named_bar(1, NCT);
-    // covers every warp's logits (after the barrier); a test hook can hold
-    // back CTA 0's arrival so that every wait on this counter runs out
-    if (tid == 0 && !(a.dbg_hold_router && cta == 0)) red_release_add(gbar_r, 1u);
     if (tid == 0) MOE_TL(g_ffn_timeline, cta, 2);
   }
 
@@ -834,19 +858,20 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       // ================= the routing result ===============================
       if (FUSED) {
         if (tid == 0) {
-          if (!wait_flag_geq(gbar_r, (uint32_t)G, lim)) {
+          s_cab = s_abort;
+          MOE_TL(g_ffn_timeline, cta, 6);
+        }
+        named_bar(1, NCT);
+        if (!s_cab) {
+          bool failed = false;
+          if (T == 1 && K <= 2 * CW)
+            select_one_token<NCT, CW>(a.tlogits, s_calls, lim, &failed, E, K, sel);
+          else
+            select_call<NCT>(TaggedLogits{a.tlogits, s_calls, lim, &failed}, T, E, K, sel);
+          if (failed) {   // some logits never arrived
             set_error(a.err, DEV_TIMEOUT_FLAG);
             s_abort = 1;
           }
-          s_cab = s_abort;
-        }
-        named_bar(1, NCT);
-        if (tid == 0) MOE_TL(g_ffn_timeline, cta, 6);
-        if (!s_cab) {
-          if (T == 1 && K <= 2 * CW)
-            select_one_token<NCT, CW>(a.logits, E, K, sel);
-          else
-            select_call<NCT>(a.logits, T, E, K, sel);
           if (tid == 0) MOE_TL(g_ffn_timeline, cta, 16);
           const int n_act = sel->n_act;
           for (int i = tid; i < T * K; i += NCT) {
@@ -866,6 +891,11 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
           if (tid == 0) s_n_act = n_act;
         } else if (tid == 0) {
           s_n_act = 0;
+        }
+        named_bar(1, NCT);
+        if (tid == 0) {   // a selection that timed out counts as no selection
+          s_cab = s_abort;
+          if (s_cab) s_n_act = 0;
         }
         named_bar(1, NCT);
         if (MODE == kFusedResident && cta == 0) named_bar_arrive(2, NCT + 32);
@@ -969,9 +999,9 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       s_wu[lane] = wt;
     }
     // gate/up: each warp sums its blocks' input groups
-    float acc[BPW][NT][2][4];
+    float acc[2][NT][2][4];   // g and u of the slice's 32 rows
 #pragma unroll
-    for (int j = 0; j < BPW; ++j)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -981,18 +1011,23 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
 #pragma unroll 1
     for (int st = 0; st < SGU; ++st, ++it) {
       const int s = it % NS;
-      // this warp's two blocks: Wg and Wu of input group st*SB/2 + warp
-      if (stage_wait(s, (it / NS) & 1) && st * SB + warp * BPW < NGU) {
+      // this warp's blocks: Wg and Wu of input groups (st*SB + warp*BPW)/2 + p
+      if (stage_wait(s, (it / NS) & 1)) {
         const uint8_t* sp = ring + (size_t)s * SBYTES;
-        const int gi = st * (SB / 2) + warp;
-        uint2 bx[NT][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          bx[nt][0] = xfrag[((size_t)nt * nks + gi * 2 + 0) * 32 + lane];
-          bx[nt][1] = xfrag[((size_t)nt * nks + gi * 2 + 1) * 32 + lane];
+        for (int p = 0; p < BPW / 2; ++p) {
+          const int b = warp * BPW + 2 * p;   // a stage's blocks come in (Wg, Wu) pairs
+          if (st * SB + b < NGU) {
+            const int gi = (st * SB + b) / 2;
+            uint2 bx[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              bx[nt][0] = xfrag[((size_t)nt * nks + gi * 2 + 0) * 32 + lane];
+              bx[nt][1] = xfrag[((size_t)nt * nks + gi * 2 + 1) * 32 + lane];
+            }
+            block_pair_mma<NT>(sp + b * kBlockBytes, sp + (b + 1) * kBlockBytes, lane, bx, acc[0], acc[1]);
+          }
         }
-        block_pair_mma<NT>(sp + (warp * BPW) * kBlockBytes, sp + (warp * BPW + 1) * kBlockBytes, lane, bx, acc[0],
-                           acc[1]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -1003,7 +1038,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
 #endif
     // partials -> shared memory, [warp][q][lane] with q = ((j*NT + nt)*2 + mt)*4 + i
 #pragma unroll
-    for (int j = 0; j < BPW; ++j)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1054,9 +1089,13 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         const int s = it % NS;
         if (stage_wait(s, (it / NS) & 1)) {
           const uint8_t* sp = ring + (size_t)s * SBYTES;
-          const int b = warp * BPW;   // RD and the stage's blocks are even: both or neither
-          if (sd * SB + b < RD)
-            block_pair_mma<NT>(sp + b * kBlockBytes, sp + (b + 1) * kBlockBytes, lane, hf, yacc[sd][0], yacc[sd][1]);
+#pragma unroll
+          for (int p = 0; p < BPW / 2; ++p) {
+            const int b = warp * BPW + 2 * p;   // RD and the stage's blocks are even: both or neither
+            if (sd * SB + b < RD)
+              block_pair_mma<NT>(sp + b * kBlockBytes, sp + (b + 1) * kBlockBytes, lane, hf, yacc[sd][2 * p],
+                                 yacc[sd][2 * p + 1]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -1071,8 +1110,10 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   }
   if (tid == 0) MOE_TL(g_ffn_timeline, cta, 9);
 
-  // ---- this CTA's partial of y -> ypart[ct][t][row] ------------------------
-  float* const yp = a.ypart + (size_t)ct * T * d;
+  // ---- this CTA's partial of y -> ypart[ct][t][row], (call tag, value)
+  // words that the combining CTAs poll: no counter and no fence
+  uint64_t* const yp = a.ypart + (size_t)ct * T * d;
+  const uint32_t tag = s_calls;
 #pragma unroll
   for (int sd = 0; sd < MAXSDN; ++sd)
 #pragma unroll
@@ -1086,17 +1127,13 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int tok = nt * 8 + 2 * cq + (i & 1);
-              if (tok < T) yp[(size_t)tok * d + rbd * 32 + mt * 16 + gq + 8 * (i >> 1)] = yacc[sd][j][nt][mt][i];
+              if (tok < T)
+                st_relaxed_u64(yp + (size_t)tok * d + rbd * 32 + mt * 16 + gq + 8 * (i >> 1),
+                               tag_word(tag, yacc[sd][j][nt][mt][i]));
             }
       }
     }
-  named_bar(1, NCT);
   if (tid == 0) {
-    red_release_add(gbar_p, 1u);   // covers every warp's partial (after the barrier)
-    if (!wait_flag_geq(gbar_p, (uint32_t)GT, lim)) {
-      set_error(a.err, DEV_TIMEOUT_FLAG);
-      s_abort = 1;
-    }
     s_cab = s_abort;
     MOE_TL(g_ffn_timeline, cta, 10);
   }
@@ -1109,17 +1146,24 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   const int c0 = warp * GT / CW, c1 = (warp + 1) * GT / CW;
   for (int item = ct; item < T * RD; item += GT) {
     const int t = item / RD, rbd = item - t * RD;
-    const float* src = a.ypart + (size_t)t * d + rbd * 32 + lane;
+    const uint64_t* src = a.ypart + (size_t)t * d + rbd * 32 + lane;
     float v = 0.f;
+    bool failed = false;
     // every load of a batch in flight before the sum (one batch covers a
-    // warp's share on grids of up to 160 CTAs)
+    // warp's share on grids of up to 160 CTAs); a partial not yet written is
+    // polled until it carries this call's tag
     constexpr int kBatch = (160 + CW - 1) / CW;
     for (int cb = c0; cb < c1; cb += kBatch) {
-      float pv[kBatch];
+      uint64_t pw[kBatch];
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) pv[q] = cb + q < c1 ? __ldcg(src + (size_t)(cb + q) * cstride) : 0.f;
+      for (int q = 0; q < kBatch; ++q) pw[q] = cb + q < c1 ? ld_relaxed_u64(src + (size_t)(cb + q) * cstride) : 0ull;
 #pragma unroll
-      for (int q = 0; q < kBatch; ++q) v += pv[q];
+      for (int q = 0; q < kBatch; ++q)
+        if (cb + q < c1) v += tagged_value(src + (size_t)(cb + q) * cstride, pw[q], tag, lim, &failed);
+    }
+    if (failed) {
+      set_error(a.err, DEV_TIMEOUT_FLAG);
+      s_abort = 1;
     }
     cmb[warp * 32 + lane] = v;
     named_bar(1, NCT);

@@ -110,7 +110,7 @@ struct FfnArgs {
   int T, d, f, k;
   float shared_weight;
   Plan* plan;                   // read (after the routing kernel) or written (fused routing)
-  float* ypart;                 // [grid][T][d] per-CTA partials of y
+  uint64_t* ypart;              // [grid][T][d] per-CTA partials of y, (call tag, value) words
   // per-call counters: word 0 counts decode calls; then two sets of
   // set_words words (router counter | partials counter | cache mode: victims
   // published | finished fetch jobs of each miss), used by alternate calls.  A call uses set (calls before it) & 1, and the set of the call
@@ -126,7 +126,7 @@ struct FfnArgs {
   int fused;
   const uint16_t* wr;           // [E][d] bf16 (this layer)
   const float* bias;            // [E] (this layer)
-  float* logits;                // [T][E] scratch
+  uint64_t* tlogits;            // [T][E] router logits, (call tag, value) words
   int E, layer;
   const int32_t* table;         // [L*E]
   int64_t* stamp;               // [C]
@@ -144,8 +144,8 @@ struct FfnArgs {
   int staging_n;
 };
 
-// words of one per-call counter set of the decode kernel: router counter,
-// partials counter, victims published, finished fetch jobs of each miss
+// words of one per-call counter set of the decode kernel: two unused words,
+// victims published, finished fetch jobs of each miss
 constexpr int kDecodeSetWords = 3 + kMaxPicks;
 
 // decode kernel modes

@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     const uint16_t* wrow = a.wr + (size_t)e * a.d;
     uint4 first[8];
     router_load_block(wrow, 0, a.d, lane, first);
-    router_row(wrow, first, a.x, a.d, a.bias[e], T, a.d, E, e, lane, a.logits);
+    float* const lg = a.logits;
+    router_row(wrow, first, a.x, a.d, a.bias[e], T, a.d, lane, [&](int t, float v) { lg[(size_t)t * E + e] = v; });
   }
 
   // ---- last CTA to arrive does the selection -----------------------------
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     MOE_TL(g_route_timeline, 200, 0);
     *a.cnt = 0;   // ready for the next launch (stream-ordered)
   }
-  select_call(a.logits, T, E, K, &sel);
+  select_call(PlainLogits{a.logits}, T, E, K, &sel);
   if (threadIdx.x == 0) MOE_TL(g_route_timeline, 200, 1);
   const int n_act = sel.n_act;
   Plan* P = a.plan;

@@ -46,12 +46,13 @@ __device__ __forceinline__ float dot8_bf16(uint4 w4, uint4 x4, float s) {
 // xstride elements apart, 16-byte aligned, global or shared memory), given
 // the row's first 2048-wide block in `first` (router_load_block at jb = 0).
 // Per token, lane chunks accumulate in u order within each 2048-wide block,
-// blocks in order, then a butterfly sum; lane 0 stores l[t, e] = dot + bias
-// at logits[t*E + e].  Tokens run in a loop (this code runs once per call,
+// blocks in order, then a butterfly sum; lane 0 hands l[t, e] = dot + bias
+// to store(t, value).  Tokens run in a loop (this code runs once per call,
 // so it is kept short).
+template <class Store>
 __device__ __forceinline__ void router_row(const uint16_t* __restrict__ wrow, const uint4 (&first)[8],
                                            const uint16_t* __restrict__ x, int xstride, float bias, int T, int d,
-                                           int E, int e, int lane, float* logits) {
+                                           int lane, Store store) {
 #pragma unroll 1
   for (int t = 0; t < T; ++t) {
     const uint16_t* xr = x + (size_t)t * xstride;
@@ -73,7 +74,7 @@ __device__ __forceinline__ void router_row(const uint16_t* __restrict__ wrow, co
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) logits[(size_t)t * E + e] = s + bias;
+    if (lane == 0) store(t, s + bias);
   }
 }
 
@@ -106,8 +107,14 @@ __device__ __forceinline__ int sel_act_index(const SelSmem* s, int id) {
 // tokens in turn: top-k (ties to the lower id), weights, ids ascending; then
 // warp 0 forms U.
 // `tl` (timeline builds only) receives %globaltimer stamps of the steps.
-template <int NTH = 0>
-__device__ __forceinline__ void select_call(const float* logits, int T, int E, int K, SelSmem* s,
+// default loader of the logits rows: plain floats through L2
+struct PlainLogits {
+  const float* p;
+  __device__ __forceinline__ float operator()(size_t i) const { return ld_cg_f32(p + i); }
+};
+
+template <int NTH = 0, class Load = PlainLogits>
+__device__ __forceinline__ void select_call(Load logits, int T, int E, int K, SelSmem* s,
                                             unsigned long long* tl = nullptr) {
   const int nthreads = NTH == 0 ? (int)blockDim.x : NTH;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,7 +129,7 @@ __device__ __forceinline__ void select_call(const float* logits, int T, int E, i
   for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
     float* row = s->row[warp];
 #pragma unroll 16
-    for (int id = lane; id < E; id += 32) row[id] = ld_cg_f32(logits + (size_t)t * E + id);
+    for (int id = lane; id < E; id += 32) row[id] = logits((size_t)t * E + id);
     __syncwarp();
     if (t == 0) SEL_TL(0);
     float my_v;

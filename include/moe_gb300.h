@@ -182,8 +182,8 @@ moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
  *     fails, so moe_forward returns MOE_ERR_CUDA before any cache state
  *     changes;
  *   MOE_INJECT_HOLD_ROUTER: in a decode layer-call with routing inside the
- *     kernel, CTA 0 never arrives on the grid-wide counter of the router
- *     logits, so every CTA's bounded wait on it runs out (after the limit of
+ *     kernel, CTA 0 never publishes its rows of the router logits, so every
+ *     CTA's bounded wait for them runs out (after the limit of
  *     moe_debug_set_wait_limit); the call returns MOE_OK (it is asynchronous)
  *     and the next moe_sync reports MOE_ERR_TIMEOUT;
  *   MOE_INJECT_HOST_REGISTER: moe_layer_create's registration of a pageable

@@ -7,8 +7,8 @@
   left registered); a device allocation fails at create (MOE_ERR_OOM, no
   memory left allocated) or at configure (MOE_ERR_OOM, the previous cache
   unchanged and usable).
-* Bounded device waits: one CTA holds back its arrival on the router's grid
-  counter (a flag nothing else sets), every CTA's wait runs out after a short
+* Bounded device waits: one CTA holds back its router logits (words that
+  nothing else writes), every CTA's wait for them runs out after a short
   limit, the kernel returns, moe_sync reports MOE_ERR_TIMEOUT and the context
   works again (after reconfiguring, for a cache that can miss).
 """
@@ -96,9 +96,9 @@ def _oracle_check(s, layer, xb):
 
 
 def test_router_wait_runs_out_and_the_context_recovers():
-    # CTA 0 holds back its arrival on the router counter: every CTA's wait
-    # on it runs out after 20 ms, the kernel returns, moe_sync reports
-    # MOE_ERR_TIMEOUT, and the next call is correct again
+    # CTA 0 holds back its router logits: every CTA's wait for them runs out
+    # after 20 ms, the kernel returns, moe_sync reports MOE_ERR_TIMEOUT, and
+    # the next call is correct again
     lib = _abi.load()
     s, layer = _resident_tiny()
     try:
