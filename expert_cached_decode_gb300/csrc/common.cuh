@@ -187,23 +187,44 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 __device__ __forceinline__ uint64_t tag_word(uint32_t tag, float v) {
   return ((uint64_t)tag << 32) | __float_as_uint(v);
 }
-// Value of a tagged word once it carries `tag` (polled, bounded by limit_ns
-// of %globaltimer); `first` is the word already loaded.  On a time-out
-// returns 0 and sets *failed.
-__device__ __forceinline__ float tagged_value(const uint64_t* p, uint64_t first, uint32_t tag, uint64_t limit_ns,
-                                              bool* failed) {
-  uint64_t v = first;
-  if ((uint32_t)(v >> 32) != tag) {
+// Values of the tagged words base[j * stride], j < n (n <= N), once each
+// carries `tag`.  All n are loaded together; while some still carry an older
+// tag, those are reloaded together (one round per L2 round trip), bounded by
+// limit_ns of %globaltimer.  Words j >= n read as 0.  On a time-out *failed
+// is set and the values are meaningless.  (Polling one word at a time costs
+// a round trip per word: with 10-20 words per lane that is several times
+// slower than these rounds.)
+template <int N>
+__device__ __forceinline__ void tagged_values(const uint64_t* base, size_t stride, int n, uint32_t tag,
+                                              uint64_t limit_ns, bool* failed, float (&v)[N]) {
+  static_assert(N <= 32, "one bit per word");
+  uint64_t w[N];
+  uint32_t miss = 0;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    if (j < n) w[j] = ld_relaxed_u64(base + (size_t)j * stride);
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    if (j < n && (uint32_t)(w[j] >> 32) != tag) miss |= 1u << j;
+  if (miss) {
     const uint64_t t0 = globaltimer();
     do {
       if (globaltimer() - t0 > limit_ns) {
         *failed = true;
-        return 0.f;
+        break;
       }
-      v = ld_relaxed_u64(p);
-    } while ((uint32_t)(v >> 32) != tag);
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if (miss >> j & 1u) w[j] = ld_relaxed_u64(base + (size_t)j * stride);
+      uint32_t still = 0;
+#pragma unroll
+      for (int j = 0; j < N; ++j)
+        if ((miss >> j & 1u) && (uint32_t)(w[j] >> 32) != tag) still |= 1u << j;
+      miss = still;
+    } while (miss);
   }
-  return __uint_as_float((uint32_t)v);
+#pragma unroll
+  for (int j = 0; j < N; ++j) v[j] = j < n ? __uint_as_float((uint32_t)w[j]) : 0.f;
 }
 
 // orders this thread's earlier generic-proxy shared-memory accesses (and

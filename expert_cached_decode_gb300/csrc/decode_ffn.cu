@@ -62,7 +62,40 @@
 namespace moe {
 
 #ifdef MOE_TIMELINE
+// Timeline builds: each CTA stamps %clock64 into shared memory (a stamp
+// that stores to global memory itself slows the warp's next collectives by
+// thousands of cycles, which distorts what it measures); the consumers'
+// last thread converts the stamps to %globaltimer ns at exit.
 __device__ unsigned long long g_ffn_timeline[512][32];
+__shared__ long long s_tl[32];
+__shared__ unsigned long long s_tl_gt0;
+#define MOE_TLS(slot) (s_tl[(slot)] = clock64())
+// a stamp by thread 0 in code the whole warp runs: the warp reconverges
+// after it (a lane-divergent branch left open makes every later warp
+// collective pay a rendezvous)
+#define MOE_TL0(slot)                     \
+  do {                                    \
+    if (threadIdx.x == 0) MOE_TLS(slot);  \
+    __syncwarp();                         \
+  } while (0)
+__device__ __forceinline__ void dtl_begin() {
+  for (int i = 0; i < 32; ++i) s_tl[i] = 0;
+  s_tl_gt0 = globaltimer();
+  s_tl[0] = clock64();
+}
+__device__ __forceinline__ void dtl_flush(int cta) {
+  if (threadIdx.x != 0) return;
+  const unsigned long long gt1 = globaltimer();
+  const long long c1 = clock64(), c0 = s_tl[0];
+  const double ns_per_cycle = c1 > c0 ? (double)(gt1 - s_tl_gt0) / (double)(c1 - c0) : 0.0;
+  for (int i = 0; i < 32; ++i)
+    g_ffn_timeline[cta][i] = s_tl[i] ? s_tl_gt0 + (unsigned long long)((double)(s_tl[i] - c0) * ns_per_cycle) : 0ull;
+}
+#define MOE_TL_FLUSH(cta) dtl_flush(cta)
+#else
+#define MOE_TLS(slot) ((void)0)
+#define MOE_TL0(slot) ((void)0)
+#define MOE_TL_FLUSH(cta) ((void)0)
 #endif
 
 constexpr int kMaxRD = 64;                                 // row blocks of d (d <= 2048)
@@ -101,20 +134,22 @@ __device__ __forceinline__ void select_one_token(const uint64_t* logits, uint32_
   uint64_t* cand = reinterpret_cast<uint64_t*>(&s->row[0][0]);   // up to E candidates
   int* ncand = reinterpret_cast<int*>(&s->topk[1][0]);
   uint64_t* top = &s->topk[2][0];                        // [K] the chosen keys, largest first
+  // contiguous ids: lane l of warp w holds ids i*32*CW + w*32 + l (i < V), so
+  // a warp's loads cover whole lines; a row shorter than CW*32 leaves later
+  // half-warps without keys (their maximum is 0)
+  const int nv = E > warp * 32 + lane ? (E - warp * 32 - lane + 32 * CW - 1) / (32 * CW) : 0;
+  float lv[V];
+  tagged_values<V>(logits + warp * 32 + lane, 32 * CW, nv, tag, lim, failed, lv);
+#ifdef MOE_TIMELINE
+  MOE_TL0(21);
+#endif
+  __syncwarp();   // lanes left the polling rounds at different times
   uint64_t key[V];
   uint64_t m = 0;
-  uint64_t w[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) {   // ids interleaved over the warps: every warp holds keys when E >= CW
-    const int id = (i * 32 + lane) * CW + warp;
-    w[i] = id < E ? ld_relaxed_u64(logits + id) : 0ull;
-  }
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int id = (i * 32 + lane) * CW + warp;
-    key[i] = id < E ? ((uint64_t)float_key(tagged_value(logits + id, w[i], tag, lim, failed)) << 32) |
-                          (uint32_t)(~(uint32_t)id)
-                    : 0ull;
+    const int id = i * 32 * CW + warp * 32 + lane;
+    key[i] = i < nv ? ((uint64_t)float_key(lv[i]) << 32) | (uint32_t)(~(uint32_t)id) : 0ull;
     m = key[i] > m ? key[i] : m;
   }
 #pragma unroll
@@ -140,6 +175,9 @@ __device__ __forceinline__ void select_one_token(const uint64_t* logits, uint32_
     if (lane == 0) wmax[NG] = tau;
   }
   named_bar(1, NTH);
+#ifdef MOE_TIMELINE
+  MOE_TL0(22);
+#endif
   const uint64_t tau = wmax[NG];
 #pragma unroll
   for (int i = 0; i < V; ++i)
@@ -153,7 +191,11 @@ __device__ __forceinline__ void select_one_token(const uint64_t* logits, uint32_
     if (r < K) top[r] = me;
   }
   named_bar(1, NTH);
+#ifdef MOE_TIMELINE
+  MOE_TL0(23);
+#endif
   if (warp == 0) {
+    __syncwarp();
     const uint64_t kk = lane < K ? top[lane] : 0ull;
     const float v = lane < K ? key_float((uint32_t)(kk >> 32)) : -INFINITY;
     const int id = lane < K ? (int)~(uint32_t)kk : 0x7fffffff;
@@ -194,15 +236,24 @@ __device__ __forceinline__ void select_one_token(const uint64_t* logits, uint32_
   named_bar(1, NTH);
 }
 
-// loader of tagged logits rows for select_call: polls each word for the
-// call's tag (bounded); a time-out is recorded in *failed
+// loader of tagged logits rows for select_call: a lane's words of row t are
+// read in batches of 8 (tagged_values, bounded); a time-out is recorded in
+// *failed
 struct TaggedLogits {
   const uint64_t* p;
   uint32_t tag;
   uint64_t lim;
   bool* failed;
-  __device__ __forceinline__ float operator()(size_t i) const {
-    return tagged_value(p + i, ld_relaxed_u64(p + i), tag, lim, failed);
+  __device__ __forceinline__ void row(float* r, int t, int E, int lane) const {
+    const int nper = (E - lane + 31) / 32;   // ids lane + 32 j, j < nper
+#pragma unroll 1
+    for (int j0 = 0; j0 < nper; j0 += 8) {
+      float v[8];
+      tagged_values<8>(p + (size_t)t * E + lane + 32 * j0, 32, nper - j0 < 8 ? nper - j0 : 8, tag, lim, failed, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j0 + j < nper) r[lane + 32 * (j0 + j)] = v[j];
+    }
   }
 };
 
@@ -400,6 +451,7 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
       const uint32_t bal = __ballot_sync(0xffffffffu, miss);
       if (miss) s_miss_ai[base + __popc(bal & ((1u << lane) - 1u))] = i;
       base += __popc(bal);
+      __syncwarp();
     }
   }
   if (tid == 0) s_evict = 0;
@@ -449,7 +501,7 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
   }
   named_bar(1, NTH);
   if (m > 0 && tid == 0) {
-    MOE_TL(g_ffn_timeline, 0, 28);
+    MOE_TLS(28);
     red_release_add(&vict[0], 1u);   // covers the plan's victim entries (after the barrier)
   }
   // commit: evicted keys leave the table before the misses enter it
@@ -568,7 +620,9 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   const int ct = CACHED ? cta - 1 : cta;       // tile index (-1: the cache manager)
   const int sh0 = ct >= 0 ? shared_first(ct, RG, GT) : 0;
   const int sh1 = ct >= 0 ? shared_first(ct + 1, RG, GT) : 0;
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 0);
+#ifdef MOE_TIMELINE
+  if (tid == 0) dtl_begin();
+#endif
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
@@ -625,7 +679,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     if (CACHED) asm volatile("fence.proxy.async.global;" ::: "memory");
     if (ok && !mbar_wait(plan_ready, 0, lim)) ok = false;
     if (ok) {
-      MOE_TL(g_ffn_timeline, cta, 4);
+      MOE_TLS(4);
       const int u0 = s_u0, u1 = s_u1;
       const uint32_t jpm = (uint32_t)(2 * RG + RD);   // fetch jobs per missing expert
       const uint32_t* ready = a.counters + 1 + (size_t)(s_calls & 1u) * a.set_words + 3;
@@ -656,7 +710,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     // the last ones
     for (uint32_t k = it > (uint32_t)NS ? it - NS : 0; k < it; ++k)
       if (!mbar_wait(&full[k % NS], (k / NS) & 1, lim)) set_error(a.err, DEV_TIMEOUT_BARRIER);
-    MOE_TL(g_ffn_timeline, cta, 5);
+    MOE_TLS(5);
     return;
   }
   if (warp == CW + 1) {
@@ -787,7 +841,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
   }
   named_bar(1, NCT);
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 1);
+  MOE_TL0(1);
   // this call's counter set; the fused kernel's CTA 0 zeroes the other one
   // (the previous call's, complete by now) for the next call
   const uint32_t call_set = FUSED ? (s_calls & 1u) : ((s_calls - 1u) & 1u);
@@ -820,7 +874,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         if (!hold) st_relaxed_u64(tl + (size_t)t * E + e, tag_word(tag, v));
       });
     }
-    if (tid == 0) MOE_TL(g_ffn_timeline, cta, 2);
+    MOE_TL0(2);
   }
 
   // ---- units: the CTA's shared-expert units, then (after the routing
@@ -841,15 +895,19 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   uint32_t it = 0;   // ring stage counter (the producer's order)
   bool routed = false;
   int u = sh0, u_end = sh1;
-  // waits for stage s (bounded); false once any warp of the CTA gave up
+  // waits for stage s (bounded); false once any warp of the CTA gave up.
+  // The answer is the same for all lanes of the warp (the MMAs that follow
+  // need the whole warp).
   auto stage_wait = [&](int s, uint32_t par) -> bool {
-    if (s_abort) return false;
-    if (!mbar_wait(&full[s], par, lim)) {
-      set_error(a.err, DEV_TIMEOUT_BARRIER);
-      s_abort = 1;
-      return false;
+    bool got = false;
+    if (!s_abort) {
+      got = mbar_wait(&full[s], par, lim);
+      if (!got) {
+        set_error(a.err, DEV_TIMEOUT_BARRIER);
+        s_abort = 1;
+      }
     }
-    return true;
+    return __all_sync(0xffffffffu, got);
   };
   for (;;) {
     if (u >= u_end) {
@@ -859,7 +917,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       if (FUSED) {
         if (tid == 0) {
           s_cab = s_abort;
-          MOE_TL(g_ffn_timeline, cta, 6);
+          MOE_TLS(6);
         }
         named_bar(1, NCT);
         if (!s_cab) {
@@ -872,7 +930,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
             set_error(a.err, DEV_TIMEOUT_FLAG);
             s_abort = 1;
           }
-          if (tid == 0) MOE_TL(g_ffn_timeline, cta, 16);
+          MOE_TL0(16);
           const int n_act = sel->n_act;
           for (int i = tid; i < T * K; i += NCT) {
             const int id = sel->sel_id[i / K][i % K];
@@ -912,7 +970,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         }
         named_bar(1, NCT);
       }
-      if (tid == 0) MOE_TL(g_ffn_timeline, cta, 7);
+      MOE_TL0(7);
       const int n_act = s_n_act;
       // unit order: resident experts first, then the misses (ascending id
       // within each), and each miss's position in the miss list
@@ -928,6 +986,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
           if (i < n_act && !miss) s_order[nh + __popc(bh & below)] = i;
           nh += __popc(bh);
           nm += __popc(bm);
+          __syncwarp();
         }
         for (int i0 = 0; i0 < n_act; i0 += 32) {
           const int i = i0 + lane;
@@ -935,6 +994,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
           const uint32_t bm = __ballot_sync(0xffffffffu, miss);
           if (miss) s_order[nh + __popc(bm & ((1u << lane) - 1u))] = i;
           nh += __popc(bm);
+          __syncwarp();
         }
       }
       const int n_miss = named_bar_count(1, NCT, CACHED && tid < n_act && s_act_slot[tid] < 0);
@@ -942,6 +1002,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         if (!s_cab)
           cache_manager<NCT>(a, n_act, n_miss, s_act_expert, s_act_slot, s_pick_act, s_w, s_clock, s_calls, ring,
                              (size_t)NS * SBYTES, vict);
+        MOE_TL_FLUSH(cta);
         return;   // CTA 0 takes no units
       }
       // this CTA's routed units, handed to the producer (it streams the
@@ -951,7 +1012,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         s_u0 = routed_first(ct, NU, RG, GT);
         s_u1 = routed_first(ct + 1, NU, RG, GT);
         mbar_arrive(plan_ready);
-        MOE_TL(g_ffn_timeline, cta, 8);
+        MOE_TLS(8);
       }
       if (CACHED && n_miss > 0) {
         // fetch jobs of the misses, spread over the tile CTAs, once CTA 0 has
@@ -971,7 +1032,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
                              const_cast<uint8_t*>(a.slots), a.expert_bytes, a.layer, a.E, d, f};
           pull_jobs<NCT, KPC>(mf, (int)((int64_t)ct * J / GT), (int)((int64_t)(ct + 1) * J / GT), ovl, ready);
         }
-        if (tid == 0) MOE_TL(g_ffn_timeline, cta, 12);
+        MOE_TL0(12);
       }
       named_bar(1, NCT);
       u = s_u0;
@@ -982,7 +1043,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     const int ai = routed ? s_order[u / RG] : -1;
 #ifdef MOE_TIMELINE
     const int tlu = routed ? u - s_u0 : -1;   // stamps of the first two routed units
-    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 17);
+    if (tlu == 1) MOE_TL0(17);
 #endif
     // the routing weight of each token for this expert (0 for a token not
     // routed to it); read in the h step, after the next barrier
@@ -998,6 +1059,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       }
       s_wu[lane] = wt;
     }
+    __syncwarp();   // warp 0's MMAs below run on the whole warp again
     // gate/up: each warp sums its blocks' input groups
     float acc[2][NT][2][4];   // g and u of the slice's 32 rows
 #pragma unroll
@@ -1031,12 +1093,16 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      __syncwarp();   // the next stage's MMAs run on the whole warp
     }
 #ifdef MOE_TIMELINE
-    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 13);
-    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 18);
+    if (tlu == 0) MOE_TL0(13);
+    if (tlu == 1) MOE_TL0(18);
 #endif
-    // partials -> shared memory, [warp][q][lane] with q = ((j*NT + nt)*2 + mt)*4 + i
+    // partials -> shared memory, [warp][q][lane] with q = ((j*NT + nt)*2 + mt)*4 + i.
+    // They overlay the staged router input: in the CTA's first shared unit
+    // the warps first wait until every warp is done with its router rows.
+    if (FUSED && !routed && u == sh0) named_bar(1, NCT);
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -1069,8 +1135,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
     named_bar(1, NCT);
 #ifdef MOE_TIMELINE
-    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 14);
-    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 19);
+    if (tlu == 0) MOE_TL0(14);
+    if (tlu == 1) MOE_TL0(19);
 #endif
     // B fragments of the down products (k = the slice's 32 rows of f)
     uint2 hf[NT][2];
@@ -1099,16 +1165,17 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        __syncwarp();   // the next stage's MMAs run on the whole warp
         ++it;
       }
     }
 #ifdef MOE_TIMELINE
-    if (tid == 0 && tlu == 0) MOE_TL(g_ffn_timeline, cta, 15);
-    if (tid == 0 && tlu == 1) MOE_TL(g_ffn_timeline, cta, 20);
+    if (tlu == 0) MOE_TL0(15);
+    if (tlu == 1) MOE_TL0(20);
 #endif
     ++u;
   }
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 9);
+  MOE_TL0(9);
 
   // ---- this CTA's partial of y -> ypart[ct][t][row], (call tag, value)
   // words that the combining CTAs poll: no counter and no fence
@@ -1135,10 +1202,13 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
   if (tid == 0) {
     s_cab = s_abort;
-    MOE_TL(g_ffn_timeline, cta, 10);
+    MOE_TLS(10);
   }
   named_bar(1, NCT);
-  if (s_cab) return;
+  if (s_cab) {
+    MOE_TL_FLUSH(cta);
+    return;
+  }
   // ---- combine: item (t, rb) = t * RD + rb for items ct, ct + GT, ...; warp
   // w adds the partials of CTAs [w*GT/CW, (w+1)*GT/CW) in order, then warp 0
   // adds the warps' sums in order
@@ -1149,17 +1219,17 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     const uint64_t* src = a.ypart + (size_t)t * d + rbd * 32 + lane;
     float v = 0.f;
     bool failed = false;
-    // every load of a batch in flight before the sum (one batch covers a
-    // warp's share on grids of up to 160 CTAs); a partial not yet written is
-    // polled until it carries this call's tag
+    // the partials of a batch are read together, in rounds until each
+    // carries this call's tag (one batch covers a warp's share on grids of
+    // up to 160 CTAs), then added in CTA order
     constexpr int kBatch = (160 + CW - 1) / CW;
     for (int cb = c0; cb < c1; cb += kBatch) {
-      uint64_t pw[kBatch];
-#pragma unroll
-      for (int q = 0; q < kBatch; ++q) pw[q] = cb + q < c1 ? ld_relaxed_u64(src + (size_t)(cb + q) * cstride) : 0ull;
+      float pv[kBatch];
+      tagged_values<kBatch>(src + (size_t)cb * cstride, cstride, c1 - cb < kBatch ? c1 - cb : kBatch, tag, lim,
+                            &failed, pv);
 #pragma unroll
       for (int q = 0; q < kBatch; ++q)
-        if (cb + q < c1) v += tagged_value(src + (size_t)(cb + q) * cstride, pw[q], tag, lim, &failed);
+        if (cb + q < c1) v += pv[q];
     }
     if (failed) {
       set_error(a.err, DEV_TIMEOUT_FLAG);
@@ -1175,7 +1245,8 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
     }
     named_bar(1, NCT);
   }
-  if (tid == 0) MOE_TL(g_ffn_timeline, cta, 11);
+  MOE_TL0(11);
+  MOE_TL_FLUSH(cta);
 }
 
 #ifdef MOE_TIMELINE

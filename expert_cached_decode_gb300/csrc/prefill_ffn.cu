@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         const int ps = j % PSTAGES;
         {
           PF_T0();
-          if (!mbar_wait(&my_bar[ps], (j / PSTAGES) & 1)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&my_bar[ps], (j / PSTAGES) & 1))) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             goto done;
           }
@@ -517,13 +517,14 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         const uint32_t use = it / STAGES;
         {
           PF_T0();
-          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1)) {
+          if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(&empty[s], (use - 1) & 1))) {
             set_error(a.err, DEV_TIMEOUT_BARRIER);
             goto done;
           }
           PF_ACC(pf_p7);
         }
         PF_T0();
+        __syncwarp();   // after lane 0's issue and the waits: stmatrix runs on the whole warp
         const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
         const uint8_t* src = my_stage + ps * PCHUNK;
         if (DOWN) {
@@ -582,12 +583,13 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       }
       {
         PF_T0();
-        if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[ab], (lt >> 1) & 1))) {
           set_error(a.err, DEV_TIMEOUT_BARRIER);
           goto done;
         }
         if (ew == 0 && lane == 0) PF_ADD(DOWN, 5);
       }
+      __syncwarp();   // tcgen05.ld below runs on the whole warp
       PF_T0();
       tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + ab * BN + hf * 16;
@@ -672,6 +674,7 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tempty[ab]);
+      __syncwarp();
       if (ew == 0 && lane == 0) {
         PF_ADD(DOWN, 4);
 #ifdef MOE_TIMELINE

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(rg::THREADS, 1)
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
       const int mt = tile % n_mt, nt = tile / n_mt;
       const int ab = lt & 1;
-      if (!mbar_wait(&tfull[ab], (lt >> 1) & 1)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[ab], (lt >> 1) & 1))) {
         ok = false;
         set_error(a.err, DEV_TIMEOUT_BARRIER);
         break;
@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(rg::THREADS, 1)
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tempty[ab]);
+      __syncwarp();   // the next tile's tcgen05.ld runs on the whole warp
     }
   }
   tc_fence_before();

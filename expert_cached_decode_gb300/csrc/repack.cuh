@@ -64,6 +64,7 @@ __device__ __forceinline__ void pack_block(uint32_t r0, uint32_t r1, uint32_t r2
     o.y = s_c | (s_d << 16);
     *reinterpret_cast<uint2*>(out + kBlockCodeBytes + 8 * lane) = o;
   }
+  __syncwarp();   // a following block's shuffles run on the whole warp again
 }
 
 // Block bi of the expert at `src` (canonical) into the expert at `dst`

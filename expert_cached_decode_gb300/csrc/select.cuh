@@ -75,6 +75,7 @@ __device__ __forceinline__ void router_row(const uint16_t* __restrict__ wrow, co
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) store(t, s + bias);
+    __syncwarp();   // the next token's shuffles run on the whole warp again
   }
 }
 
@@ -102,15 +103,20 @@ __device__ __forceinline__ int sel_act_index(const SelSmem* s, int id) {
 // Every participating thread calls this: the whole block when NTH is 0,
 // else the first NTH threads (warps 0 .. NTH/32-1, synchronised by named
 // barrier 1); warps below kSelWarps select.
-// Reads the logits rows [T][E] from global memory through L2 (they were
-// written by other CTAs of this kernel or of the same launch); warps take
+// Reads the logits rows [T][E] through the loader (`logits.row`: plain loads
+// through L2 after the writers were waited for, or tagged words polled until
+// they carry the call's tag); warps take
 // tokens in turn: top-k (ties to the lower id), weights, ids ascending; then
 // warp 0 forms U.
 // `tl` (timeline builds only) receives %globaltimer stamps of the steps.
-// default loader of the logits rows: plain floats through L2
+// default loader of the logits rows: plain floats through L2; row(r, t, E,
+// lane) fills r[id] = l[t, id] for the lane's ids lane, lane + 32, ...
 struct PlainLogits {
   const float* p;
-  __device__ __forceinline__ float operator()(size_t i) const { return ld_cg_f32(p + i); }
+  __device__ __forceinline__ void row(float* r, int t, int E, int lane) const {
+#pragma unroll 16
+    for (int id = lane; id < E; id += 32) r[id] = ld_cg_f32(p + (size_t)t * E + id);
+  }
 };
 
 template <int NTH = 0, class Load = PlainLogits>
@@ -128,8 +134,7 @@ __device__ __forceinline__ void select_call(Load logits, int T, int E, int K, Se
   step_bar<NTH>();
   for (int t = warp; warp < kSelWarps && t < T; t += kSelWarps) {
     float* row = s->row[warp];
-#pragma unroll 16
-    for (int id = lane; id < E; id += 32) row[id] = logits((size_t)t * E + id);
+    logits.row(row, t, E, lane);
     __syncwarp();
     if (t == 0) SEL_TL(0);
     float my_v;
