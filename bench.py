@@ -74,7 +74,7 @@ def peaks():
 
 
 # the sources the decode kernel is compiled from
-DECODE_SOURCES = ("decode_ffn.cu", "select.cuh", "common.cuh", "internal.h", "repack.cuh")
+DECODE_SOURCES = ("decode_ffn.cu", "select.cuh", "common.cuh", "internal.h", "repack.cuh", "fetch.cuh")
 
 
 def source_hash():
