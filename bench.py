@@ -290,6 +290,22 @@ def make_host_pool(cfg_id, entries, workers=16):
     return shm, np.ndarray((entries, B), dtype=np.uint8, buffer=shm.buf)
 
 
+def pack_pool_in_place(pool, d, f, chunk=256):
+    """Re-lay the canonical experts of `pool` (numpy [P][B_x]) into the
+    device block layout, chunk by chunk through device memory, on the GPU."""
+    import torch
+    from expert_cached_decode_gb300.layer import moe_pack_experts
+    n, B = pool.shape
+    src = torch.empty((chunk, B), dtype=torch.uint8, device="cuda")
+    dst = torch.empty((chunk, B), dtype=torch.uint8, device="cuda")
+    for i0 in range(0, n, chunk):
+        m = min(chunk, n - i0)
+        src[:m].copy_(torch.from_numpy(pool[i0:i0 + m]))
+        moe_pack_experts(src[:m], dst[:m], m, d, f)
+        torch.from_numpy(pool[i0:i0 + m]).copy_(dst[:m].cpu())
+    torch.cuda.synchronize()
+
+
 def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
     """Host -> device bandwidth of back-to-back expert-sized copies from pinned memory."""
     import torch
@@ -310,11 +326,14 @@ def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
     return float(np.median(out))
 
 
-def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1):
+def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1):
     """48-layer stack with the 8,445-slot cache that starts empty (miss path):
     the warm-up passes over the call stream, then the measured pass.
     miss_mode 1: the GPU reads missing experts from the host pool itself;
-    0: the host issues the copies after reading the routing plan."""
+    0: the host issues the copies after reading the routing plan.
+    pool_layout 1: the host pool holds the device block layout (converted
+    once at setup), so a missing expert is computed straight from it while
+    it is written to its slot; 0: canonical, fetched and re-laid out first."""
     import time
     import torch
     from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA, expert_nbytes
@@ -325,12 +344,14 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1):
     t0 = time.time()
     xs = draw_stack_tokens(cfg_id, calls, wl.n_layers)
     shm, pool = make_host_pool(cfg_id, P)
+    if pool_layout == 1:
+        pack_pool_in_place(pool, wl.d, wl.f)
     s = Synth(wl, bias_lambda=BIAS_LAMBDA)
     wr = np.stack([s.router(l)[0] for l in range(wl.n_layers)])
     b = np.stack([s.router(l)[2] for l in range(wl.n_layers)])
     shared = np.stack([s.shared_packed(l) for l in range(wl.n_layers)])
     layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
-                     host_pool_entries=0 if P == wl.keys else P)
+                     host_pool_entries=0 if P == wl.keys else P, host_pool_layout=pool_layout)
     layer.moe_set_miss_mode(miss_mode)
     layer.moe_cache_configure(wl.capacity)
     setup_s = time.time() - t0
@@ -368,7 +389,12 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1):
     return {"workload": f"{wl.name}: 48 layers, T={wl.tokens} per call, Zipf s={wl.zipf_s} (lambda "
                         f"{BIAS_LAMBDA}), {wl.capacity} slots starting empty, {wl.warm_passes} warm-up passes "
                         f"then the measured pass of {calls} calls",
-            "miss_copies": "GPU reads the host pool" if miss_mode == 1 else "host-issued cudaMemcpyAsync",
+            "miss_copies": ("host-issued cudaMemcpyAsync" if miss_mode == 0 else
+                            "GPU computes each missing expert straight from the host pool (device block layout) "
+                            "and writes it to its victim slot" if pool_layout == 1 else
+                            "GPU fetches each missing expert from the host pool (canonical) into its slot, then "
+                            "computes"),
+            "host_pool_layout": "device block layout" if pool_layout == 1 else "canonical",
             "host_pool_entries": P,
             "host_pool_note": "expert (l, e) is read from entry (512 l + e) mod P; copy sizes, counts and "
                               "the cache's behaviour do not depend on P",
@@ -399,12 +425,13 @@ def run_stack_sweep(pool_entries=2048, calls=500, tokens=(1, 4, 7), capacities=(
     t0 = time.time()
     xs = draw_stack_tokens(cfg_id, calls, wl.n_layers, T=max(tokens))
     shm, pool = make_host_pool(cfg_id, pool_entries)
+    pack_pool_in_place(pool, wl.d, wl.f)
     s = Synth(wl, bias_lambda=BIAS_LAMBDA)
     wr = np.stack([s.router(l)[0] for l in range(wl.n_layers)])
     b = np.stack([s.router(l)[2] for l in range(wl.n_layers)])
     shared = np.stack([s.shared_packed(l) for l in range(wl.n_layers)])
     layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
-                     host_pool_entries=pool_entries)
+                     host_pool_entries=pool_entries, host_pool_layout=1)
     layer.moe_set_miss_mode(1)
     setup_s = time.time() - t0
     xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
@@ -653,7 +680,8 @@ def run_gpu(args):
             try:
                 cfgs = (3, 4) if args.stack_config == 0 else (args.stack_config,)
                 modes = (1, 0) if args.stack_mode < 0 else (args.stack_mode,)
-                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m) for c in cfgs for m in modes]
+                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m, pool_layout=args.stack_pool_layout)
+                                 for c in cfgs for m in modes]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:
@@ -692,6 +720,8 @@ def main():
                          "0 = one per (layer, expert), 50.7 GB, slow to fill (default 2048, 4.2 GB)")
     ap.add_argument("--stack-config", type=int, default=0, choices=(0, 3, 4),
                     help="--stack: 3 = verify stack only, 4 = concurrent stack only (default both)")
+    ap.add_argument("--stack-pool-layout", type=int, default=1, choices=(0, 1),
+                    help="host pool of the stacks: 1 device block layout (default), 0 canonical")
     ap.add_argument("--stack-mode", type=int, default=1, choices=(-1, 0, 1),
                     help="--stack: 1 = GPU pulls misses (default), 0 = host-issued copies, -1 = both")
     ap.add_argument("--stack-sweep", type=int, default=0, metavar="CALLS",

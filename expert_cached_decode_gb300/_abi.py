@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "
 ENTRY_POINTS = ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                 "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_layer_destroy",
                 "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure",
-                "moe_debug_set_wait_limit", "moe_last_error")
+                "moe_debug_set_wait_limit", "moe_last_error", "moe_pack_experts")
 
 MOE_MISS_HOST_COPY = 0
 MOE_MISS_DEVICE_PULL = 1
@@ -34,7 +34,12 @@ class MoeLayerDesc(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
                 ("shared_q", ctypes.c_void_p), ("host_pool", ctypes.c_void_p),
-                ("host_pool_entries", ctypes.c_int64), ("shared_weight", ctypes.c_float)]
+                ("host_pool_entries", ctypes.c_int64), ("shared_weight", ctypes.c_float),
+                ("host_pool_layout", ctypes.c_int32)]
+
+
+MOE_POOL_CANONICAL = 0
+MOE_POOL_DEVICE = 1
 
 
 class MoeStats(ctypes.Structure):
@@ -81,11 +86,13 @@ def load():
     L.moe_set_miss_mode.argtypes = [vp, i32]
     L.moe_debug_inject_failure.argtypes = [i32, i64]
     L.moe_debug_set_wait_limit.argtypes = [vp, i64]
+    L.moe_pack_experts.argtypes = [vp, vp, i64, i32, i32, vp]
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     for name in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                  "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_route_topk_noalloc",
-                 "moe_set_miss_mode", "moe_debug_inject_failure", "moe_debug_set_wait_limit"):
+                 "moe_set_miss_mode", "moe_debug_inject_failure", "moe_debug_set_wait_limit",
+                 "moe_pack_experts"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

@@ -80,6 +80,7 @@ struct moe_ctx {
   const uint8_t* host_pool = nullptr;
   const uint8_t* host_pool_dev = nullptr;   // device address of the registered pool (NULL: none)
   bool pull = false;                        // misses pulled by the GPU
+  bool pool_dev_layout = false;             // host pool entries already in the device block layout
   int64_t P = 0;
   bool registered = false;
   // cache
@@ -280,6 +281,8 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   if (!D.router_w || !D.shared_q || !D.host_pool)
     return fail(MOE_ERR_INVALID_ARG, "router_w, shared_q and host_pool are required");
   if (D.host_pool_entries < 0) return fail(MOE_ERR_INVALID_ARG, "host_pool_entries < 0");
+  if (D.host_pool_layout != MOE_POOL_CANONICAL && D.host_pool_layout != MOE_POOL_DEVICE)
+    return fail(MOE_ERR_INVALID_ARG, "host_pool_layout must be MOE_POOL_CANONICAL or MOE_POOL_DEVICE");
 
   moe_ctx* c = new moe_ctx();
   c->d = D.d;
@@ -291,6 +294,7 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   c->shared_weight = D.shared_weight;
   c->P = D.host_pool_entries ? D.host_pool_entries : (int64_t)D.n_layers * D.n_experts;
   c->host_pool = static_cast<const uint8_t*>(D.host_pool);
+  c->pool_dev_layout = D.host_pool_layout == MOE_POOL_DEVICE;
   moe_status st = MOE_OK;
 #define CREATE_TRY(call)                      \
   do {                                        \
@@ -520,7 +524,16 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
   c->qcur = 0;
   CUDA_TRY(cudaMemset(c->clock, 0, sizeof(int64_t)));
   CUDA_TRY(cudaMemset(c->stats, 0, (size_t)c->L * ST_N * sizeof(int64_t)));
-  // preload: gather the canonical experts of the keys (pool entry key mod P)
+  // preload: the experts of the keys (pool entry key mod P) into slots 0, 1,
+  // ...: a copy each from a device-layout pool, else gathered and re-laid out
+  if (c->pool_dev_layout) {
+    for (int64_t i = 0; i < n_pre; ++i)
+      CUDA_TRY(cudaMemcpyAsync(c->slots + (size_t)i * c->B, c->host_pool + (size_t)(keys[i] % c->P) * c->B, c->B,
+                               cudaMemcpyHostToDevice, 0));
+    CUDA_TRY(cudaDeviceSynchronize());
+    c->configured = true;
+    return MOE_OK;
+  }
   std::vector<int32_t> slot_ids(chunk);
   uint8_t* stage = static_cast<uint8_t*>(tmp.p[0]);
   int32_t* slots_dev = static_cast<int32_t*>(tmp.p[1]);
@@ -722,6 +735,7 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   fa.q_out = c->lruq[c->qcur ^ 1];
   fa.C = (int)c->C;
   fa.host_pool = c->host_pool_dev;
+  fa.direct = c->pool_dev_layout ? 1 : 0;
   fa.pool_entries = c->P;
   fa.staging = c->staging;
   fa.staging_n = c->staging_n;
@@ -801,7 +815,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
     c->qcur ^= 1;
     const MissFetch mf{c->p_miss_expert, c->p_miss_slot, c->host_pool_dev, c->P, c->slots, c->B,
                        layer, c->E, c->d, c->f};
-    CUDA_TRY(launch_prefill_fetch(mf, c->p_info, s, c->num_sms));
+    CUDA_TRY(launch_prefill_fetch(mf, c->p_info, c->pool_dev_layout, s, c->num_sms));
   }
   PrefillPlanArgs pa{};
   pa.counts = c->p_counts;
@@ -947,6 +961,7 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
     mp.layer = layer;
     mp.E = c->E;
     mp.err = c->err;
+    mp.dst_slots = c->pool_dev_layout ? c->slots : nullptr;
     CUDA_TRY(launch_miss_pull(mp, s, c->num_sms));
     RepackArgs rp{};
     rp.src = c->staging;
@@ -956,7 +971,7 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
     rp.d = c->d;
     rp.f = c->f;
     rp.plan = c->plan;
-    CUDA_TRY(launch_repack_misses(rp, s, c->num_sms));
+    if (!c->pool_dev_layout) CUDA_TRY(launch_repack_misses(rp, s, c->num_sms));
     CommitArgs ca{};
     ca.plan = c->plan;
     ca.counters = c->counters;
@@ -986,10 +1001,10 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
     const int64_t entry = key % c->P;
     if (injected(MOE_INJECT_MISS_COPY))
       return fail(MOE_ERR_CUDA, "injected failure: issue of miss copy %d of the layer-call", j);
-    CUDA_TRY(cudaMemcpyAsync(c->staging + (size_t)j * c->B, c->host_pool + (size_t)entry * c->B, c->B,
-                             cudaMemcpyHostToDevice, c->side));
+    uint8_t* dst = c->pool_dev_layout ? c->slots + (size_t)p.miss_slot[j] * c->B : c->staging + (size_t)j * c->B;
+    CUDA_TRY(cudaMemcpyAsync(dst, c->host_pool + (size_t)entry * c->B, c->B, cudaMemcpyHostToDevice, c->side));
   }
-  if (m > 0) {
+  if (m > 0 && !c->pool_dev_layout) {
     RepackArgs rp{};
     rp.src = c->staging;
     rp.src_stride = c->B;
@@ -1095,5 +1110,47 @@ extern "C" moe_status moe_cache_export(moe_ctx* c, int32_t* owner, int64_t* stam
   CUDA_TRY(cudaDeviceSynchronize());
   CUDA_TRY(cudaMemcpy(owner, c->owner, c->C * sizeof(int32_t), cudaMemcpyDeviceToHost));
   CUDA_TRY(cudaMemcpy(stamp, c->stamp, c->C * sizeof(int64_t), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+// The GPU address of a buffer the GPU can reach (device memory, or
+// page-locked host memory through its mapping); NULL otherwise.
+static const void* gpu_address(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
+extern "C" moe_status moe_pack_experts(const void* src, void* dst, int64_t n, int32_t d, int32_t f, void* stream) {
+  if (!src || !dst) return fail(MOE_ERR_INVALID_ARG, "NULL src or dst");
+  if (n < 0) return fail(MOE_ERR_INVALID_ARG, "n < 0");
+  if (d <= 0 || d % 256 != 0 || d > 2048)
+    return fail(MOE_ERR_INVALID_ARG, "d must be a positive multiple of 256, at most 2048");
+  if (f <= 0 || f % 64 != 0 || f > 1024) return fail(MOE_ERR_INVALID_ARG, "f must be a multiple of 64 in [64, 1024]");
+  if (n == 0) return MOE_OK;
+  const int64_t B = (int64_t)3 * d * f * 3 / 8 + (int64_t)3 * d * f / 32 * 2;
+  const uint8_t* s8 = static_cast<const uint8_t*>(src);
+  const uint8_t* d8 = static_cast<const uint8_t*>(dst);
+  if (s8 < d8 + n * B && d8 < s8 + n * B) return fail(MOE_ERR_INVALID_ARG, "src and dst overlap");
+  const void* sg = gpu_address(src);
+  const void* dg = gpu_address(dst);
+  if (!sg || !dg) return fail(MOE_ERR_INVALID_ARG, "src and dst must be device memory or page-locked host memory");
+  const int64_t chunk = 1 << 16;   // experts per launch (the grid stays far below its limit)
+  for (int64_t i0 = 0; i0 < n; i0 += chunk) {
+    RepackArgs ra{};
+    ra.src = static_cast<const uint8_t*>(sg) + i0 * B;
+    ra.src_stride = B;
+    ra.dst_base = const_cast<uint8_t*>(static_cast<const uint8_t*>(dg)) + i0 * B;
+    ra.dst_stride = B;
+    ra.n_experts = (int)(n - i0 < chunk ? n - i0 : chunk);
+    ra.d = d;
+    ra.f = f;
+    CUDA_TRY(launch_repack(ra, static_cast<cudaStream_t>(stream)));
+  }
   return MOE_OK;
 }

@@ -113,6 +113,14 @@ struct DCfg {
   static constexpr int MAXSDN = kMaxRD / SB;       // down stages of a unit at most
 };
 
+// Per mode: with the host pool in the device layout two more warps copy the
+// stages of missing experts from the host pool into the ring.
+template <int NT, int MODE>
+struct KCfg : DCfg<NT> {
+  static constexpr int HSW = MODE == kFusedCachedDirect ? 2 : 0;   // host-stage warps
+  static constexpr int THREADS = (DCfg<NT>::CW + 2 + HSW) * 32;
+};
+
 // Index in U of chosen expert `id`.
 __device__ __forceinline__ int dsel_act_index(const SelSmem* s, int id) { return sel_act_index(s, id); }
 
@@ -566,15 +574,20 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
 // MODE kPlanRead: the routing plan comes from memory (routing kernel and
 // host-issued miss copies before this launch).  kFusedResident: routing in
 // this kernel, every key resident.  kFusedCached: routing in this kernel with
-// a cache that may miss (CTA 0 manages the cache).
+// a cache that may miss (CTA 0 manages the cache; the other CTAs fetch the
+// misses into their victim slots, then compute).  kFusedCachedDirect: the
+// same with the host pool in the device layout: a missing expert's stages
+// are copied from the host pool into the ring by the host-stage warps, which
+// also write them into the victim slot, so no fetch runs ahead of the units.
 template <int NT, int MODE>
-__global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArgs a) {
+__global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(FfnArgs a) {
   using Cfg = DCfg<NT>;
   constexpr int CW = Cfg::CW, BPW = Cfg::BPW, NS = Cfg::NS, NQ = Cfg::NQ, SB = Cfg::SB, MAXSDN = Cfg::MAXSDN;
   constexpr int SBYTES = Cfg::SBYTES;
   constexpr int NCT = CW * 32;   // consumer threads (named barrier 1)
   constexpr bool FUSED = MODE != kPlanRead;
-  constexpr bool CACHED = MODE == kFusedCached;
+  constexpr bool DIRECT = MODE == kFusedCachedDirect;
+  constexpr bool CACHED = MODE == kFusedCached || DIRECT;
   extern __shared__ __align__(128) uint8_t smem[];
   const int d = a.d, f = a.f, T = a.T, K = a.k;
   const int RG = f / 32;            // f slices = units per expert
@@ -613,6 +626,13 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
   // of the consumers around further barriers is the same in all of them.
   __shared__ volatile int s_abort;
   __shared__ int s_cab;
+  // direct mode: ring stages the producer hands to the host-stage warps, in
+  // ring order (host source, victim-slot destination, bytes (0 ends), stage)
+  constexpr int NDQ = DIRECT ? NS : 1;
+  __shared__ const uint8_t* s_dq_src[NDQ];
+  __shared__ uint8_t* s_dq_dst[NDQ];
+  __shared__ int s_dq_bytes[NDQ], s_dq_stage[NDQ];
+  __shared__ uint64_t s_dq_full[NDQ], s_dq_empty[NDQ];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -629,6 +649,11 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       mbar_init(&empty[i], CW);
     }
     mbar_init(plan_ready, 1);
+    if (DIRECT)
+      for (int i = 0; i < NDQ; ++i) {
+        mbar_init(&s_dq_full[i], 1);
+        mbar_init(&s_dq_empty[i], 1);
+      }
     s_abort = 0;
     s_cab = 0;
     mbar_init_fence();
@@ -672,6 +697,44 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       }
       return true;
     };
+    // direct mode: a missing expert's stages go to the host-stage warps
+    // (source in the host pool, destination the victim slot), in ring order
+    uint32_t nd = 0;   // stages handed over
+    auto hand_over = [&](const uint8_t* src, uint8_t* dst, uint32_t bytes, int s) -> bool {
+      const int q = nd % NDQ;
+      if (nd >= (uint32_t)NDQ && !mbar_wait(&s_dq_empty[q], (nd / NDQ - 1) & 1, lim)) return false;
+      s_dq_src[q] = src;
+      s_dq_dst[q] = dst;
+      s_dq_bytes[q] = (int)bytes;
+      s_dq_stage[q] = s;
+      mbar_arrive(&s_dq_full[q]);
+      ++nd;
+      return true;
+    };
+    auto issue_unit_host = [&](const uint8_t* hb, uint8_t* vb, int rb) -> bool {
+      const int64_t gu = gu_block_offset(rb, 0, 0, d), dn = down_block_offset(0, rb, d, f);
+      for (int st = 0; st < SGU + SDN; ++st, ++it) {
+        if (s_abort) return false;
+        const int s = it % NS;
+        const uint32_t use = it / NS;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, lim)) return false;
+        int64_t off;
+        uint32_t bytes;
+        if (st < SGU) {
+          const int b0 = st * SB;
+          const int nb = NGU - b0 < SB ? NGU - b0 : SB;
+          off = gu + (int64_t)b0 * kBlockBytes;
+          bytes = (uint32_t)nb * kBlockBytes;
+        } else {
+          const int b0 = (st - SGU) * SB;
+          const int nb = RD - b0 < SB ? RD - b0 : SB;
+          off = dn + (int64_t)b0 * kBlockBytes;
+          bytes = (uint32_t)nb * kBlockBytes;
+        }
+        if (!hand_over(hb + off, vb + off, bytes, s)) return false;
+      }
+      return true;
+    };
     // the shared expert's weights never change: its units start at once
     for (int rb = sh0; rb < sh1 && ok; ++rb) ok = issue_unit(a.shared_expert, rb);
     pdl_wait();   // slots (and their contents) may have been written by earlier work
@@ -683,12 +746,28 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       const int u0 = s_u0, u1 = s_u1;
       const uint32_t jpm = (uint32_t)(2 * RG + RD);   // fetch jobs per missing expert
       const uint32_t* ready = a.counters + 1 + (size_t)(s_calls & 1u) * a.set_words + 3;
+      const uint32_t* vict_w = a.counters + 1 + (size_t)(s_calls & 1u) * a.set_words + 2;
+      bool have_victims = false;
       for (int u = u0; u < u1 && ok; ++u) {
         const int ai = s_order[u / RG];
         const int j = CACHED ? s_mrank[ai] : -1;
         const uint8_t* eb;
         if (j < 0) {
           eb = expert_base(ai);
+        } else if (DIRECT) {
+          // a missing expert: its victim slot is known once CTA 0 has
+          // published the victims
+          if (!have_victims) {
+            if (!wait_flag_geq(vict_w, 1u, lim)) {
+              ok = false;
+              break;
+            }
+            have_victims = true;
+          }
+          const int64_t entry = ((int64_t)a.layer * a.E + s_act_expert[ai]) % a.pool_entries;
+          uint8_t* vb = const_cast<uint8_t*>(a.slots) + (int64_t)__ldcg(&a.plan->miss_slot[j]) * a.expert_bytes;
+          ok = issue_unit_host(a.host_pool + entry * a.expert_bytes, vb, u % RG);
+          continue;
         } else {
           // a missing expert: every job of its fetch is done (other CTAs'
           // generic stores, ordered before the bulk copies by the proxy fence)
@@ -706,12 +785,66 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
       set_error(a.err, DEV_TIMEOUT_BARRIER);
       s_abort = 1;
     }
+    if (DIRECT && !hand_over(nullptr, nullptr, 0u, 0)) {   // no more stages: the host-stage warps stop
+      set_error(a.err, DEV_TIMEOUT_BARRIER);
+      s_abort = 1;
+    }
     // no copy may still be in flight when the CTA exits: wait, bounded, for
     // the last ones
     for (uint32_t k = it > (uint32_t)NS ? it - NS : 0; k < it; ++k)
       if (!mbar_wait(&full[k % NS], (k / NS) & 1, lim)) set_error(a.err, DEV_TIMEOUT_BARRIER);
     MOE_TLS(5);
     return;
+  }
+  if (DIRECT && warp >= CW + 2) {
+    // ---------------- host-stage warps (direct mode) --------------------------
+    // Each stage the producer hands over is copied by these 64 threads from
+    // the host pool (16-byte pieces, all of a thread's pieces in flight at
+    // once) into its ring stage and into the victim slot; then one thread
+    // completes the stage's full barrier (no bytes are expected on it) and
+    // frees the hand-over entry.  Nothing in this call reads the victim
+    // slot: every unit of a missing expert takes its stages from the host.
+    if (ct < 0) return;
+    const int ht = tid - (CW + 2) * 32;
+    constexpr int PER = (SBYTES / 16 + 63) / 64;   // 16-byte pieces per thread of a stage
+#pragma unroll 1
+    for (uint32_t k = 0;; ++k) {
+      const int q = k % NDQ;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_dq_full[q], (k / NDQ) & 1, lim))) {
+        if (lane == 0) {
+          set_error(a.err, DEV_TIMEOUT_BARRIER);
+          s_abort = 1;
+        }
+        return;
+      }
+      const int n = s_dq_bytes[q] / 16;
+      if (n == 0) return;
+      const uint4* src = reinterpret_cast<const uint4*>(s_dq_src[q]);
+      uint4* dst = reinterpret_cast<uint4*>(s_dq_dst[q]);
+      const int st = s_dq_stage[q];
+      uint4* stg = reinterpret_cast<uint4*>(ring + (size_t)st * SBYTES);
+      uint4 v[PER];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int c = ht + 64 * i;
+        if (c < n) v[i] = src[c];
+      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int c = ht + 64 * i;
+        if (c < n) {
+          stg[c] = v[i];
+          dst[c] = v[i];
+        }
+      }
+      fence_proxy_async_smem();   // the stage is refilled by bulk copies later
+      named_bar(3, 64);
+      if (ht == 0) {
+        mbar_arrive(&full[st]);
+        mbar_arrive(&s_dq_empty[q]);
+      }
+      __syncwarp();
+    }
   }
   if (warp == CW + 1) {
     // ---------------- control: the call's plan, stamps and counters ---------
@@ -1014,7 +1147,7 @@ __global__ void __launch_bounds__(DCfg<NT>::THREADS, 1) decode_ffn_kernel(FfnArg
         mbar_arrive(plan_ready);
         MOE_TLS(8);
       }
-      if (CACHED && n_miss > 0) {
+      if (CACHED && !DIRECT && n_miss > 0) {
         // fetch jobs of the misses, spread over the tile CTAs, once CTA 0 has
         // published the victims
         if (tid == 0) {
@@ -1265,7 +1398,7 @@ static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int gri
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(DCfg<NT>::THREADS);
+  cfg.blockDim = dim3(KCfg<NT, MODE>::THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1280,10 +1413,12 @@ cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl) {
   if (a.grid <= 0 || (a.cached && (!a.fused || a.grid < 2))) return cudaErrorInvalidValue;
   if (a.T <= 8) {
     if (!a.fused) return launch_nt<1, kPlanRead>(a, s, pdl, a.grid);
-    return a.cached ? launch_nt<1, kFusedCached>(a, s, pdl, a.grid) : launch_nt<1, kFusedResident>(a, s, pdl, a.grid);
+    if (!a.cached) return launch_nt<1, kFusedResident>(a, s, pdl, a.grid);
+    return a.direct ? launch_nt<1, kFusedCachedDirect>(a, s, pdl, a.grid) : launch_nt<1, kFusedCached>(a, s, pdl, a.grid);
   }
   if (!a.fused) return launch_nt<2, kPlanRead>(a, s, pdl, a.grid);
-  return a.cached ? launch_nt<2, kFusedCached>(a, s, pdl, a.grid) : launch_nt<2, kFusedResident>(a, s, pdl, a.grid);
+  if (!a.cached) return launch_nt<2, kFusedResident>(a, s, pdl, a.grid);
+  return a.direct ? launch_nt<2, kFusedCachedDirect>(a, s, pdl, a.grid) : launch_nt<2, kFusedCached>(a, s, pdl, a.grid);
 }
 
 // Whether one CTA of every decode-kernel variant fits on an SM at hidden
@@ -1296,16 +1431,18 @@ cudaError_t decode_ffn_fits(int d, bool* fits) {
 #define MOE_FIT(NTV, MODEV)                                                                                   \
   e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_ffn_kernel<NTV, MODEV>), ffn_smem_bytes<NTV>(d)); \
   if (e != cudaSuccess) return e;                                                                             \
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_ffn_kernel<NTV, MODEV>, DCfg<NTV>::THREADS,    \
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_ffn_kernel<NTV, MODEV>, KCfg<NTV, MODEV>::THREADS, \
                                                     ffn_smem_bytes<NTV>(d));                                   \
   if (e != cudaSuccess) return e;                                                                             \
   if (n < 1) *fits = false;
   MOE_FIT(1, kPlanRead)
   MOE_FIT(1, kFusedResident)
   MOE_FIT(1, kFusedCached)
+  MOE_FIT(1, kFusedCachedDirect)
   MOE_FIT(2, kPlanRead)
   MOE_FIT(2, kFusedResident)
   MOE_FIT(2, kFusedCached)
+  MOE_FIT(2, kFusedCachedDirect)
 #undef MOE_FIT
   return cudaSuccess;
 }

@@ -97,6 +97,7 @@ struct MissPullArgs {
   int64_t expert_bytes;
   uint8_t* staging;          // [staging_n][expert_bytes]
   int staging_n;
+  uint8_t* dst_slots;        // if set (device-layout pool): copy into the misses' victim slots instead
   int layer, E;
   uint32_t* err;
 };
@@ -138,7 +139,8 @@ struct FfnArgs {
   const int32_t* q_in;          // [C] slots, least recently used first
   int32_t* q_out;               // [C] the order after this call
   int C;
-  const uint8_t* host_pool;     // device address of the registered host pool (canonical experts)
+  const uint8_t* host_pool;     // device address of the registered host pool
+  int direct;                   // the host pool holds the device block layout (kFusedCachedDirect)
   int64_t pool_entries;         // key (layer, e) reads entry (layer*E + e) mod pool_entries
   uint8_t* staging;             // [staging_n][expert_bytes] canonical copies of this call's misses
   int staging_n;
@@ -149,7 +151,10 @@ struct FfnArgs {
 constexpr int kDecodeSetWords = 3 + kMaxPicks;
 
 // decode kernel modes
-enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2 };
+// kFusedCachedDirect: as kFusedCached with the host pool in the device block
+// layout: a missing expert's stages come straight from the host pool into
+// the units (and into its victim slot), with no fetch ahead of them.
+enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2, kFusedCachedDirect = 3 };
 
 struct RouterGemmArgs {
   const float* bias;   // [E]
@@ -277,7 +282,8 @@ cudaError_t launch_prefill_down(const CUtensorMap& tmH, const CUtensorMap& tmHlo
 cudaError_t launch_prefill_combine(const PrefillCombineArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_cache(const PrefillCacheArgs& a, cudaStream_t s);
 struct MissFetch;
-cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, cudaStream_t s, int num_sms);
+cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, bool device_layout, cudaStream_t s,
+                                 int num_sms);
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
 // whether one CTA of every decode-kernel variant fits on an SM at hidden size d
 cudaError_t decode_ffn_fits(int d, bool* fits);

@@ -206,7 +206,34 @@ cudaError_t launch_prefill_cache(const PrefillCacheArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, cudaStream_t s, int num_sms) {
+// With the host pool in the device block layout a miss is a plain copy of
+// its bytes: 16-byte pieces over the whole grid, four in flight per thread.
+__global__ void __launch_bounds__(256) prefill_copy_kernel(MissFetch f, const int32_t* n_miss) {
+  const int m = *n_miss;
+  const int64_t per = f.expert_bytes / 16;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  for (int j = 0; j < m; ++j) {
+    const int64_t entry = ((int64_t)f.layer * f.E + __ldcg(&f.miss_expert[j])) % f.pool_entries;
+    const uint4* src = reinterpret_cast<const uint4*>(f.host_pool + entry * f.expert_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(f.slots + (int64_t)__ldcg(&f.miss_slot[j]) * f.expert_bytes);
+    int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; c + 3 * nthr < per; c += 4 * nthr) {
+      const uint4 v0 = src[c], v1 = src[c + nthr], v2 = src[c + 2 * nthr], v3 = src[c + 3 * nthr];
+      dst[c] = v0;
+      dst[c + nthr] = v1;
+      dst[c + 2 * nthr] = v2;
+      dst[c + 3 * nthr] = v3;
+    }
+    for (; c < per; c += nthr) dst[c] = src[c];
+  }
+}
+
+cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, bool device_layout, cudaStream_t s,
+                                 int num_sms) {
+  if (device_layout) {
+    prefill_copy_kernel<<<4 * num_sms, 256, 0, s>>>(f, n_miss);
+    return cudaGetLastError();
+  }
   const size_t dyn = fetch_job_bytes(f.d, f.f);
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(prefill_fetch_kernel), dyn);
   if (e != cudaSuccess) return e;

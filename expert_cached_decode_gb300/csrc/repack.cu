@@ -39,7 +39,8 @@ __global__ void __launch_bounds__(256) miss_pull_kernel(MissPullArgs a) {
   for (int j = 0; j < m; ++j) {
     const int64_t entry = ((int64_t)a.layer * a.E + a.plan->miss_expert[j]) % a.pool_entries;
     const uint4* src = reinterpret_cast<const uint4*>(a.host_pool + entry * a.expert_bytes);
-    uint4* dst = reinterpret_cast<uint4*>(a.staging + (int64_t)j * a.expert_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(a.dst_slots ? a.dst_slots + (int64_t)a.plan->miss_slot[j] * a.expert_bytes
+                                                      : a.staging + (int64_t)j * a.expert_bytes);
     int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; c + 3 * nthr < per; c += 4 * nthr) {   // four loads in flight per thread
       const uint4 v0 = src[c], v1 = src[c + nthr], v2 = src[c + 2 * nthr], v3 = src[c + 3 * nthr];

@@ -46,13 +46,13 @@ class MoELayer:
     """
 
     def __init__(self, d, f, n_experts, top_k, n_layers, router_w, router_b, shared_q, host_pool,
-                 host_pool_entries=0, shared_weight=1.0, group=32):
+                 host_pool_entries=0, shared_weight=1.0, group=32, host_pool_layout=0):
         self._lib = _abi.load()
         self._keep = (router_w, router_b, shared_q, host_pool)
         desc = MoeLayerDesc(d=d, f=f, n_experts=n_experts, top_k=top_k, n_layers=n_layers, group=group,
                             router_w=_ptr(router_w), router_b=_ptr(router_b), shared_q=_ptr(shared_q),
                             host_pool=_ptr(host_pool), host_pool_entries=host_pool_entries,
-                            shared_weight=shared_weight)
+                            shared_weight=shared_weight, host_pool_layout=host_pool_layout)
         ctx = ctypes.c_void_p()
         check(self._lib.moe_layer_create(ctypes.byref(desc), ctypes.byref(ctx)), "moe_layer_create")
         self.ctx = ctx
@@ -145,3 +145,12 @@ def moe_route_topk_noalloc(x, router_w, router_b, top_k, idx, w, stream=None):
     E = router_w.shape[0]
     check(L.moe_route_topk_noalloc(_ptr(x), _ptr(router_w), _ptr(router_b), T, d, E, top_k, _ptr(idx), _ptr(w),
                                    _stream(stream)), "moe_route_topk_noalloc")
+
+
+def moe_pack_experts(src, dst, n, d, f, stream=None):
+    """Binding of moe_pack_experts: n experts of shape (d, f), canonical
+    packed bytes in `src` -> device block layout in `dst`.  Both are uint8
+    tensors on the GPU or in page-locked host memory, B_x * n bytes each.
+    Asynchronous on `stream`."""
+    L = _abi.load()
+    check(L.moe_pack_experts(_ptr(src), _ptr(dst), int(n), int(d), int(f), _stream(stream)), "moe_pack_experts")

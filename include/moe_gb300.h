@@ -80,7 +80,15 @@ typedef struct {
   int64_t host_pool_entries; /* P; identity (l, e) reads entry (l*E + e) mod P;
                                 0 means P = L*E (one entry per identity) */
   float shared_weight;     /* weight of the shared expert in the combine (1.0) */
+  int32_t host_pool_layout; /* MOE_POOL_CANONICAL (0): host_pool entries in the
+                              canonical packed format; MOE_POOL_DEVICE (1): in the
+                              device block layout (moe_pack_experts), so a miss is
+                              a plain copy and the decode kernel computes a missing
+                              expert straight from the host pool while it writes
+                              the expert into its victim slot */
 } moe_layer_desc;
+
+enum { MOE_POOL_CANONICAL = 0, MOE_POOL_DEVICE = 1 };
 
 /* Cumulative counters since the last moe_cache_configure.  A token pick is a
  * hit iff its (layer, expert) was resident when the layer-call began ("hits /
@@ -248,6 +256,17 @@ moe_status moe_route_topk_noalloc(const void* x_bf16, const void* router_w_bf16,
 
 /* Message of the last failing call on this thread ("" if none). */
 const char* moe_last_error(void);
+
+/* Re-lay n experts of shape (d, f) from the canonical packed format (src) into
+ * the device block layout (dst), each expert B_x bytes, on `stream` (a
+ * cudaStream_t, NULL for the default stream); asynchronous.  src and dst must
+ * not overlap and must be addressable by the GPU: device memory or
+ * page-locked host memory.  The same bytes, permuted: the layout the slots
+ * hold (32-row x 32-input blocks of codes and scales in mma fragment order).
+ * No counterpart on the pages, which keep experts in their file format; it
+ * prepares a host pool once, before moe_layer_create with MOE_POOL_DEVICE.
+ * Errors: INVALID_ARG (shapes as for moe_layer_create, n < 0, NULL), CUDA. */
+moe_status moe_pack_experts(const void* src, void* dst, int64_t n, int32_t d, int32_t f, void* stream);
 
 #ifdef __cplusplus
 }

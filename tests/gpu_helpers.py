@@ -20,8 +20,10 @@ def make_pool(s: Synth, entries):
     return pool
 
 
-def make_layer(s: Synth, pool_entries=None, layers=None):
-    from expert_cached_decode_gb300.layer import MoELayer
+def make_layer(s: Synth, pool_entries=None, layers=None, pool_layout=0):
+    """pool_layout 1: the canonical pool is re-laid out on the GPU
+    (moe_pack_experts) into a second pinned buffer that the layer uses."""
+    from expert_cached_decode_gb300.layer import MoELayer, moe_pack_experts
     wl = s.wl
     L = wl.n_layers
     P = wl.keys if pool_entries is None else pool_entries
@@ -29,8 +31,13 @@ def make_layer(s: Synth, pool_entries=None, layers=None):
     b = np.stack([s.router(l)[2] for l in range(L)])
     shared = np.stack([s.shared_packed(l) for l in range(L)])
     pool = make_pool(s, P)
+    if pool_layout == 1:
+        packed = torch.empty_like(pool).pin_memory()
+        moe_pack_experts(pool, packed, P, wl.d, wl.f)
+        torch.cuda.synchronize()
+        pool = packed
     layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, L, wr, b, shared, pool,
-                     host_pool_entries=0 if P == wl.keys else P)
+                     host_pool_entries=0 if P == wl.keys else P, host_pool_layout=pool_layout)
     layer._pool = pool
     layer._shared_np = shared
     return layer

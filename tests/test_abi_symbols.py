@@ -59,3 +59,10 @@ def test_null_arguments_are_rejected_without_a_gpu(lib_path):
     assert b"NULL" in L.moe_last_error()
     assert L.moe_forward(None, 0, None, 1, None, None, None) == -1
     L.moe_layer_destroy(None)
+    # the pool re-layout checks its arguments before touching the GPU
+    buf = ctypes.create_string_buffer(64)
+    assert L.moe_pack_experts(None, buf, 1, 256, 64, None) == -1
+    assert L.moe_pack_experts(buf, buf, -1, 256, 64, None) == -1
+    assert L.moe_pack_experts(buf, buf, 1, 200, 64, None) == -1
+    assert L.moe_pack_experts(buf, buf, 1, 256, 96, None) == -1
+    assert L.moe_pack_experts(buf, buf, 0, 256, 64, None) == 0

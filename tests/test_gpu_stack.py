@@ -31,8 +31,10 @@ POOL_ENTRIES = 2048
 
 
 def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None, miss_mode=None,
-              prefill=None):
-    """... then, with prefill=(layer, T), one prefill chunk of T tokens at that
+              prefill=None, pool_layout=0):
+    """Every layer-call of `passes` passes over the stack, compared with the
+    oracle (pool_layout 1: the host pool in the device block layout) ...
+    then, with prefill=(layer, T), one prefill chunk of T tokens at that
     layer on the warm cache: its cache step (slots, misses, victims, evicted
     keys, counts) bit-exact against the oracle's and every output within
     2e-3 * rms."""
@@ -48,7 +50,7 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
         for b in range(calls):
             so.routes[(b, l)] = (idx[l, b].astype(np.int64), w[l, b])
             so.x_bits[(b, l)] = xs[l, b]
-    layer = make_layer(s, pool_entries=pool_entries)
+    layer = make_layer(s, pool_entries=pool_entries, pool_layout=pool_layout)
     if miss_mode is not None:
         layer.moe_set_miss_mode(miss_mode)
     layer.moe_cache_configure(wl.capacity)            # empty cache
@@ -112,15 +114,21 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
     return meas["hits"] / meas["picks"], tot, st
 
 
+@pytest.mark.parametrize("pool_layout", [0, 1])
 @pytest.mark.parametrize("miss_mode,tokens", [(MOE_MISS_DEVICE_PULL, 5), (MOE_MISS_HOST_COPY, 5),
-                                             (MOE_MISS_DEVICE_PULL, 1)])
-def test_small_stack_with_evictions(miss_mode, tokens):
+                                             (MOE_MISS_DEVICE_PULL, 1), (MOE_MISS_DEVICE_PULL, 12)])
+def test_small_stack_with_evictions(miss_mode, tokens, pool_layout):
     # both ways of fetching misses: the GPU reading the host pool, or host-issued copies;
-    # one-token calls take the selection's single-token path
+    # one-token calls take the selection's single-token path, 12-token calls the second
+    # n-tile; pool_layout 1 keeps the host pool in the device block layout (a missing
+    # expert computed straight from the host pool while it is written to its slot)
     over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=tokens, capacity=40, calls=60)
+    if tokens > 8:
+        over["capacity"] = 64
     rate, tot, _ = run_stack(3, passes=2, pool_entries=96, overrides=over,
                              ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode,
-                             prefill=(2, 300) if miss_mode == MOE_MISS_DEVICE_PULL else None)
+                             prefill=(2, 300) if miss_mode == MOE_MISS_DEVICE_PULL else None,
+                             pool_layout=pool_layout)
     assert tot["evictions"] > 0 and tot["token_misses"] > 0
     assert 0.0 < rate < 1.0
 
