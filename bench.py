@@ -326,14 +326,18 @@ def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
     return float(np.median(out))
 
 
-def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1):
+def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, ahead=False):
     """48-layer stack with the 8,445-slot cache that starts empty (miss path):
     the warm-up passes over the call stream, then the measured pass.
     miss_mode 1: the GPU reads missing experts from the host pool itself;
     0: the host issues the copies after reading the routing plan.
     pool_layout 1: the host pool holds the device block layout (converted
     once at setup), so a missing expert is computed straight from it while
-    it is written to its slot; 0: canonical, fetched and re-laid out first."""
+    it is written to its slot; 0: canonical, fetched and re-laid out first.
+    ahead: every layer-call made with moe_forward_ahead naming the next
+    layer-call of its pass (cross-layer lookahead; the stack's layers take
+    independent tokens), so its routing, cache step and misses run one
+    launch early; the first call of a pass prepares itself."""
     import time
     import torch
     from moe_inputs import Synth, WORKLOADS, BIAS_LAMBDA, expert_nbytes
@@ -358,19 +362,26 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1):
     xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
     y = torch.empty((wl.tokens, wl.d), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
+    steps = [(c, l) for c in range(calls) for l in range(wl.n_layers)]
+
+    def one_pass():
+        for i, (c, l) in enumerate(steps):
+            if ahead:
+                nc, nl = steps[i + 1] if i + 1 < len(steps) else (0, 0)
+                layer.moe_forward_ahead(l, xdev[l, c], y, next_layer=nl,
+                                        next_x=xdev[nl, nc] if i + 1 < len(steps) else None)
+            else:
+                layer.moe_forward(l, xdev[l, c], y)
+
     with torch.cuda.stream(stream):
         for _ in range(wl.warm_passes):
-            for c in range(calls):
-                for l in range(wl.n_layers):
-                    layer.moe_forward(l, xdev[l, c], y)
+            one_pass()
     stream.synchronize()
     before = layer.moe_cache_stats()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     with torch.cuda.stream(stream):
-        for c in range(calls):
-            for l in range(wl.n_layers):
-                layer.moe_forward(l, xdev[l, c], y)
+        one_pass()
     e1.record(stream)
     stream.synchronize()
     ms = e0.elapsed_time(e1)
@@ -395,6 +406,8 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1):
                             "GPU fetches each missing expert from the host pool (canonical) into its slot, then "
                             "computes"),
             "host_pool_layout": "device block layout" if pool_layout == 1 else "canonical",
+            "lookahead": ("each layer-call routes the next one and copies its misses (moe_forward_ahead)"
+                          if ahead else "none"),
             "host_pool_entries": P,
             "host_pool_note": "expert (l, e) is read from entry (512 l + e) mod P; copy sizes, counts and "
                               "the cache's behaviour do not depend on P",
@@ -680,8 +693,9 @@ def run_gpu(args):
             try:
                 cfgs = (3, 4) if args.stack_config == 0 else (args.stack_config,)
                 modes = (1, 0) if args.stack_mode < 0 else (args.stack_mode,)
-                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m, pool_layout=args.stack_pool_layout)
-                                 for c in cfgs for m in modes]
+                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m, pool_layout=args.stack_pool_layout,
+                                           ahead=a) for c in cfgs for m in modes
+                                 for a in ((False, True) if m == 1 and args.stack_pool_layout == 1 else (False,))]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:

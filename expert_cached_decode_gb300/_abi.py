@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "
 ENTRY_POINTS = ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                 "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_layer_destroy",
                 "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure",
-                "moe_debug_set_wait_limit", "moe_last_error", "moe_pack_experts")
+                "moe_debug_set_wait_limit", "moe_last_error", "moe_pack_experts", "moe_forward_ahead")
 
 MOE_MISS_HOST_COPY = 0
 MOE_MISS_DEVICE_PULL = 1
@@ -87,12 +87,13 @@ def load():
     L.moe_debug_inject_failure.argtypes = [i32, i64]
     L.moe_debug_set_wait_limit.argtypes = [vp, i64]
     L.moe_pack_experts.argtypes = [vp, vp, i64, i32, i32, vp]
+    L.moe_forward_ahead.argtypes = [vp, i32, vp, i32, vp, vp, ctypes.POINTER(MoeTrace), i32, vp]
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     for name in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                  "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_route_topk_noalloc",
                  "moe_set_miss_mode", "moe_debug_inject_failure", "moe_debug_set_wait_limit",
-                 "moe_pack_experts"):
+                 "moe_pack_experts", "moe_forward_ahead"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

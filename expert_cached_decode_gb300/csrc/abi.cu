@@ -81,6 +81,13 @@ struct moe_ctx {
   const uint8_t* host_pool_dev = nullptr;   // device address of the registered pool (NULL: none)
   bool pull = false;                        // misses pulled by the GPU
   bool pool_dev_layout = false;             // host pool entries already in the device block layout
+  // lookahead (moe_forward_ahead): a layer-call whose routing, cache step and
+  // miss copies are done and whose experts run next; its plan is plans(ahead_pi)
+  Plan* plan2 = nullptr;
+  bool ahead_valid = false;
+  int ahead_layer = -1, ahead_T = 0, ahead_pi = 0;
+  const void* ahead_x = nullptr;
+  Plan* plans(int i) { return i ? plan2 : plan; }
   int64_t P = 0;
   bool registered = false;
   // cache
@@ -367,6 +374,7 @@ extern "C" moe_status moe_layer_create(const moe_layer_desc* desc, moe_ctx** out
   CREATE_TRY(dev_alloc(&c->route_cnt, sizeof(uint32_t)));
   CREATE_TRY(cudaMemset(c->route_cnt, 0, sizeof(uint32_t)));
   CREATE_TRY(dev_alloc(&c->plan, sizeof(Plan)));
+  CREATE_TRY(dev_alloc(&c->plan2, sizeof(Plan)));
   CREATE_TRY(cudaMemset(c->plan, 0, sizeof(Plan)));
   CREATE_TRY(cudaHostAlloc(&c->plan_host, sizeof(Plan), cudaHostAllocDefault));
   CREATE_TRY(dev_alloc(&c->ypart, (size_t)c->num_sms * kMaxDecodeT * c->d * sizeof(uint64_t)));
@@ -414,6 +422,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->logits);
   cudaFree(c->route_cnt);
   cudaFree(c->plan);
+  cudaFree(c->plan2);
   if (c->plan_host) cudaFreeHost(c->plan_host);
   cudaFree(c->ypart);
   cudaFree(c->tlogits);
@@ -532,6 +541,7 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
                                cudaMemcpyHostToDevice, 0));
     CUDA_TRY(cudaDeviceSynchronize());
     c->configured = true;
+  c->ahead_valid = false;
     return MOE_OK;
   }
   std::vector<int32_t> slot_ids(chunk);
@@ -560,6 +570,7 @@ extern "C" moe_status moe_cache_configure(moe_ctx* c, int64_t capacity, const in
   }
   CUDA_TRY(cudaDeviceSynchronize());
   c->configured = true;
+  c->ahead_valid = false;
   return MOE_OK;
 }
 
@@ -742,8 +753,8 @@ static FfnArgs ffn_args(moe_ctx* c, int layer, const void* x, int T, float* y) {
   return fa;
 }
 
-static moe_status fill_trace(moe_ctx* c, cudaStream_t s, int T, moe_trace* tr) {
-  CUDA_TRY(cudaMemcpyAsync(c->plan_host, c->plan, sizeof(Plan), cudaMemcpyDeviceToHost, s));
+static moe_status fill_trace(moe_ctx* c, cudaStream_t s, int T, moe_trace* tr, const Plan* plan = nullptr) {
+  CUDA_TRY(cudaMemcpyAsync(c->plan_host, plan ? plan : c->plan, sizeof(Plan), cudaMemcpyDeviceToHost, s));
   CUDA_TRY(cudaStreamSynchronize(s));
   const Plan& p = *c->plan_host;
   const int n = T * c->k;
@@ -918,12 +929,80 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   return MOE_OK;
 }
 
+// One kAhead launch: the current call (layer, x) from plan `cur` when
+// has_cur, and the routing, cache step and miss copies of the next call
+// (next_layer, next_x) into plan `nxt` when has_next.
+static moe_status launch_ahead(moe_ctx* c, bool has_cur, int layer, const void* x, float* y, int T, bool has_next,
+                               int next_layer, const void* next_x, const Plan* cur, Plan* nxt, cudaStream_t s) {
+  const int rl = has_next ? next_layer : layer;   // the routing fields describe the next call
+  FfnArgs fa = ffn_args(c, rl, has_next ? next_x : x, T, y);
+  fa.shared_expert = c->shared + (size_t)layer * c->B;
+  fa.x = static_cast<const uint16_t*>(has_cur ? x : next_x);
+  fa.x_route = static_cast<const uint16_t*>(has_next ? next_x : x);
+  fa.y = y;
+  fa.plan = nxt;
+  fa.cur_plan = cur;
+  fa.has_cur = has_cur ? 1 : 0;
+  fa.has_next = has_next ? 1 : 0;
+  fa.fused = 1;
+  fa.cached = 1;
+  fa.ahead = 1;
+  CUDA_TRY(launch_decode_ffn(fa, s, true));
+  if (has_next) c->qcur ^= 1;
+  else CUDA_TRY(launch_calls_bump(c->counters, s));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_forward_ahead(moe_ctx* c, int32_t layer, const void* x, int32_t T, float* y, void* stream,
+                                        moe_trace* trace, int32_t next_layer, const void* next_x) {
+  moe_status st = check_common(c, layer, x, T, kMaxDecodeT);
+  if (st != MOE_OK) return st;
+  if (!c->configured) return fail(MOE_ERR_STATE, "moe_cache_configure must come first");
+  if (!y) return fail(MOE_ERR_INVALID_ARG, "NULL output");
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(next_x) % 16)
+    return fail(MOE_ERR_INVALID_ARG, "x and next_x must be 16-byte aligned");
+  if (next_x && (next_layer < 0 || next_layer >= c->L))
+    return fail(MOE_ERR_INVALID_ARG, "next layer %d out of range", next_layer);
+  if (!c->pull || !c->pool_dev_layout || c->num_sms < 2 || !c->host_pool_dev)
+    return fail(MOE_ERR_UNIMPLEMENTED,
+                "lookahead needs the GPU miss path and a host pool in the device layout (MOE_POOL_DEVICE)");
+  if (c->C < (int64_t)2 * kMaxDecodeT * c->k)
+    return fail(MOE_ERR_UNIMPLEMENTED, "lookahead needs capacity >= %d (two layer-calls' experts)",
+                2 * kMaxDecodeT * c->k);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!(c->ahead_valid && c->ahead_layer == layer && c->ahead_x == x && c->ahead_T == T)) {
+    if (c->ahead_valid)
+      return fail(MOE_ERR_STATE, "the prepared layer-call (layer %d) must run before another", c->ahead_layer);
+    // no call prepared: route (layer, x), run its cache step and copy its misses
+    st = launch_ahead(c, false, layer, nullptr, nullptr, T, true, layer, x, nullptr, c->plans(c->ahead_pi), s);
+    if (st != MOE_OK) return st;
+  }
+  const Plan* cur = c->plans(c->ahead_pi);
+  st = launch_ahead(c, true, layer, x, y, T, next_x != nullptr, next_layer, next_x, cur, c->plans(c->ahead_pi ^ 1), s);
+  if (st != MOE_OK) {
+    c->ahead_valid = false;
+    return st;
+  }
+  c->ahead_valid = next_x != nullptr;
+  c->ahead_layer = next_layer;
+  c->ahead_x = next_x;
+  c->ahead_T = T;
+  c->ahead_pi ^= 1;
+  if (trace) return fill_trace(c, s, T, trace, cur);
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int32_t T, float* y, void* stream,
                                   moe_trace* trace) {
   moe_status st = check_common(c, layer, x, T, kMaxPrefillT);
   if (st != MOE_OK) return st;
   if (!c->configured) return fail(MOE_ERR_STATE, "moe_cache_configure must come first");
   if (!y) return fail(MOE_ERR_INVALID_ARG, "NULL output");
+  if (c->ahead_valid) {   // a layer-call prepared by moe_forward_ahead comes first
+    if (layer != c->ahead_layer || x != c->ahead_x || T != c->ahead_T)
+      return fail(MOE_ERR_STATE, "the prepared layer-call (layer %d) must run before another", c->ahead_layer);
+    return moe_forward_ahead(c, layer, x, T, y, stream, trace, 0, nullptr);
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (T > kMaxDecodeT) return prefill_forward(c, layer, x, T, y, s, trace);
   if (reinterpret_cast<uintptr_t>(x) % 16) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
@@ -1043,6 +1122,7 @@ extern "C" moe_status moe_forward(moe_ctx* c, int32_t layer, const void* x, int3
 
 extern "C" moe_status moe_set_miss_mode(moe_ctx* c, int32_t mode) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "NULL context");
+  if (c->ahead_valid) return fail(MOE_ERR_STATE, "a layer-call prepared by moe_forward_ahead is pending");
   if (mode == MOE_MISS_HOST_COPY) {
     c->pull = false;
     return MOE_OK;

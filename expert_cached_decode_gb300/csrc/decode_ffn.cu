@@ -117,7 +117,7 @@ struct DCfg {
 // stages of missing experts from the host pool into the ring.
 template <int NT, int MODE>
 struct KCfg : DCfg<NT> {
-  static constexpr int HSW = MODE == kFusedCachedDirect ? 2 : 0;   // host-stage warps
+  static constexpr int HSW = MODE == kFusedCachedDirect || MODE == kAhead ? 2 : 0;   // host-stage warps
   static constexpr int THREADS = (DCfg<NT>::CW + 2 + HSW) * 32;
 };
 
@@ -414,9 +414,10 @@ __device__ __forceinline__ int group_exclusive_scan(int v, int* s_warp, int* tot
 // ascending expert id, take the least recently used slots in (stamp, slot id)
 // order, which is the order of q (least recent first) with the hits skipped.
 // The call's touched slots (hits and victims) move, in slot-id order, to the
-// recent end of q.  The victims are published first (vict[0]), because CTAs
-// 1..G-1 wait for them before pulling the misses; then the commit (table,
-// owners, stamps), the next order, the plan and the statistics.  `scratch`
+// recent end of q.  The victims and the miss count are published first
+// (vict[0], on every call), because CTAs 1..G-1 wait for them before pulling
+// the misses; then the commit (table, owners, stamps), the next order, the
+// plan and the statistics.  `scratch`
 // is shared memory this CTA does not otherwise use.
 template <int NTH>
 __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m, const int* s_act_expert,
@@ -507,10 +508,11 @@ __device__ __forceinline__ void cache_manager(const FfnArgs& a, int n_act, int m
     P->act_hit[i] = s_hitf[i];
     P->act_expert[i] = s_act_expert[i];
   }
+  if (tid == 0) P->n_miss = m;
   named_bar(1, NTH);
-  if (m > 0 && tid == 0) {
+  if (tid == 0) {   // published on every call (lookahead copies wait for it even without misses)
     MOE_TLS(28);
-    red_release_add(&vict[0], 1u);   // covers the plan's victim entries (after the barrier)
+    red_release_add(&vict[0], 1u);   // covers the plan's miss count and victim entries (after the barrier)
   }
   // commit: evicted keys leave the table before the misses enter it
   for (int j = tid; j < m; j += NTH) {
@@ -587,7 +589,8 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
   constexpr int NCT = CW * 32;   // consumer threads (named barrier 1)
   constexpr bool FUSED = MODE != kPlanRead;
   constexpr bool DIRECT = MODE == kFusedCachedDirect;
-  constexpr bool CACHED = MODE == kFusedCached || DIRECT;
+  constexpr bool AHEAD = MODE == kAhead;
+  constexpr bool CACHED = MODE == kFusedCached || DIRECT || AHEAD;
   extern __shared__ __align__(128) uint8_t smem[];
   const int d = a.d, f = a.f, T = a.T, K = a.k;
   const int RG = f / 32;            // f slices = units per expert
@@ -638,8 +641,12 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
   const int G = gridDim.x, cta = blockIdx.x;
   const int GT = CACHED ? G - 1 : G;           // CTAs that take units
   const int ct = CACHED ? cta - 1 : cta;       // tile index (-1: the cache manager)
-  const int sh0 = ct >= 0 ? shared_first(ct, RG, GT) : 0;
-  const int sh1 = ct >= 0 ? shared_first(ct + 1, RG, GT) : 0;
+  // kAhead: whether this launch has a current call to compute and a next
+  // call to route (a launch that only prepares, or only finishes, a sequence)
+  const bool CUR = !AHEAD || a.has_cur != 0;
+  const bool NEXT = !AHEAD || a.has_next != 0;
+  const int sh0 = ct >= 0 && CUR ? shared_first(ct, RG, GT) : 0;
+  const int sh1 = ct >= 0 && CUR ? shared_first(ct + 1, RG, GT) : 0;
 #ifdef MOE_TIMELINE
   if (tid == 0) dtl_begin();
 #endif
@@ -846,6 +853,49 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
       __syncwarp();
     }
   }
+  if (AHEAD && warp >= CW + 2) {
+    // ---------------- miss copies of the next call (kAhead) ------------------
+    // Once CTA 0 has published the next call's victims, the two extra warps
+    // of every tile CTA copy the next call's missing experts (device layout:
+    // the slot's own bytes) from the host pool into their victim slots, an
+    // even share of 16-byte pieces each, four in flight per thread.  The next
+    // launch finds them resident; nothing in this launch reads them.
+    if (ct < 0 || !NEXT) return;
+    int m = 0;
+    if (lane == 0) {
+      // the call's tag (s_calls) is written before the consumers hand the
+      // producer its units: wait for that hand-over, then for the victims
+      const bool tagged = mbar_wait(plan_ready, 0, lim);
+      const uint32_t* vict_w = a.counters + 1 + (size_t)(s_calls & 1u) * a.set_words + 2;
+      if (!tagged || !wait_flag_geq(vict_w, 1u, lim)) {
+        set_error(a.err, DEV_TIMEOUT_FLAG);
+        s_abort = 1;
+      } else {
+        m = __ldcg(&a.plan->n_miss);
+      }
+    }
+    __syncwarp();   // lane 0's acquire of the victims orders the other lanes' plan reads
+    m = __shfl_sync(0xffffffffu, m, 0);
+    const int64_t per = a.expert_bytes / 16;
+    const int64_t nthr = (int64_t)GT * 64;
+    const int64_t t0 = (int64_t)ct * 64 + (tid - (CW + 2) * 32);
+    for (int j = 0; j < m; ++j) {
+      const int64_t entry = ((int64_t)a.layer * a.E + __ldcg(&a.plan->miss_expert[j])) % a.pool_entries;
+      const uint4* src = reinterpret_cast<const uint4*>(a.host_pool + entry * a.expert_bytes);
+      uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(a.slots) +
+                                            (int64_t)__ldcg(&a.plan->miss_slot[j]) * a.expert_bytes);
+      int64_t c = t0;
+      for (; c + 3 * nthr < per; c += 4 * nthr) {
+        const uint4 v0 = src[c], v1 = src[c + nthr], v2 = src[c + 2 * nthr], v3 = src[c + 3 * nthr];
+        dst[c] = v0;
+        dst[c + nthr] = v1;
+        dst[c + 2 * nthr] = v2;
+        dst[c + 3 * nthr] = v3;
+      }
+      for (; c < per; c += nthr) dst[c] = src[c];
+    }
+    return;
+  }
   if (warp == CW + 1) {
     // ---------------- control: the call's plan, stamps and counters ---------
     // (every key resident: CTA 0 publishes them off the units' path)
@@ -930,12 +980,14 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
   uint32_t* const xfw = reinterpret_cast<uint32_t*>(xfrag);
   constexpr int kXPer = (NT * 8 * 256 + NCT - 1) / NCT;   // 16-byte chunks per thread (d <= 2048)
   uint4 xv[kXPer];
+  uint4 xn[AHEAD ? kXPer : 1];   // kAhead: the next call's tokens, for the router
 #pragma unroll
   for (int q = 0; q < kXPer; ++q) {
     const int i = tid + q * NCT;
     if (i < T * cpr) {
       const int n = i / cpr, c = i - n * cpr;
-      xv[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
+      if (CUR) xv[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)n * d + c * 8));
+      if (AHEAD && NEXT) xn[AHEAD ? q : 0] = __ldg(reinterpret_cast<const uint4*>(a.x_route + (size_t)n * d + c * 8));
     }
   }
   if (FUSED) {
@@ -947,8 +999,9 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
     s_calls = calls;
     s_clock = clk;
   }
-  auto put_x = [&](int n, int c, uint4 v) {
-    if (FUSED) *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) = v;
+  auto put_x = [&](int n, int c, uint4 v, uint4 vr) {
+    if (FUSED && NEXT) *reinterpret_cast<uint4*>(xraw + (size_t)n * xs + c * 8) = AHEAD ? vr : v;
+    if (!CUR) return;
     uint32_t* w = xfw + ((((size_t)(n >> 3) * nks + (c >> 1)) * 32 + (n & 7) * 4) << 1) + (c & 1);
     w[0] = pack_half2_from_bf16(v.x);
     w[2] = pack_half2_from_bf16(v.y);
@@ -960,7 +1013,7 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
     const int i = tid + q * NCT;
     if (i < T * cpr) {
       const int n = i / cpr, c = i - n * cpr;
-      put_x(n, c, xv[q]);
+      put_x(n, c, xv[q], xn[AHEAD ? q : 0]);
     }
   }
   // zero fragments of the token slots T .. NT*8-1: 32 contiguous bytes per
@@ -986,7 +1039,7 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
     for (int i = tid; i < a.set_words; i += NCT) other[i] = 0;
   }
 
-  if (FUSED) {
+  if (FUSED && NEXT) {
     // ---- router rows e = cta + G*j, one warp per row -----------------------
     for (int j = warp;; j += CW) {
       const int e = cta + G * j;
@@ -1047,7 +1100,11 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
       if (routed) break;
       routed = true;
       // ================= the routing result ===============================
-      if (FUSED) {
+      if (AHEAD && cta == 0 && !NEXT) {   // no next call to route (the call count moves on after the launch)
+        MOE_TL_FLUSH(cta);
+        return;
+      }
+      if (FUSED && !(AHEAD && cta != 0)) {
         if (tid == 0) {
           s_cab = s_abort;
           MOE_TLS(6);
@@ -1091,14 +1148,18 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
         named_bar(1, NCT);
         if (MODE == kFusedResident && cta == 0) named_bar_arrive(2, NCT + 32);
       } else {
-        const Plan* P = a.plan;   // the routing plan is complete and visible
-        for (int i = tid; i < kMaxPicks; i += NCT) s_act_slot[i] = P->act_slot[i];
-        for (int i = tid; i < T * K; i += NCT) {
-          s_pick_act[i] = P->pick_act[i];
-          s_w[i] = P->w[i];
+        // the routing plan is complete and visible (kAhead: the current
+        // call's, written by the previous launch; all its experts resident)
+        const Plan* P = AHEAD ? a.cur_plan : a.plan;
+        if (CUR) {
+          for (int i = tid; i < kMaxPicks; i += NCT) s_act_slot[i] = P->act_slot[i];
+          for (int i = tid; i < T * K; i += NCT) {
+            s_pick_act[i] = P->pick_act[i];
+            s_w[i] = P->w[i];
+          }
         }
         if (tid == 0) {
-          s_n_act = P->n_act;
+          s_n_act = CUR ? P->n_act : 0;
           s_cab = s_abort;
         }
         named_bar(1, NCT);
@@ -1309,6 +1370,10 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
     ++u;
   }
   MOE_TL0(9);
+  if (!CUR) {   // a launch that only routes the next call: no output
+    MOE_TL_FLUSH(cta);
+    return;
+  }
 
   // ---- this CTA's partial of y -> ypart[ct][t][row], (call tag, value)
   // words that the combining CTAs poll: no counter and no fence
@@ -1388,6 +1453,16 @@ extern "C" int moe_debug_timeline_ffn(unsigned long long* out) {
 }
 #endif
 
+// After a kAhead launch without a next call (no cache step ran in it) the
+// call count moves on in a launch of its own, ordered after it on the
+// stream, so that no CTA of that launch can read two different counts.
+__global__ void calls_bump_kernel(uint32_t* counters) { *counters += 1u; }
+
+cudaError_t launch_calls_bump(uint32_t* counters, cudaStream_t s) {
+  calls_bump_kernel<<<1, 1, 0, s>>>(counters);
+  return cudaGetLastError();
+}
+
 template <int NT, int MODE>
 static cudaError_t launch_nt(const FfnArgs& a, cudaStream_t s, bool pdl, int grid) {
   constexpr int NCT = DCfg<NT>::CW * 32;
@@ -1413,10 +1488,12 @@ cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl) {
   if (a.grid <= 0 || (a.cached && (!a.fused || a.grid < 2))) return cudaErrorInvalidValue;
   if (a.T <= 8) {
     if (!a.fused) return launch_nt<1, kPlanRead>(a, s, pdl, a.grid);
+    if (a.ahead) return launch_nt<1, kAhead>(a, s, pdl, a.grid);
     if (!a.cached) return launch_nt<1, kFusedResident>(a, s, pdl, a.grid);
     return a.direct ? launch_nt<1, kFusedCachedDirect>(a, s, pdl, a.grid) : launch_nt<1, kFusedCached>(a, s, pdl, a.grid);
   }
   if (!a.fused) return launch_nt<2, kPlanRead>(a, s, pdl, a.grid);
+  if (a.ahead) return launch_nt<2, kAhead>(a, s, pdl, a.grid);
   if (!a.cached) return launch_nt<2, kFusedResident>(a, s, pdl, a.grid);
   return a.direct ? launch_nt<2, kFusedCachedDirect>(a, s, pdl, a.grid) : launch_nt<2, kFusedCached>(a, s, pdl, a.grid);
 }
@@ -1439,10 +1516,12 @@ cudaError_t decode_ffn_fits(int d, bool* fits) {
   MOE_FIT(1, kFusedResident)
   MOE_FIT(1, kFusedCached)
   MOE_FIT(1, kFusedCachedDirect)
+  MOE_FIT(1, kAhead)
   MOE_FIT(2, kPlanRead)
   MOE_FIT(2, kFusedResident)
   MOE_FIT(2, kFusedCached)
   MOE_FIT(2, kFusedCachedDirect)
+  MOE_FIT(2, kAhead)
 #undef MOE_FIT
   return cudaSuccess;
 }

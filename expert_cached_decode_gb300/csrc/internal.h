@@ -141,6 +141,12 @@ struct FfnArgs {
   int C;
   const uint8_t* host_pool;     // device address of the registered host pool
   int direct;                   // the host pool holds the device block layout (kFusedCachedDirect)
+  // kAhead: the routing fields above (layer, wr, bias, table row, plan,
+  // stats) describe the next call; these the current one
+  int ahead;
+  int has_cur, has_next;        // a current call to compute / a next call to route
+  const Plan* cur_plan;         // the current call's plan (written by the previous launch)
+  const uint16_t* x_route;      // [T][d] bf16 tokens of the next call
   int64_t pool_entries;         // key (layer, e) reads entry (layer*E + e) mod pool_entries
   uint8_t* staging;             // [staging_n][expert_bytes] canonical copies of this call's misses
   int staging_n;
@@ -154,7 +160,11 @@ constexpr int kDecodeSetWords = 3 + kMaxPicks;
 // kFusedCachedDirect: as kFusedCached with the host pool in the device block
 // layout: a missing expert's stages come straight from the host pool into
 // the units (and into its victim slot), with no fetch ahead of them.
-enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2, kFusedCachedDirect = 3 };
+// kAhead: the current call's experts come from a plan prepared by the
+// previous launch (all resident), while this launch routes the next call
+// (router rows, selection, cache step in CTA 0) and copies its misses from a
+// device-layout host pool into their victim slots.
+enum FfnMode : int { kPlanRead = 0, kFusedResident = 1, kFusedCached = 2, kFusedCachedDirect = 3, kAhead = 4 };
 
 struct RouterGemmArgs {
   const float* bias;   // [E]
@@ -287,5 +297,6 @@ cudaError_t launch_prefill_fetch(const MissFetch& f, const int32_t* n_miss, bool
 cudaError_t launch_decode_ffn(const FfnArgs& a, cudaStream_t s, bool pdl);
 // whether one CTA of every decode-kernel variant fits on an SM at hidden size d
 cudaError_t decode_ffn_fits(int d, bool* fits);
+cudaError_t launch_calls_bump(uint32_t* counters, cudaStream_t s);
 
 }  // namespace moe

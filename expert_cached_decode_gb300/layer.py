@@ -77,18 +77,27 @@ class MoELayer:
     def moe_forward(self, layer, x, y, stream=None, trace=False):
         """y[T, d] (fp32, device) <- layer-call on x[T, d] (bf16, device).
         With trace=True returns a dict of host arrays (synchronises)."""
-        T = x.shape[0]
+        call = lambda tr: self._lib.moe_forward(self.ctx, layer, _ptr(x), x.shape[0], _ptr(y), _stream(stream), tr)
+        return self._run(call, x.shape[0], trace, "moe_forward")
+
+    def moe_forward_ahead(self, layer, x, y, next_layer=0, next_x=None, stream=None, trace=False):
+        """moe_forward of (layer, x) that also routes the layer-call
+        (next_layer, next_x), runs its cache step and copies its misses;
+        that call must be the next forward on this layer (same x tensor)."""
+        call = lambda tr: self._lib.moe_forward_ahead(self.ctx, layer, _ptr(x), x.shape[0], _ptr(y), _stream(stream),
+                                                      tr, int(next_layer), _ptr(next_x))
+        return self._run(call, x.shape[0], trace, "moe_forward_ahead")
+
+    def _run(self, call, T, trace, where):
         if not trace:
-            check(self._lib.moe_forward(self.ctx, layer, _ptr(x), T, _ptr(y), _stream(stream), None),
-                  "moe_forward")
+            check(call(None), where)
             return None
         n = T * self.k
         bufs = {"idx": np.zeros(n, np.int32), "w": np.zeros(n, np.float32), "slot": np.zeros(n, np.int32),
                 "miss_expert": np.zeros(n, np.int32), "miss_slot": np.zeros(n, np.int32),
                 "evicted_key": np.zeros(n, np.int32)}
         tr = MoeTrace(**{k: _ptr(v) for k, v in bufs.items()})
-        check(self._lib.moe_forward(self.ctx, layer, _ptr(x), T, _ptr(y), _stream(stream), ctypes.byref(tr)),
-              "moe_forward")
+        check(call(ctypes.byref(tr)), where)
         m = tr.n_miss
         return {"idx": bufs["idx"].reshape(T, self.k), "w": bufs["w"].reshape(T, self.k),
                 "slot": bufs["slot"].reshape(T, self.k), "miss_expert": bufs["miss_expert"][:m].copy(),

@@ -183,6 +183,28 @@ moe_status moe_forward(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t 
 typedef enum { MOE_MISS_HOST_COPY = 0, MOE_MISS_DEVICE_PULL = 1 } moe_miss_mode;
 moe_status moe_set_miss_mode(moe_ctx* ctx, int32_t mode);
 
+/* moe_forward for decode calls (T <= 16) with cross-layer lookahead, for a
+ * stream of layer-calls whose inputs are known ahead (as the layers of the
+ * stack workload, which take independent tokens): besides the layer-call
+ * (layer, x), the launch routes the layer-call (next_layer, next_x, same T),
+ * runs its cache step and copies its misses into their victim slots, all
+ * while the experts of (layer, x) compute.  That next call's experts then
+ * run in the following moe_forward_ahead or moe_forward on this context,
+ * which must name the same layer, the same x pointer (contents unchanged)
+ * and T; until it does, every other call that touches the cache returns
+ * MOE_ERR_STATE.  next_x == NULL: no next call.  The first call of a
+ * sequence also prepares itself (one more launch).  Cache steps run in call
+ * order, so hits, misses, victims, counters and the LRU state are exactly
+ * those of the same calls made with moe_forward; the trace describes (layer,
+ * x).  Needs the GPU miss path (MOE_MISS_DEVICE_PULL), a host pool in the
+ * device layout (MOE_POOL_DEVICE) and a capacity of at least 32 * top_k
+ * slots (two layer-calls' experts, so that no victim of the next call is an
+ * expert this call still reads); else MOE_ERR_UNIMPLEMENTED.  Cross-layer
+ * prefetch of the scope table's NEXT-1 (no counterpart on the pages, whose
+ * layer inputs depend on the previous layer). */
+moe_status moe_forward_ahead(moe_ctx* ctx, int32_t layer, const void* x_bf16, int32_t T, float* y,
+                             void* stream, moe_trace* trace, int32_t next_layer, const void* next_x_bf16);
+
 /* Test hook: make the nth (>= 1) future event of `kind` fail once, then
  * disarm; kind 0 disarms.  Process-wide, not thread-safe.  Errors:
  * INVALID_ARG for an unknown kind or nth < 1.

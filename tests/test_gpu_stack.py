@@ -31,9 +31,11 @@ POOL_ENTRIES = 2048
 
 
 def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls=None, miss_mode=None,
-              prefill=None, pool_layout=0):
+              prefill=None, pool_layout=0, ahead=False):
     """Every layer-call of `passes` passes over the stack, compared with the
-    oracle (pool_layout 1: the host pool in the device block layout) ...
+    oracle (pool_layout 1: the host pool in the device block layout; ahead:
+    every layer-call made with moe_forward_ahead naming the next one of the
+    sequence, so its routing, cache step and misses run one launch early) ...
     then, with prefill=(layer, T), one prefill chunk of T tokens at that
     layer on the warm cache: its cache step (slots, misses, victims, evicted
     keys, counts) bit-exact against the oracle's and every output within
@@ -58,28 +60,32 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
     y = torch.empty((T, wl.d), dtype=torch.float32, device="cuda")
     memo = ExpertMemo(s, pool_entries)
     meas = {"hits": 0, "picks": 0}
-    for p in range(passes):
-        for b in range(calls):
-            call = p * calls + b
-            for l in range(L):
-                tr = layer.moe_forward(l, xdev[l, b], y, trace=True)
-                oi, ow, res = so.layer_call(call, b, l)
-                assert np.array_equal(tr["idx"], oi), (p, b, l)
-                assert np.abs(tr["w"] - ow).max() <= W_TOL
-                keys = so.key(l, oi)
-                want_slot = res.slots[np.searchsorted(res.keys, keys)]
-                assert np.array_equal(tr["slot"], want_slot), (p, b, l)
-                assert np.array_equal(tr["miss_expert"], res.miss_keys - l * wl.n_experts), (p, b, l)
-                assert np.array_equal(tr["miss_slot"], res.miss_slots), (p, b, l)
-                assert np.array_equal(tr["evicted_key"], res.evicted), (p, b, l)
-                assert tr["token_hits"] == res.token_hits and tr["token_misses"] == res.token_misses
-                assert tr["n_distinct"] == res.keys.size
-                if p == passes - 1:
-                    meas["hits"] += res.token_hits
-                    meas["picks"] += res.token_hits + res.token_misses
-                    if (b, l) in ffn_sample:
-                        want = oracle_y(memo, l, xs[l, b], oi, ow)
-                        assert_close_rms(y.cpu().numpy(), want, what=f"y call {b} layer {l}")
+    seq = [(p, b, l) for p in range(passes) for b in range(calls) for l in range(L)]
+    for i, (p, b, l) in enumerate(seq):
+        call = p * calls + b
+        if ahead:
+            nxt = seq[i + 1] if i + 1 < len(seq) else None
+            tr = layer.moe_forward_ahead(l, xdev[l, b], y, next_layer=nxt[2] if nxt else 0,
+                                         next_x=xdev[nxt[2], nxt[1]] if nxt else None, trace=True)
+        else:
+            tr = layer.moe_forward(l, xdev[l, b], y, trace=True)
+        oi, ow, res = so.layer_call(call, b, l)
+        assert np.array_equal(tr["idx"], oi), (p, b, l)
+        assert np.abs(tr["w"] - ow).max() <= W_TOL
+        keys = so.key(l, oi)
+        want_slot = res.slots[np.searchsorted(res.keys, keys)]
+        assert np.array_equal(tr["slot"], want_slot), (p, b, l)
+        assert np.array_equal(tr["miss_expert"], res.miss_keys - l * wl.n_experts), (p, b, l)
+        assert np.array_equal(tr["miss_slot"], res.miss_slots), (p, b, l)
+        assert np.array_equal(tr["evicted_key"], res.evicted), (p, b, l)
+        assert tr["token_hits"] == res.token_hits and tr["token_misses"] == res.token_misses
+        assert tr["n_distinct"] == res.keys.size
+        if p == passes - 1:
+            meas["hits"] += res.token_hits
+            meas["picks"] += res.token_hits + res.token_misses
+            if (b, l) in ffn_sample:
+                want = oracle_y(memo, l, xs[l, b], oi, ow)
+                assert_close_rms(y.cpu().numpy(), want, what=f"y call {b} layer {l}")
     if prefill is not None:
         from moe_inputs import bf16_bits_to_f64
         from oracle.routing import route
@@ -114,21 +120,25 @@ def run_stack(cfg_id, passes, pool_entries, overrides=None, ffn_sample=(), calls
     return meas["hits"] / meas["picks"], tot, st
 
 
-@pytest.mark.parametrize("pool_layout", [0, 1])
+@pytest.mark.parametrize("pool_layout,ahead", [(0, False), (1, False), (1, True)])
 @pytest.mark.parametrize("miss_mode,tokens", [(MOE_MISS_DEVICE_PULL, 5), (MOE_MISS_HOST_COPY, 5),
                                              (MOE_MISS_DEVICE_PULL, 1), (MOE_MISS_DEVICE_PULL, 12)])
-def test_small_stack_with_evictions(miss_mode, tokens, pool_layout):
+def test_small_stack_with_evictions(miss_mode, tokens, pool_layout, ahead):
     # both ways of fetching misses: the GPU reading the host pool, or host-issued copies;
     # one-token calls take the selection's single-token path, 12-token calls the second
     # n-tile; pool_layout 1 keeps the host pool in the device block layout (a missing
     # expert computed straight from the host pool while it is written to its slot)
+    if ahead and miss_mode != MOE_MISS_DEVICE_PULL:
+        pytest.skip("lookahead runs on the GPU miss path only")
     over = dict(d=256, f=128, n_experts=32, top_k=4, n_layers=6, tokens=tokens, capacity=40, calls=60)
     if tokens > 8:
         over["capacity"] = 64
+    if ahead:   # lookahead needs room for two layer-calls' experts (32 * top_k); more keys keep it evicting
+        over.update(capacity=128, n_layers=12)
     rate, tot, _ = run_stack(3, passes=2, pool_entries=96, overrides=over,
                              ffn_sample={(0, 0), (17, 3), (59, 5)}, miss_mode=miss_mode,
                              prefill=(2, 300) if miss_mode == MOE_MISS_DEVICE_PULL else None,
-                             pool_layout=pool_layout)
+                             pool_layout=pool_layout, ahead=ahead)
     assert tot["evictions"] > 0 and tot["token_misses"] > 0
     assert 0.0 < rate < 1.0
 
