@@ -326,7 +326,7 @@ def measure_h2d_gbs(chunk=EXPERT_BYTES, total=1 << 30, reps=5):
     return float(np.median(out))
 
 
-def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, ahead=False):
+def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, aheads=(False,)):
     """48-layer stack with the 8,445-slot cache that starts empty (miss path):
     the warm-up passes over the call stream, then the measured pass.
     miss_mode 1: the GPU reads missing experts from the host pool itself;
@@ -334,7 +334,9 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, ahead
     pool_layout 1: the host pool holds the device block layout (converted
     once at setup), so a missing expert is computed straight from it while
     it is written to its slot; 0: canonical, fetched and re-laid out first.
-    ahead: every layer-call made with moe_forward_ahead naming the next
+    aheads: one result per entry, on the same layer and host pool (the cache
+    reconfigured, so it starts empty each time).  ahead True: every
+    layer-call made with moe_forward_ahead naming the next
     layer-call of its pass (cross-layer lookahead; the stack's layers take
     independent tokens), so its routing, cache step and misses run one
     launch early; the first call of a pass prepares itself."""
@@ -357,36 +359,39 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, ahead
     layer = MoELayer(wl.d, wl.f, wl.n_experts, wl.top_k, wl.n_layers, wr, b, shared, pool,
                      host_pool_entries=0 if P == wl.keys else P, host_pool_layout=pool_layout)
     layer.moe_set_miss_mode(miss_mode)
-    layer.moe_cache_configure(wl.capacity)
     setup_s = time.time() - t0
     xdev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda()
     y = torch.empty((wl.tokens, wl.d), dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     steps = [(c, l) for c in range(calls) for l in range(wl.n_layers)]
+    runs = []
 
-    def one_pass():
-        for i, (c, l) in enumerate(steps):
-            if ahead:
-                nc, nl = steps[i + 1] if i + 1 < len(steps) else (0, 0)
-                layer.moe_forward_ahead(l, xdev[l, c], y, next_layer=nl,
-                                        next_x=xdev[nl, nc] if i + 1 < len(steps) else None)
-            else:
-                layer.moe_forward(l, xdev[l, c], y)
+    for ahead in aheads:
+        layer.moe_cache_configure(wl.capacity)
+        def one_pass():
+            for i, (c, l) in enumerate(steps):
+                if ahead:
+                    nc, nl = steps[i + 1] if i + 1 < len(steps) else (0, 0)
+                    layer.moe_forward_ahead(l, xdev[l, c], y, next_layer=nl,
+                                            next_x=xdev[nl, nc] if i + 1 < len(steps) else None)
+                else:
+                    layer.moe_forward(l, xdev[l, c], y)
 
-    with torch.cuda.stream(stream):
-        for _ in range(wl.warm_passes):
+        with torch.cuda.stream(stream):
+            for _ in range(wl.warm_passes):
+                one_pass()
+        stream.synchronize()
+        before = layer.moe_cache_stats()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
             one_pass()
-    stream.synchronize()
-    before = layer.moe_cache_stats()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        one_pass()
-    e1.record(stream)
-    stream.synchronize()
-    ms = e0.elapsed_time(e1)
-    after = layer.moe_cache_stats()
-    dlt = {k: after[k] - before[k] for k in after}
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        after = layer.moe_cache_stats()
+        dlt = {k: after[k] - before[k] for k in after}
+        runs.append((ahead, ms, dlt))
     layer.close()
     del pool
     shm.close()
@@ -394,33 +399,36 @@ def run_stack(cfg_id, pool_entries=0, calls=0, miss_mode=1, pool_layout=1, ahead
     h2d = measure_h2d_gbs()
     hbm, _ = peaks()
     B = expert_nbytes(wl.d, wl.f)
-    distinct_bytes = (dlt["distinct_hits"] + dlt["distinct_misses"] + dlt["layer_calls"]) * B  # + shared
-    t_bound = max(distinct_bytes / (hbm * 1e9), dlt["miss_bytes"] / (h2d * 1e9))
-    tokens = calls * wl.tokens
-    return {"workload": f"{wl.name}: 48 layers, T={wl.tokens} per call, Zipf s={wl.zipf_s} (lambda "
-                        f"{BIAS_LAMBDA}), {wl.capacity} slots starting empty, {wl.warm_passes} warm-up passes "
-                        f"then the measured pass of {calls} calls",
-            "miss_copies": ("host-issued cudaMemcpyAsync" if miss_mode == 0 else
-                            "GPU computes each missing expert straight from the host pool (device block layout) "
-                            "and writes it to its victim slot" if pool_layout == 1 else
-                            "GPU fetches each missing expert from the host pool (canonical) into its slot, then "
-                            "computes"),
-            "host_pool_layout": "device block layout" if pool_layout == 1 else "canonical",
-            "lookahead": ("each layer-call routes the next one and copies its misses (moe_forward_ahead)"
-                          if ahead else "none"),
-            "host_pool_entries": P,
-            "host_pool_note": "expert (l, e) is read from entry (512 l + e) mod P; copy sizes, counts and "
-                              "the cache's behaviour do not depend on P",
-            "tokens_per_s": tokens / (ms / 1e3), "ms_measured_pass": ms,
-            "token_hit_rate": dlt["token_hits"] / max(1, dlt["token_hits"] + dlt["token_misses"]),
-            "distinct_expert_bytes": distinct_bytes, "miss_bytes": dlt["miss_bytes"],
-            "h2d_gbs_measured": h2d, "hbm_gbs": hbm,
-            "roofline": {"bound_ms": 1e3 * t_bound, "frac": 1e3 * t_bound / ms,
-                         "note": "max(distinct-expert bytes / HBM, miss bytes / measured H2D)",
-                         "serialised_bound_ms": 1e3 * (distinct_bytes / (hbm * 1e9) + dlt["miss_bytes"] / (h2d * 1e9)),
-                         "serialised_note": "distinct-expert bytes / HBM + miss bytes / H2D: copies and expert "
-                                            "reads never overlapping"},
-            "setup_s": setup_s}
+    out = []
+    for ahead, ms, dlt in runs:
+        distinct_bytes = (dlt["distinct_hits"] + dlt["distinct_misses"] + dlt["layer_calls"]) * B  # + shared
+        t_bound = max(distinct_bytes / (hbm * 1e9), dlt["miss_bytes"] / (h2d * 1e9))
+        tokens = calls * wl.tokens
+        out.append({"workload": f"{wl.name}: 48 layers, T={wl.tokens} per call, Zipf s={wl.zipf_s} (lambda "
+                            f"{BIAS_LAMBDA}), {wl.capacity} slots starting empty, {wl.warm_passes} warm-up passes "
+                            f"then the measured pass of {calls} calls",
+                "miss_copies": ("host-issued cudaMemcpyAsync" if miss_mode == 0 else
+                                "GPU computes each missing expert straight from the host pool (device block layout) "
+                                "and writes it to its victim slot" if pool_layout == 1 else
+                                "GPU fetches each missing expert from the host pool (canonical) into its slot, then "
+                                "computes"),
+                "host_pool_layout": "device block layout" if pool_layout == 1 else "canonical",
+                "lookahead": ("each layer-call routes the next one and copies its misses (moe_forward_ahead)"
+                              if ahead else "none"),
+                "host_pool_entries": P,
+                "host_pool_note": "expert (l, e) is read from entry (512 l + e) mod P; copy sizes, counts and "
+                                  "the cache's behaviour do not depend on P",
+                "tokens_per_s": tokens / (ms / 1e3), "ms_measured_pass": ms,
+                "token_hit_rate": dlt["token_hits"] / max(1, dlt["token_hits"] + dlt["token_misses"]),
+                "distinct_expert_bytes": distinct_bytes, "miss_bytes": dlt["miss_bytes"],
+                "h2d_gbs_measured": h2d, "hbm_gbs": hbm,
+                "roofline": {"bound_ms": 1e3 * t_bound, "frac": 1e3 * t_bound / ms,
+                             "note": "max(distinct-expert bytes / HBM, miss bytes / measured H2D)",
+                             "serialised_bound_ms": 1e3 * (distinct_bytes / (hbm * 1e9) + dlt["miss_bytes"] / (h2d * 1e9)),
+                             "serialised_note": "distinct-expert bytes / HBM + miss bytes / H2D: copies and expert "
+                                                "reads never overlapping"},
+                "setup_s": setup_s})
+    return out
 
 
 def run_stack_sweep(pool_entries=2048, calls=500, tokens=(1, 4, 7), capacities=(9057, 8445, 6144)):
@@ -693,9 +701,10 @@ def run_gpu(args):
             try:
                 cfgs = (3, 4) if args.stack_config == 0 else (args.stack_config,)
                 modes = (1, 0) if args.stack_mode < 0 else (args.stack_mode,)
-                line["stack"] = [run_stack(c, args.stack_pool, miss_mode=m, pool_layout=args.stack_pool_layout,
-                                           ahead=a) for c in cfgs for m in modes
-                                 for a in ((False, True) if m == 1 and args.stack_pool_layout == 1 else (False,))]
+                line["stack"] = [r for c in cfgs for m in modes
+                                 for r in run_stack(c, args.stack_pool, miss_mode=m, pool_layout=args.stack_pool_layout,
+                                                    aheads=(False, True) if m == 1 and args.stack_pool_layout == 1
+                                                    else (False,))]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:
