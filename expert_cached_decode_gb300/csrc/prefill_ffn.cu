@@ -225,17 +225,12 @@ constexpr int CLUSTER = 2;             // CTAs sharing each token tile (TMA mult
 constexpr int B_HALF = B_BYTES / CLUSTER;   // token rows a CTA loads for both
 }  // namespace pg
 
-// Expand one 32x32 block (448 B at `bp`, shared memory) into 32 rows and 32
-// k columns of a 128-byte-swizzled K-major fp16 tile, as RN(q * scale).
-// The expanded registers are in mma A-fragment order, which is the order
-// stmatrix takes: register (mt, ks, rh, rl) holds, for lane (g, c), rows
-// mt*16 + 8rl + g and k pair 16ks + 8rh + 2c, so one m8n8.x4 store per
-// (mt, ks) writes four 8x8 sub-tiles; lane L gives the address of row L%8 of
-// sub-tile L/8 (rl = (L/8)%2, rh = L/16).  `lane_base` = tile + (row offset
-// of the block + 8*((L/8)%2) + L%8) * 128; sw = (L%8) << 4 (the swizzle of
-// that row); KC = the first 16-byte chunk of the block's k columns (0 or 4).
-template <int KC>
-__device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lane, uint32_t lane_base, uint32_t sw) {
+// One 32x32 block (448 B at `bp`, shared memory) expanded to RN(q * scale)
+// fp16 pairs in mma A-fragment order: register (mt, ks, rh, rl) holds, for
+// lane (g, c), rows mt*16 + 8rl + g and k pair 16ks + 8rh + 2c.  The
+// multiplies are volatile so that the whole expansion stays where it is
+// written: producers expand before they wait for a free tile stage.
+__device__ __forceinline__ void expand_block(const uint8_t* bp, int lane, uint32_t (&v)[16]) {
   const uint32_t* wp = reinterpret_cast<const uint32_t*>(bp);
   const uint32_t w0 = wp[lane], w1 = wp[32 + lane], w2 = wp[64 + lane];
   const uint2 sc = *reinterpret_cast<const uint2*>(bp + kBlockCodeBytes + (lane >> 2) * 8);
@@ -244,18 +239,29 @@ __device__ __forceinline__ void dequant_block_to_tile(const uint8_t* bp, int lan
                           __byte_perm(sc.y, 0, 0x3232)};
   uint32_t A[16];
   dequant_block(w0, w1, w2, A);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    asm volatile("mul.rn.f16x2 %0, %1, %2;" : "=r"(v[i]) : "r"(A[i]), "r"(s2[2 * (i >> 3) + (i & 1)]));
+}
+
+// An expanded block written as 32 rows and 32 k columns of a
+// 128-byte-swizzled K-major fp16 tile.  The A-fragment order is the order
+// stmatrix takes, so one m8n8.x4 store per (mt, ks) writes four 8x8
+// sub-tiles; lane L gives the address of row L%8 of sub-tile L/8
+// (rl = (L/8)%2, rh = L/16).  `lane_base` = tile + (row offset of the block
+// + 8*((L/8)%2) + L%8) * 128; sw = (L%8) << 4 (the swizzle of that row);
+// KC = the first 16-byte chunk of the block's k columns (0 or 4).
+template <int KC>
+__device__ __forceinline__ void store_block_tile(const uint32_t (&v)[16], int lane, uint32_t lane_base, uint32_t sw) {
   const uint32_t rh = (uint32_t)(lane >> 4);
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-      uint32_t v[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v[r]) : "r"(A[mt * 8 + ks * 4 + r]), "r"(s2[2 * mt + (r & 1)]));
+      const int r0 = mt * 8 + ks * 4;
       const uint32_t addr = lane_base + (uint32_t)(mt * 2048) + ((((uint32_t)(KC + 2 * ks) + rh) << 4) ^ sw);
-      asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]),
-                   "r"(v[1]), "r"(v[2]), "r"(v[3])
+      asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[r0]),
+                   "r"(v[r0 + 1]), "r"(v[r0 + 2]), "r"(v[r0 + 3])
                    : "memory");
     }
   }
@@ -512,6 +518,16 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
           }
           PF_ACC(pf_p6);
         }
+        // both blocks expanded into registers first: once the tile stage is
+        // free only the stores remain before the MMA can use it
+        uint32_t v0[16], v1[16];
+        {
+          PF_T0();
+          const uint8_t* src = my_stage + ps * PCHUNK;
+          expand_block(src, lane, v0);
+          expand_block(src + kBlockBytes, lane, v1);
+          PF_ACC(pf_p8);
+        }
         const uint32_t it = lt * n_kb + kb;
         const int s = it % STAGES;
         const uint32_t use = it / STAGES;
@@ -526,21 +542,20 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
         PF_T0();
         __syncwarp();   // after lane 0's issue and the waits: stmatrix runs on the whole warp
         const uint32_t tile_lane = smem_u32(stages + s * STAGE_BYTES) + lane_off;
-        const uint8_t* src = my_stage + ps * PCHUNK;
         if (DOWN) {
           if (p & 1) {
-            dequant_block_to_tile<4>(src, lane, tile_lane, gx);
-            dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane + 32 * 128, gx);
+            store_block_tile<4>(v0, lane, tile_lane, gx);
+            store_block_tile<4>(v1, lane, tile_lane + 32 * 128, gx);
           } else {
-            dequant_block_to_tile<0>(src, lane, tile_lane, gx);
-            dequant_block_to_tile<0>(src + kBlockBytes, lane, tile_lane + 32 * 128, gx);
+            store_block_tile<0>(v0, lane, tile_lane, gx);
+            store_block_tile<0>(v1, lane, tile_lane + 32 * 128, gx);
           }
         } else if (!hi_group) {
-          dequant_block_to_tile<0>(src, lane, tile_lane, gx);                                // Wg
-          dequant_block_to_tile<0>(src + kBlockBytes, lane, tile_lane + GU_ROWS * 128, gx);  // Wu
+          store_block_tile<0>(v0, lane, tile_lane, gx);                 // Wg
+          store_block_tile<0>(v1, lane, tile_lane + GU_ROWS * 128, gx);  // Wu
         } else {
-          dequant_block_to_tile<4>(src, lane, tile_lane, gx);
-          dequant_block_to_tile<4>(src + kBlockBytes, lane, tile_lane + GU_ROWS * 128, gx);
+          store_block_tile<4>(v0, lane, tile_lane, gx);
+          store_block_tile<4>(v1, lane, tile_lane + GU_ROWS * 128, gx);
         }
         fence_proxy_async_smem();
         __syncwarp();
