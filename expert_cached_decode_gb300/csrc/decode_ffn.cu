@@ -1104,6 +1104,7 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
         MOE_TL_FLUSH(cta);
         return;
       }
+      bool planned = false;   // warp 0: the producer already has its units
       if (FUSED && !(AHEAD && cta != 0)) {
         if (tid == 0) {
           s_cab = s_abort;
@@ -1122,19 +1123,50 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
           }
           MOE_TL0(16);
           const int n_act = sel->n_act;
+          if (MODE == kFusedResident && warp == 0) {
+            // every expert resident: the producer needs only U's slots and
+            // this CTA's unit range, so warp 0 hands them over at once; the
+            // routing weights and the rest of the bookkeeping follow while
+            // the first copies are in flight.  (A selection that timed out
+            // still yields valid ids: the units run, the call reports the
+            // error.)
+            for (int i = lane; i < n_act; i += 32) {
+              int slot = s_tab[sel->act[i]];
+              if (slot < 0) {
+                set_error(a.err, DEV_NOT_RESIDENT);
+                slot = 0;
+              }
+              s_act_slot[i] = slot;
+              s_act_expert[i] = sel->act[i];
+              s_order[i] = i;
+              s_mrank[i] = -1;
+            }
+            __syncwarp();
+            if (lane == 0) {
+              const int NU = n_act * RG;
+              s_u0 = routed_first(ct, NU, RG, GT);
+              s_u1 = routed_first(ct + 1, NU, RG, GT);
+              mbar_arrive(plan_ready);
+              MOE_TLS(8);
+            }
+            __syncwarp();
+            planned = true;
+          }
           for (int i = tid; i < T * K; i += NCT) {
             const int id = sel->sel_id[i / K][i % K];
             s_pick_act[i] = dsel_act_index(sel, id);
             s_w[i] = sel->sel_w[i / K][i % K];
           }
-          for (int i = tid; i < n_act; i += NCT) {
-            int slot = s_tab[sel->act[i]];
-            if (slot < 0 && !CACHED) {
-              set_error(a.err, DEV_NOT_RESIDENT);
-              slot = 0;
+          if (MODE != kFusedResident) {
+            for (int i = tid; i < n_act; i += NCT) {
+              int slot = s_tab[sel->act[i]];
+              if (slot < 0 && !CACHED) {
+                set_error(a.err, DEV_NOT_RESIDENT);
+                slot = 0;
+              }
+              s_act_slot[i] = slot;   // cached: -1 marks a miss until CTA 0 assigns its victim
+              s_act_expert[i] = sel->act[i];
             }
-            s_act_slot[i] = slot;   // cached: -1 marks a miss until CTA 0 assigns its victim
-            s_act_expert[i] = sel->act[i];
           }
           if (tid == 0) s_n_act = n_act;
         } else if (tid == 0) {
@@ -1168,7 +1200,7 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
       const int n_act = s_n_act;
       // unit order: resident experts first, then the misses (ascending id
       // within each), and each miss's position in the miss list
-      if (warp == 0) {
+      if (warp == 0 && !planned) {
         int nh = 0, nm = 0;
         for (int i0 = 0; i0 < n_act; i0 += 32) {
           const int i = i0 + lane;
@@ -1201,7 +1233,7 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
       }
       // this CTA's routed units, handed to the producer (it streams the
       // resident experts' units at once and waits per missing expert)
-      if (tid == 0) {
+      if (tid == 0 && !planned) {
         const int NU = s_cab ? 0 : n_act * RG;
         s_u0 = routed_first(ct, NU, RG, GT);
         s_u1 = routed_first(ct + 1, NU, RG, GT);
