@@ -747,8 +747,20 @@ __global__ void __launch_bounds__(KCfg<NT, MODE>::THREADS, 1) decode_ffn_kernel(
     pdl_wait();   // slots (and their contents) may have been written by earlier work
     // slots of this call's misses were written by other CTAs' generic stores
     if (CACHED) asm volatile("fence.proxy.async.global;" ::: "memory");
-    if (ok && !mbar_wait(plan_ready, 0, lim)) ok = false;
-    if (ok) {
+    if (AHEAD) {
+      // the current call's plan was completed by the previous launch (visible
+      // once pdl_wait returned) with every expert resident and U's order as
+      // the unit order: the routed units stream at once, while the consumers
+      // still route the next call
+      const Plan* P = a.cur_plan;
+      const int NU = CUR ? __ldcg(&P->n_act) * RG : 0;
+      const int u0 = routed_first(ct, NU, RG, GT), u1 = routed_first(ct + 1, NU, RG, GT);
+      for (int u = u0; u < u1 && ok; ++u)
+        ok = issue_unit(a.slots + (int64_t)__ldcg(&P->act_slot[u / RG]) * a.expert_bytes, u % RG);
+    } else if (ok && !mbar_wait(plan_ready, 0, lim)) {
+      ok = false;
+    }
+    if (ok && !AHEAD) {
       MOE_TLS(4);
       const int u0 = s_u0, u1 = s_u1;
       const uint32_t jpm = (uint32_t)(2 * RG + RD);   // fetch jobs per missing expert
