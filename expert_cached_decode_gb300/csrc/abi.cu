@@ -123,7 +123,7 @@ struct moe_ctx {
   uint16_t* p_hg_lo = nullptr;   // [T*(k+1)][f] fp16 (lo part of h)
   int32_t* p_perm = nullptr;
   float* p_wsort = nullptr;
-  int32_t* p_inv = nullptr;      // [T*k] sorted row of each pick
+  int32_t* p_pick = nullptr;     // [T*k] pick of each routed sorted row
   int32_t* p_miss_expert = nullptr;   // [E] the chunk's misses (cache that can miss)
   int32_t* p_miss_slot = nullptr;
   int32_t* p_evicted = nullptr;
@@ -438,7 +438,7 @@ extern "C" void moe_layer_destroy(moe_ctx* c) {
   cudaFree(c->p_hg_lo);
   cudaFree(c->p_perm);
   cudaFree(c->p_wsort);
-  cudaFree(c->p_inv);
+  cudaFree(c->p_pick);
   cudaFree(c->p_miss_expert);
   cudaFree(c->p_miss_slot);
   cudaFree(c->p_evicted);
@@ -653,7 +653,7 @@ static moe_status ensure_prefill_ffn_scratch(moe_ctx* c) {
       {reinterpret_cast<void**>(&c->p_hg_lo), (size_t)rows * c->f * sizeof(uint16_t)},
       {reinterpret_cast<void**>(&c->p_perm), (size_t)rows * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_wsort), (size_t)rows * sizeof(float)},
-      {reinterpret_cast<void**>(&c->p_inv), (size_t)kMaxPrefillT * c->k * sizeof(int32_t)},
+      {reinterpret_cast<void**>(&c->p_pick), (size_t)kMaxPrefillT * c->k * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_miss_expert), (size_t)c->E * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_miss_slot), (size_t)c->E * sizeof(int32_t)},
       {reinterpret_cast<void**>(&c->p_evicted), (size_t)c->E * sizeof(int32_t)},
@@ -854,7 +854,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   sa.cursor = c->p_cursor;
   sa.perm = c->p_perm;
   sa.wsort = c->p_wsort;
-  sa.inv = c->p_inv;
+  sa.pick = c->p_pick;
   sa.T = T;
   sa.k = c->k;
   sa.shared_weight = c->shared_weight;
@@ -878,6 +878,7 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   ga.hg_lo = c->p_hg_lo;
   ga.perm = c->p_perm;
   ga.wsort = c->p_wsort;
+  ga.pick = c->p_pick;
   ga.y = y;
   ga.osort = c->p_osort;
   ga.E = c->E;
@@ -888,7 +889,6 @@ static moe_status prefill_forward(moe_ctx* c, int layer, const void* x, int T, f
   CUDA_TRY(launch_prefill_down(th, thl, ga, s, c->num_sms));
   PrefillCombineArgs cb{};
   cb.osort = c->p_osort;
-  cb.inv = c->p_inv;
   cb.y = y;
   cb.T = T;
   cb.k = c->k;

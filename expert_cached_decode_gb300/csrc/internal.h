@@ -233,7 +233,7 @@ struct PrefillScatterArgs {
   int32_t* cursor;
   int32_t* perm;           // [T*k + T] token of each sorted row
   float* wsort;            // [T*k + T] combine weight of each sorted row
-  int32_t* inv;            // [T*k] sorted row of pick t*k + i
+  int32_t* pick;           // [T*k] pick t*k + i of each routed sorted row
   int T, k;
   float shared_weight;
 };
@@ -250,15 +250,15 @@ struct PrefillGemmArgs {
   uint16_t* hg_lo;         // [rows][f] fp16 lo part of h
   const int32_t* perm;
   const float* wsort;
+  const int32_t* pick;     // [T*k] pick t*k + i of each routed sorted row
   float* y;                // [T][d]: the shared expert's weighted output (down GEMM)
-  float* osort;            // [T*k][d]: weighted output of each routed pick, by sorted row
+  float* osort;            // [T*k][d]: weighted output of pick t*k + i in row t*k + i
   int E, d, f;
   uint32_t* err;
 };
 
 struct PrefillCombineArgs {
-  const float* osort;      // [T*k][d]
-  const int32_t* inv;      // [T*k] sorted row of each pick
+  const float* osort;      // [T*k][d], row t*k + i: pick i of token t
   float* y;                // [T][d], holds the shared expert's part on entry
   int T, k, d;
 };

@@ -147,7 +147,7 @@ __global__ void prefill_scatter_kernel(PrefillScatterArgs a) {
     const int pos = atomicAdd(&a.cursor[e], 1);
     a.perm[pos] = i / a.k;
     a.wsort[pos] = a.w[i];
-    a.inv[i] = pos;
+    a.pick[pos] = i;
   } else if (i < picks + a.T) {
     const int t = i - picks;
     a.perm[picks + t] = t;
@@ -586,13 +586,16 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
       // down: the token and routing weight of every column this warp reads,
       // loaded before the accumulator is ready (lane j of chunk cc holds
       // column cc*32 + 16hf + j, j < 16)
+      // (routed tiles: the pick index instead of the token, the row of
+      // osort that the column's output goes to)
       int ctok[kPrefillBN / 32];
       float cw[kPrefillBN / 32];
       if (DOWN) {
+        const bool routed = tl.group < a.E;
 #pragma unroll
         for (int cc = 0; cc < kPrefillBN / 32; ++cc) {
           const int col = cc * 32 + hf * 16 + (lane & 15);
-          ctok[cc] = col < tl.nlen ? a.perm[tl.row0 + col] : 0;
+          ctok[cc] = col < tl.nlen ? (routed ? a.pick[tl.row0 + col] : a.perm[tl.row0 + col]) : 0;
           cw[cc] = col < tl.nlen ? a.wsort[tl.row0 + col] : 0.f;
         }
       }
@@ -666,16 +669,17 @@ __global__ void __launch_bounds__(pg::THREADS, 1)
               tokc = ctok[q];
               wc = cw[q];
             }
-          // routed expert: the weighted output of each pick goes to its own
-          // sorted row of osort (summed per token later, in a fixed order);
-          // the shared expert (every token once): straight into y
+          // routed expert: the weighted output of pick t*k + i goes to row
+          // t*k + i of osort (so a token's picks are contiguous for the
+          // combine, which sums them in pick order); the shared expert
+          // (every token once): straight into y
           const int drow = tl.m * BM + quarter * 32 + lane;
           if (tl.group < a.E) {
-            float* ocol = a.osort + (size_t)(tl.row0 + col0) * a.d + drow;
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
+              const int pk = __shfl_sync(0xffffffffu, tokc, jj);
               const float w = __shfl_sync(0xffffffffu, wc, jj);
-              if (col0 + jj < tl.nlen) ocol[(size_t)jj * a.d] = __uint_as_float(r[jj]) * w;
+              if (col0 + jj < tl.nlen) a.osort[(size_t)pk * a.d + drow] = __uint_as_float(r[jj]) * w;
             }
           } else {
 #pragma unroll
@@ -791,7 +795,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(PrefillCombineArgs
     float4 o[kMaxTopK];
 #pragma unroll
     for (int kk = 0; kk < kMaxTopK; ++kk)
-      if (kk < a.k) o[kk] = __ldcs(reinterpret_cast<const float4*>(a.osort + (size_t)a.inv[t * a.k + kk] * a.d) + c);
+      if (kk < a.k) o[kk] = __ldcs(reinterpret_cast<const float4*>(a.osort + ((size_t)t * a.k + kk) * a.d) + c);
 #pragma unroll
     for (int kk = 0; kk < kMaxTopK; ++kk) {
       if (kk < a.k) {
