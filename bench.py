@@ -234,6 +234,67 @@ def run_prefill(steps, warmup, sweep=(4096, 6144, 8192, 12288, 16384)):
     return out
 
 
+# -------------------------------------------------------- KV-streaming window --
+def run_kv_window(steps=20, warmup=3, n_layers=2):
+    """KV-streaming window (NEXT-4): per layer 131,072 cells of 1,056 B, the
+    first 32,768 in VRAM and the rest in page-locked host memory.  A step
+    reads every block of every layer once (a dense attention read; the pages
+    do not give which blocks their sparse attention reads), resident blocks
+    from HBM, the others straight from host memory.  Bound: the host part at
+    the measured host->device rate, the HBM part (window read + all blocks
+    written) at the measured HBM rate, whichever is longer."""
+    import torch
+    from moe_inputs.kv import KV_BLOCK_CELLS, KV_CELL_BYTES, KV_CONTEXT_CELLS, KV_RESIDENT_CELLS, kv_cells
+    from expert_cached_decode_gb300.layer import KVWindow
+    n, R, cb, bc = KV_CONTEXT_CELLS, KV_RESIDENT_CELLS, KV_CELL_BYTES, KV_BLOCK_CELLS
+    host = torch.empty(n_layers * (n - R) * cb, dtype=torch.uint8, pin_memory=True)
+    kv = KVWindow(n_layers, n, R, cb, bc, host)
+    try:
+        for l in range(n_layers):
+            src = torch.from_numpy(kv_cells(0, l, n, cb)).cuda()
+            kv.moe_kv_write(l, 0, src)
+            torch.cuda.synchronize()
+            del src
+        nb = n // bc
+        ids = torch.arange(nb, dtype=torch.int32, device="cuda")
+        dst = torch.empty((nb, bc * cb), dtype=torch.uint8, device="cuda")
+        stream = torch.cuda.current_stream()
+        def step():
+            for l in range(n_layers):
+                kv.moe_kv_read_blocks(l, ids, dst, stream)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        r0, h0 = kv.moe_kv_stats()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        r1, h1 = kv.moe_kv_stats()
+        host_bytes = n_layers * (n - R) * cb
+        hbm_bytes = n_layers * (R * cb + n * cb)   # window read + every block written
+        h2d = measure_h2d_gbs()
+        hbm, kind = peaks()
+        t_bound = max(host_bytes / (h2d * 1e9), hbm_bytes / (hbm * 1e9))
+        return {"workload": f"kv-window: {n_layers} layers x {n:,} cells x {cb} B, first {R:,} cells of each in "
+                            f"VRAM, blocks of {bc} cells, every block read once per step",
+                "ms_per_step": ms, "blocks_per_step": n_layers * nb,
+                "block_hit_rate": (h1 - h0) / max(1, r1 - r0),
+                "host_gbs": host_bytes / (ms / 1e3) / 1e9, "total_gbs": n_layers * n * cb / (ms / 1e3) / 1e9,
+                "h2d_gbs_measured": h2d,
+                "roofline": {"bound": "h2d" if host_bytes / h2d >= hbm_bytes / hbm else "hbm",
+                             "bound_ms": t_bound * 1e3, "frac": t_bound * 1e3 / ms,
+                             "note": "host part at the measured cudaMemcpy H2D rate (expert-sized copies from "
+                                     "pinned memory), HBM part (window read + blocks written) at "
+                                     f"MEASURED_PEAKS.json hbm_gbs ({kind})"},
+                "gpu_launches_per_step": n_layers}
+    finally:
+        kv.close()
+
+
 # ------------------------------------------------------------ 48-layer stack --
 def _draw_layer_tokens(args):
     cfg_id, lam, layer, calls, T = args
@@ -707,6 +768,11 @@ def run_gpu(args):
                                                     else (False,))]
             except Exception as ex:   # reported, not hidden
                 line["stack"] = {"error": str(ex)[:300]}
+        if args.kv and T == 1 and CALLS == DEFAULT_CALLS:
+            try:
+                line["kv_window"] = run_kv_window()
+            except Exception as ex:   # reported, not hidden
+                line["kv_window"] = {"error": str(ex)[:300]}
         if not args.no_cpu_baseline and T == 1:
             n = args.cpu_calls
             ra = cpu_oracle_all_cores(n)
@@ -750,6 +816,10 @@ def main():
     ap.add_argument("--stack-sweep", type=int, default=0, metavar="CALLS",
                     help="verify width (T = 1, 4, 7) x cache capacity (9,057 / 8,445 / 6,144) sweep on the "
                          "verify stack, CALLS calls per pass")
+    ap.add_argument("--kv", action="store_true", default=True,
+                    help="also time the KV-streaming window (dense block reads of two 131,072-cell layers)")
+    ap.add_argument("--no-kv", dest="kv", action="store_false")
+    ap.add_argument("--kv-only", action="store_true", help="time only the KV-streaming window")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="time only the prefill path at T tokens (profiling runs)")
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="T",
@@ -765,6 +835,10 @@ def main():
         # the step runs on one GPU by scope; there is no multi-GPU arm
         print(f"bench.py: single GPU only (got --gpus {args.gpus}, WORLD_SIZE {_dist()[0]})", file=sys.stderr)
         sys.exit(2)
+    elif args.kv_only:
+        import torch
+        torch.cuda.set_device(_dist()[2])
+        print(json.dumps({"kv_window": run_kv_window(args.steps, args.warmup)}), flush=True)
     elif args.prefill_only:
         import torch
         torch.cuda.set_device(_dist()[2])

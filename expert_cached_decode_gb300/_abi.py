@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_OOM", -3: "
 ENTRY_POINTS = ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                 "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_layer_destroy",
                 "moe_route_topk_noalloc", "moe_set_miss_mode", "moe_debug_inject_failure",
-                "moe_debug_set_wait_limit", "moe_last_error", "moe_pack_experts", "moe_forward_ahead")
+                "moe_debug_set_wait_limit", "moe_last_error", "moe_pack_experts", "moe_forward_ahead",
+                "moe_kv_create", "moe_kv_write", "moe_kv_read_blocks", "moe_kv_stats", "moe_kv_destroy")
 
 MOE_MISS_HOST_COPY = 0
 MOE_MISS_DEVICE_PULL = 1
@@ -40,6 +41,12 @@ class MoeLayerDesc(ctypes.Structure):
 
 MOE_POOL_CANONICAL = 0
 MOE_POOL_DEVICE = 1
+
+
+class MoeKvDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("cell_bytes", ctypes.c_int32), ("n_cells", ctypes.c_int64),
+                ("resident_cells", ctypes.c_int64), ("block_cells", ctypes.c_int32),
+                ("host_cells", ctypes.c_void_p)]
 
 
 class MoeStats(ctypes.Structure):
@@ -88,12 +95,19 @@ def load():
     L.moe_debug_set_wait_limit.argtypes = [vp, i64]
     L.moe_pack_experts.argtypes = [vp, vp, i64, i32, i32, vp]
     L.moe_forward_ahead.argtypes = [vp, i32, vp, i32, vp, vp, ctypes.POINTER(MoeTrace), i32, vp]
+    L.moe_kv_create.argtypes = [ctypes.POINTER(MoeKvDesc), ctypes.POINTER(vp)]
+    L.moe_kv_write.argtypes = [vp, i32, i64, i64, vp, vp]
+    L.moe_kv_read_blocks.argtypes = [vp, i32, vp, i32, vp, vp]
+    L.moe_kv_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    L.moe_kv_destroy.argtypes = [vp]
+    L.moe_kv_destroy.restype = None
     L.moe_last_error.argtypes = []
     L.moe_last_error.restype = ctypes.c_char_p
     for name in ("moe_layer_create", "moe_cache_configure", "moe_route_topk", "moe_forward",
                  "moe_sync", "moe_cache_stats", "moe_cache_export", "moe_route_topk_noalloc",
                  "moe_set_miss_mode", "moe_debug_inject_failure", "moe_debug_set_wait_limit",
-                 "moe_pack_experts", "moe_forward_ahead"):
+                 "moe_pack_experts", "moe_forward_ahead", "moe_kv_create", "moe_kv_write",
+                 "moe_kv_read_blocks", "moe_kv_stats"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

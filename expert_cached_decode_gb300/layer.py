@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 from . import _abi
-from ._abi import MoeLayerDesc, MoeStats, MoeTrace, check
+from ._abi import MoeKvDesc, MoeLayerDesc, MoeStats, MoeTrace, check
 
 
 def _ptr(a):
@@ -163,3 +163,50 @@ def moe_pack_experts(src, dst, n, d, f, stream=None):
     Asynchronous on `stream`."""
     L = _abi.load()
     check(L.moe_pack_experts(_ptr(src), _ptr(dst), int(n), int(d), int(f), _stream(stream)), "moe_pack_experts")
+
+
+class KVWindow:
+    """Binding of the KV-streaming window (moe_kv_*): per layer the first
+    resident_cells cells in VRAM, the rest in `host_cells` (a page-locked
+    uint8 tensor or array of n_layers * (n_cells - resident_cells) *
+    cell_bytes bytes that must outlive the window)."""
+
+    def __init__(self, n_layers, n_cells, resident_cells, cell_bytes, block_cells, host_cells):
+        self._lib = _abi.load()
+        self._keep = host_cells
+        desc = MoeKvDesc(n_layers=n_layers, cell_bytes=cell_bytes, n_cells=n_cells, resident_cells=resident_cells,
+                         block_cells=block_cells, host_cells=_ptr(host_cells))
+        kv = ctypes.c_void_p()
+        check(self._lib.moe_kv_create(ctypes.byref(desc), ctypes.byref(kv)), "moe_kv_create")
+        self.kv = kv
+        self.n_layers, self.n_cells, self.resident_cells = n_layers, n_cells, resident_cells
+        self.cell_bytes, self.block_cells = cell_bytes, block_cells
+
+    def moe_kv_write(self, layer, first_cell, src, stream=None):
+        """Cells [first_cell, first_cell + len(src)) of `layer` from src [n, cell_bytes] uint8 (device or pinned)."""
+        check(self._lib.moe_kv_write(self.kv, int(layer), int(first_cell), int(src.shape[0]), _ptr(src),
+                                     _stream(stream)), "moe_kv_write")
+
+    def moe_kv_read_blocks(self, layer, block_ids, dst, stream=None):
+        """dst[i] <- block block_ids[i] (device int32 ids; dst [n, block_cells * cell_bytes] uint8, device)."""
+        check(self._lib.moe_kv_read_blocks(self.kv, int(layer), _ptr(block_ids), int(block_ids.shape[0]), _ptr(dst),
+                                           _stream(stream)), "moe_kv_read_blocks")
+
+    def moe_kv_stats(self):
+        """(block reads, block reads served from VRAM) since create; synchronises."""
+        r, h = ctypes.c_int64(), ctypes.c_int64()
+        check(self._lib.moe_kv_stats(self.kv, ctypes.byref(r), ctypes.byref(h)), "moe_kv_stats")
+        return int(r.value), int(h.value)
+
+    def moe_kv_destroy(self):
+        if self.kv is not None and self.kv.value:
+            self._lib.moe_kv_destroy(self.kv)
+        self.kv = None
+
+    close = moe_kv_destroy
+
+    def __del__(self):
+        try:
+            self.moe_kv_destroy()
+        except Exception:
+            pass

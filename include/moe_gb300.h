@@ -290,6 +290,70 @@ const char* moe_last_error(void);
  * Errors: INVALID_ARG (shapes as for moe_layer_create, n < 0, NULL), CUDA. */
 moe_status moe_pack_experts(const void* src, void* dst, int64_t n, int32_t d, int32_t f, void* stream);
 
+/* ---- KV-streaming window (the attention side of the same engine) ---------
+ * Page "单卡5090跑125B 大模型", §2.1-§2.2 and §7.2: per QSA layer the engine
+ * keeps the first 32,768 of 131,072 KV cells (int8, 1,056 bytes per cell)
+ * in VRAM and streams the rest from page-locked host memory block by block,
+ * counting the share of block reads served from VRAM.  The window moves
+ * bytes only (a cell is opaque); which blocks a step reads is the caller's
+ * choice (the pages do not give the attention's block choice).
+ *
+ * A layer's cells 0 .. n_cells-1: cell c < resident_cells lives in the
+ * library's VRAM window, cell c >= resident_cells in the caller's host
+ * buffer at [layer][c - resident_cells].  Block b is cells
+ * [b*block_cells, (b+1)*block_cells); it hits VRAM when b*block_cells <
+ * resident_cells (resident_cells is a multiple of block_cells, so a block
+ * is wholly on one side). */
+typedef struct moe_kv moe_kv;   /* opaque, library-owned */
+
+typedef struct {
+  int32_t n_layers;        /* layers with a KV window (> 0) */
+  int32_t cell_bytes;      /* bytes per cell, a positive multiple of 16 */
+  int64_t n_cells;         /* cells per layer, a positive multiple of block_cells */
+  int64_t resident_cells;  /* the first cells of each layer held in VRAM: a multiple
+                              of block_cells in [0, n_cells] */
+  int32_t block_cells;     /* cells per block read (> 0) */
+  void* host_cells;        /* [n_layers][n_cells - resident_cells][cell_bytes] HOST
+                              memory owned by the caller, 16-byte aligned, valid
+                              until moe_kv_destroy; registered (cudaHostRegister)
+                              by the library when it is not page-locked.  May be
+                              NULL when resident_cells == n_cells. */
+} moe_kv_desc;
+
+/* Allocates the VRAM window (n_layers * resident_cells * cell_bytes) and the
+ * read counters; synchronous.  Errors: INVALID_ARG (sizes as above, host
+ * memory given as device memory), OOM, HOST_PIN (registration or mapping of
+ * host_cells failed), CUDA.  Nothing is left allocated on error. */
+moe_status moe_kv_create(const moe_kv_desc* desc, moe_kv** out);
+
+/* Writes cells [first_cell, first_cell + n) of `layer` from `src` (n *
+ * cell_bytes bytes, device or host memory): the resident part into the
+ * window, the rest into the host buffer; asynchronous on `stream`.
+ * Errors: INVALID_ARG (layer or cell range), CUDA. */
+moe_status moe_kv_write(moe_kv* kv, int32_t layer, int64_t first_cell, int64_t n, const void* src,
+                        void* stream);
+
+/* Block reads of one layer: dst[i] (block_cells * cell_bytes bytes, device
+ * memory, 16-byte aligned) <- block block_ids[i] (device int32 array of
+ * n_blocks ids, repeats allowed).  Resident blocks are read from VRAM, the
+ * others from the host buffer through its device mapping; one kernel launch,
+ * asynchronous on `stream`.  Adds n_blocks to the read counter and the
+ * resident ones to the hit counter.  An id outside [0, n_cells/block_cells)
+ * reads nothing (its dst block is left as it was) and is reported by the next
+ * moe_kv_stats.  Errors: INVALID_ARG (layer, n_blocks < 0, NULL or
+ * misaligned pointers), CUDA. */
+moe_status moe_kv_read_blocks(moe_kv* kv, int32_t layer, const int32_t* block_ids, int32_t n_blocks, void* dst,
+                              void* stream);
+
+/* Totals since create: block reads and the reads served from VRAM (either
+ * pointer may be NULL).  Synchronises the device.  Returns INVALID_ARG (once)
+ * if a read named a block outside the layer. */
+moe_status moe_kv_stats(moe_kv* kv, int64_t* block_reads, int64_t* block_hits);
+
+/* Frees the window and unregisters host_cells if the library registered it;
+ * synchronises the device.  NULL is a no-op. */
+void moe_kv_destroy(moe_kv* kv);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,3 +66,26 @@ def test_null_arguments_are_rejected_without_a_gpu(lib_path):
     assert L.moe_pack_experts(buf, buf, 1, 200, 64, None) == -1
     assert L.moe_pack_experts(buf, buf, 1, 256, 96, None) == -1
     assert L.moe_pack_experts(buf, buf, 0, 256, 64, None) == 0
+
+
+def test_kv_window_arguments_are_rejected_without_a_gpu(lib_path):
+    from expert_cached_decode_gb300 import _abi
+    L = _abi.load()
+    assert L.moe_kv_create(None, None) == -1
+    out = ctypes.c_void_p()
+    host = ctypes.create_string_buffer(4096 + 16)
+    base = ctypes.addressof(host) + (-ctypes.addressof(host)) % 16
+
+    def desc(**kw):
+        d = dict(n_layers=1, cell_bytes=64, n_cells=64, resident_cells=32, block_cells=8, host_cells=base)
+        d.update(kw)
+        return _abi.MoeKvDesc(**d)
+
+    for bad in (dict(n_layers=0), dict(cell_bytes=40), dict(block_cells=0), dict(n_cells=60),
+                dict(resident_cells=36), dict(resident_cells=72), dict(host_cells=None), dict(host_cells=base + 8)):
+        assert L.moe_kv_create(ctypes.byref(desc(**bad)), ctypes.byref(out)) == -1, bad
+        assert out.value is None
+    assert L.moe_kv_read_blocks(None, 0, None, 1, None, None) == -1
+    assert L.moe_kv_write(None, 0, 0, 1, None, None) == -1
+    assert L.moe_kv_stats(None, None, None) == -1
+    L.moe_kv_destroy(None)
