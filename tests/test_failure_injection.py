@@ -95,16 +95,18 @@ def _oracle_check(s, layer, xb):
     assert_close_rms(y.cpu().numpy(), oracle_y(ExpertMemo(s, s.wl.keys), 0, xb, idx, w))
 
 
-def test_router_wait_runs_out_and_the_context_recovers():
+@pytest.mark.parametrize("T", [1, 4])
+def test_router_wait_runs_out_and_the_context_recovers(T):
     # CTA 0 holds back its router logits: every CTA's wait for them runs out
     # after 20 ms, the kernel returns, moe_sync reports MOE_ERR_TIMEOUT, and
-    # the next call is correct again
+    # the next call is correct again (T = 1: the one-token selection, whose
+    # CTAs hand the producer its units right after selecting)
     lib = _abi.load()
     s, layer = _resident_tiny()
     try:
         layer.moe_debug_set_wait_limit(20_000_000)
-        xb = s.tokens_many(0, [3], T=4)[0]
-        y = torch.empty((4, s.wl.d), dtype=torch.float32, device="cuda")
+        xb = s.tokens_many(0, [3], T=T)[0]
+        y = torch.empty((T, s.wl.d), dtype=torch.float32, device="cuda")
         assert lib.moe_debug_inject_failure(_abi.MOE_INJECT_HOLD_ROUTER, 1) == 0
         layer.moe_forward(0, to_device_bf16(xb), y)      # asynchronous: no error yet
         with pytest.raises(MoeError) as ei:
